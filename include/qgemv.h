@@ -1,0 +1,219 @@
+/*
+ * qgemv.h -- C ABI of the GB300 (sm_103a) quantized GEMV / skinny GEMM library
+ * (libqgemv.so).
+ *
+ * What it computes (sources are web pages; cited by title and section):
+ *
+ *  qgemv_w4a16 / qgemm_w4a16_skinny
+ *    "MLX Runner: An Inference Engine You Can Read", section "Architecture:
+ *    one command buffer per token": each group of weights is stored as 4-bit
+ *    integer codes plus one scale and one bias, weight = scale x code + bias,
+ *    and the decode kernels multiply against the packed codes directly without
+ *    ever storing a dequantized copy. Section "Optimized against a known
+ *    ceiling": decode reads nearly every weight once, so it is bounded by
+ *    memory bandwidth. The skinny form (several activation rows sharing one
+ *    weight read) is the continuous batcher of "Krill Teardown", section
+ *    "Core mechanisms", and the 16-token tree verification of the Uzu article,
+ *    section "Producing several tokens from one model pass".
+ *
+ *  moe_mxfp4_expert_forward
+ *    "Running Kimi K3 (2.8T) on one Apple Silicon Mac" (Deltafin), section
+ *    "How it works": the router selects 16 experts per token and only those
+ *    experts' weights are read; section "Technical approach / compute": the
+ *    expert GEMV decodes MXFP4 (E2M1 codes, E8M0 block scale applied to the
+ *    fp32 exponent) in the same pass as the multiply.
+ *
+ *  hadamard32_quant_i8 / gemm_w8a8_i32
+ *    Uzu article, section "How Uzu optimizes bytes and tokens per pass":
+ *    activations are quantized to 8 bits at run time so both matmul operands
+ *    are integers; before quantization a block-diagonal randomized Hadamard
+ *    transform (random sign flips, then a +-1 Hadamard per 32-value block)
+ *    spreads outliers, and it is exactly invertible.
+ *
+ * Conventions shared by every entry point
+ *  - Every array pointer is a DEVICE pointer (global memory of the current
+ *    device). The caller allocates and owns all of them; the library never
+ *    allocates device memory and keeps no per-call state.
+ *  - Arrays are dense, row-major, contiguous. bf16 / fp16 arrays are passed as
+ *    their 16-bit patterns (uint16_t). uint32_t "words" hold packed codes.
+ *  - Every pointer must be 16-byte aligned (QG_ERR_MISALIGNED otherwise).
+ *  - Outputs must not alias inputs.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream). Work is enqueued asynchronously on it; the return value reports
+ *    host-side validation and launch errors only. Device-side timeouts of
+ *    bounded waits are reported by qg_device_error().
+ *  - Validation happens before anything is launched; on any error nothing is
+ *    enqueued and the outputs are untouched.
+ *  - Results are deterministic: the same inputs on the same device give
+ *    bit-identical outputs (no floating-point atomics).
+ *  - Accuracy: floating-point outputs y satisfy, per element,
+ *        |y - y_exact| <= 2e-3 * sum_k |x_k * w_k| + 1e-5
+ *    against the exact (float64) value from the same quantized inputs; the
+ *    integer outputs (int8 codes, int32 products, expert indices) are exact.
+ */
+#ifndef QGEMV_H
+#define QGEMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QG_API __attribute__((visibility("default")))
+#else
+#define QG_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QG_OK = 0,
+    QG_ERR_INVALID_ARG = 1,     /* null pointer, bad size or shape           */
+    QG_ERR_MISALIGNED = 2,      /* a pointer is not 16-byte aligned          */
+    QG_ERR_UNSUPPORTED = 3,     /* valid request this build does not handle  */
+    QG_ERR_WORKSPACE = 4,       /* workspace missing or too small            */
+    QG_ERR_CUDA = 5,            /* a CUDA runtime call or launch failed      */
+    QG_ERR_DEVICE_TIMEOUT = 6   /* a kernel's bounded wait gave up           */
+} qg_status;
+
+/* Static, human-readable name of a status. Never NULL. */
+QG_API const char *qg_status_string(qg_status s);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+QG_API int qg_version(void);
+
+/*
+ * qgemv_w4a16 -- y = W x for one activation row (M = 1), W stored as affine
+ * 4-bit groups ("MLX Runner ...", "Architecture: one command buffer per
+ * token").
+ *
+ *   wq         uint32 [N][K/8]: code k of row n is bits [4(k%8), 4(k%8)+3]
+ *              of wq[n][k/8] (eight codes per word, lowest nibble first).
+ *   scales_f16 fp16 [N][K/group_size]: scale s of (row n, group k/group_size).
+ *   biases_f16 fp16 [N][K/group_size]: bias b of the same group.
+ *   x_bf16     bf16 [K].
+ *   y          fp32 [N] (output): y[n] = sum_k (s * q[n][k] + b) * x[k].
+ *   group_size 64 (other sizes return QG_ERR_UNSUPPORTED).
+ *   K          multiple of group_size; N >= 1.
+ *   workspace  may be NULL when ws_bytes == 0; qg_gemv_workspace_size()
+ *              gives the size needed (currently 0 for every shape).
+ */
+QG_API qg_status qgemv_w4a16(const uint32_t *wq, const uint16_t *scales_f16,
+                      const uint16_t *biases_f16, const uint16_t *x_bf16, float *y,
+                      int N, int K, int group_size, void *workspace, size_t ws_bytes,
+                      void *stream);
+
+QG_API size_t qg_gemv_workspace_size(int N, int K, int group_size);
+
+/*
+ * qgemm_w4a16_skinny -- Y = X W^T for a few activation rows, each weight read
+ * once for all rows ("Krill Teardown", "Core mechanisms"; Uzu article,
+ * "Producing several tokens from one model pass").
+ *
+ *   wq, scales_f16, biases_f16, N, K, group_size: as qgemv_w4a16.
+ *   x_bf16  bf16 [M][K].
+ *   y       fp32 [M][N] (output): y[m][n] = sum_k (s q[n][k] + b) x[m][k].
+ *   M       1..32 (M = 1 is the same result as qgemv_w4a16).
+ *   workspace / ws_bytes: at least qg_skinny_workspace_size(M, N, K,
+ *           group_size) bytes of device memory, 16-byte aligned; the
+ *           contents need no initialization and are clobbered.
+ */
+QG_API qg_status qgemm_w4a16_skinny(const uint32_t *wq, const uint16_t *scales_f16,
+                             const uint16_t *biases_f16, const uint16_t *x_bf16,
+                             float *y, int M, int N, int K, int group_size,
+                             void *workspace, size_t ws_bytes, void *stream);
+
+QG_API size_t qg_skinny_workspace_size(int M, int N, int K, int group_size);
+
+/*
+ * moe_mxfp4_expert_forward -- routed-expert MoE layer with MXFP4 experts
+ * ("Running Kimi K3 ...", "How it works" and "Technical approach / compute").
+ *
+ *   x_bf16         bf16 [T][H] token activations.
+ *   router_logits  fp32 [T][E].
+ *   gate_q, up_q   uint8 [E][I][H/2]: E2M1 codes, two per byte, element 2j in
+ *                  the low nibble and 2j+1 in the high nibble.
+ *   gate_e8m0, up_e8m0 uint8 [E][I][H/32]: E8M0 block scale 2^(e-127) of
+ *                  each run of 32 codes along H (e = 255 is not allowed).
+ *   down_q         uint8 [E][H][I/2]; down_e8m0 uint8 [E][H][I/32].
+ *   T >= 1, H and I multiples of 64, 1 <= top_k <= E <= 1024, top_k <= 32.
+ *   y              fp32 [T][H] (output).
+ *   topk_idx       int32 [T][top_k] (output): the experts with the largest
+ *                  logits, in descending logit order, ties to the lower index.
+ *   topk_w         fp32 [T][top_k] (output): their softmax probabilities over
+ *                  all E experts (not renormalized over the top_k).
+ *   Computes, for token t and slot j with e = topk_idx[t][j], p = topk_w[t][j]:
+ *       g = Wg[e] x_t, u = Wu[e] x_t, h = silu(g) * u (kept in fp32),
+ *       y[t] = sum_j p * (Wd[e] h), the sum taken in slot order.
+ *   workspace      at least qg_moe_workspace_size(T, H, I, E, top_k) bytes,
+ *                  16-byte aligned; clobbered. The fp32 activations h of pair
+ *                  (t, j) are left at byte offset qg_moe_workspace_h_offset()
+ *                  as an array [T*top_k][I] (row t*top_k + j), for inspection.
+ */
+QG_API qg_status moe_mxfp4_expert_forward(const uint16_t *x_bf16, const float *router_logits,
+                                   const uint8_t *gate_q, const uint8_t *gate_e8m0,
+                                   const uint8_t *up_q, const uint8_t *up_e8m0,
+                                   const uint8_t *down_q, const uint8_t *down_e8m0,
+                                   int T, int H, int I, int E, int top_k,
+                                   float *y, int32_t *topk_idx, float *topk_w,
+                                   void *workspace, size_t ws_bytes, void *stream);
+
+QG_API size_t qg_moe_workspace_size(int T, int H, int I, int E, int top_k);
+QG_API size_t qg_moe_workspace_h_offset(int T, int H, int I, int E, int top_k);
+
+/*
+ * hadamard32_quant_i8 -- block-32 randomized Walsh-Hadamard transform and
+ * per-row symmetric int8 quantization (Uzu article, "How Uzu optimizes bytes
+ * and tokens per pass").
+ *
+ *   x_bf16     bf16 [M][K], K a multiple of 32, M >= 1.
+ *   sign_bits  uint32 [K/32]: bit j of word b set = negate element 32b+j
+ *              before the transform. Apply the same vector to the weights.
+ *   q          int8 [M][K] (output); scale fp32 [M] (output).
+ *   Per row m and block b, in fp32: v_j = +-x[m][32b+j]; the butterflies with
+ *   spans 1, 2, 4, 8, 16 map each pair (i, i+h) (bit h of i clear) to
+ *   (a + c, a - c) (unnormalized: H H^T = 32 I). Then s_m = max|z| / 127 and
+ *   q = clamp(rint(z / s_m), -127, 127) with round-half-even IEEE division;
+ *   an all-zero row gives s_m = 0 and q = 0. Codes are bit-exact.
+ *   Dequantization: x . w = (s_x s_w / 32) * sum_k q_x[k] q_w[k].
+ */
+QG_API qg_status hadamard32_quant_i8(const uint16_t *x_bf16, const uint32_t *sign_bits,
+                              int8_t *q, float *scale, int M, int K, void *stream);
+
+/*
+ * gemm_w8a8_i32 -- exact integer product C[m][n] = sum_k a[m][k] * w[n][k]
+ * (Uzu article, "How Uzu optimizes bytes and tokens per pass": int8 x int8 on
+ * the int8 matrix path, 16 verify rows).
+ *
+ *   a   int8 [M][K] (activation codes, e.g. from hadamard32_quant_i8).
+ *   w   int8 [N][K] (per-output-channel weight codes).
+ *   c   int32 [M][N] (output), exact.
+ *   1 <= M <= 32, K a multiple of 64 with K * 127 * 128 < 2^31.
+ */
+QG_API qg_status gemm_w8a8_i32(const int8_t *a, const int8_t *w, int32_t *c,
+                        int M, int N, int K, void *stream);
+
+/*
+ * qg_set_pdl -- process-wide launch mode. With enable != 0 every kernel is
+ * launched with programmatic dependent launch, so its weight streaming may
+ * start while the previous kernel on the stream is still draining. Activations
+ * and outputs are only touched after the dependency resolves, but WEIGHTS may
+ * be read early: enable it only when no work immediately preceding a call on
+ * the same stream writes that call's weight arrays. Default: off.
+ */
+QG_API void qg_set_pdl(int enable);
+
+/*
+ * qg_device_error -- the sticky device-side error word of the current device:
+ * 0 when no kernel has given up a bounded wait, otherwise a nonzero code
+ * naming where it gave up. Synchronizes the device. With clear != 0 the word
+ * is reset to 0. Returns QG_ERR_DEVICE_TIMEOUT when the word was nonzero.
+ */
+QG_API qg_status qg_device_error(uint32_t *code, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QGEMV_H */

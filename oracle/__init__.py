@@ -249,7 +249,7 @@ def dsilu(g):
 
 
 def moe_forward(x, logits, gate_q, gate_s, up_q, up_s, down_q, down_s, top_k,
-                tokens=None, threads=0, h_override=None):
+                tokens=None, threads=0, h_override=None, get_expert=None):
     """Routed-expert MoE forward for the selected tokens, float64.
 
     x bf16 bits [T][H]; logits fp32 [T][E]; gate/up codes [E][I][H/2] with
@@ -262,14 +262,15 @@ def moe_forward(x, logits, gate_q, gate_s, up_q, up_s, down_q, down_s, top_k,
     through SwiGLU and the down product (see tolerance notes in the tests).
     If h_override[(t, j)] is given, that h replaces the oracle's own h for the
     down product (stage-wise check of the down GEMV on the kernel's h).
+    get_expert(e) -> (gq, gs, uq, us, dq, ds) of expert e may replace the six
+    arrays (then pass None for them), so large expert sets stay off the host.
     """
     xs = _np(x, np.uint16)
     T, H = xs.shape
     idx, wts, _ = router(logits, top_k)
-    gq = _np(gate_q, np.uint8); gs = _np(gate_s, np.uint8)
-    uq = _np(up_q, np.uint8); us = _np(up_s, np.uint8)
-    dq = _np(down_q, np.uint8); ds = _np(down_s, np.uint8)
-    I = gq.shape[1]
+    if get_expert is None:
+        arrs = [_np(a, np.uint8) for a in (gate_q, gate_s, up_q, up_s, down_q, down_s)]
+        get_expert = lambda e: tuple(a[e] for a in arrs)  # noqa: E731
     if tokens is None:
         tokens = range(T)
     xf = (xs.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
@@ -281,8 +282,9 @@ def moe_forward(x, logits, gate_q, gate_s, up_q, up_s, down_q, down_s, top_k,
         for j in range(top_k):
             e = int(idx[t, j])
             p = float(wts[t, j])
-            g, ag, _ = mxfp4_gemv(gq[e], gs[e], xf[t], threads=threads)
-            u, au, _ = mxfp4_gemv(uq[e], us[e], xf[t], threads=threads)
+            gq, gs, uq, us, dq, ds = get_expert(e)
+            g, ag, _ = mxfp4_gemv(gq, gs, xf[t], threads=threads)
+            u, au, _ = mxfp4_gemv(uq, us, xf[t], threads=threads)
             tg = TOL_REL * ag + TOL_ABS
             tu = TOL_REL * au + TOL_ABS
             h = silu(g) * u
@@ -291,7 +293,7 @@ def moe_forward(x, logits, gate_q, gate_s, up_q, up_s, down_q, down_s, top_k,
             dh = (np.abs(dsilu(g) * u) * tg + np.abs(silu(g)) * tu
                   + 1.1 * tg * tu + 0.25 * tg * tg * np.abs(u))
             hin = h if h_override is None else np.asarray(h_override[(t, j)], np.float64)
-            o, ao, aw = mxfp4_gemv(dq[e], ds[e], hin, wv=dh, threads=threads)
+            o, ao, aw = mxfp4_gemv(dq, ds, hin, wv=dh, threads=threads)
             y += p * o
             yb += p * (TOL_REL * ao + TOL_ABS + aw) + 1e-6 * p * np.abs(o)
             out["g"][(t, j)] = g

@@ -1,0 +1,205 @@
+"""Python binding of libqgemv, the GB300 (sm_103a) quantized GEMV library.
+
+Thin ctypes marshalling over the C ABI in ``include/qgemv.h``: every function
+takes CUDA tensors, passes their device pointers and the current torch stream,
+and raises on a non-OK status. All arithmetic runs in the library's kernels;
+there is no fallback path. PyTorch only supplies device memory and streams.
+
+Entry points (same names as the C ABI):
+  qgemv_w4a16, qgemm_w4a16_skinny, moe_mxfp4_expert_forward,
+  hadamard32_quant_i8, gemm_w8a8_i32
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libqgemv.so")
+
+QG_OK = 0
+_STATUS = {0: "QG_OK", 1: "QG_ERR_INVALID_ARG", 2: "QG_ERR_MISALIGNED", 3: "QG_ERR_UNSUPPORTED",
+           4: "QG_ERR_WORKSPACE", 5: "QG_ERR_CUDA", 6: "QG_ERR_DEVICE_TIMEOUT"}
+
+EXPORTS = [
+    "qg_status_string", "qg_version", "qgemv_w4a16", "qg_gemv_workspace_size", "qgemm_w4a16_skinny",
+    "qg_skinny_workspace_size", "moe_mxfp4_expert_forward", "qg_moe_workspace_size",
+    "qg_moe_workspace_h_offset", "hadamard32_quant_i8", "gemm_w8a8_i32", "qg_set_pdl", "qg_device_error",
+]
+
+
+class QGError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {_STATUS.get(status, status)}")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libqgemv.so (built by build.py). Raises if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libqgemv.so is not built ({LIB_PATH}); run "
+                              "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.qg_status_string.restype = ctypes.c_char_p
+        L.qg_status_string.argtypes = [I]
+        L.qg_version.restype = I
+        L.qgemv_w4a16.restype = I
+        L.qgemv_w4a16.argtypes = [P, P, P, P, P, I, I, I, P, Z, P]
+        L.qg_gemv_workspace_size.restype = Z
+        L.qg_gemv_workspace_size.argtypes = [I, I, I]
+        L.qgemm_w4a16_skinny.restype = I
+        L.qgemm_w4a16_skinny.argtypes = [P, P, P, P, P, I, I, I, I, P, Z, P]
+        L.qg_skinny_workspace_size.restype = Z
+        L.qg_skinny_workspace_size.argtypes = [I, I, I, I]
+        L.moe_mxfp4_expert_forward.restype = I
+        L.moe_mxfp4_expert_forward.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, P, P, P, P, Z, P]
+        L.qg_moe_workspace_size.restype = Z
+        L.qg_moe_workspace_size.argtypes = [I, I, I, I, I]
+        L.qg_moe_workspace_h_offset.restype = Z
+        L.qg_moe_workspace_h_offset.argtypes = [I, I, I, I, I]
+        L.hadamard32_quant_i8.restype = I
+        L.hadamard32_quant_i8.argtypes = [P, P, P, P, I, I, P]
+        L.gemm_w8a8_i32.restype = I
+        L.gemm_w8a8_i32.argtypes = [P, P, P, I, I, I, P]
+        L.qg_set_pdl.restype = None
+        L.qg_set_pdl.argtypes = [I]
+        L.qg_device_error.restype = I
+        L.qg_device_error.argtypes = [P, I]
+        _lib = L
+    return _lib
+
+
+def _check(status: int, where: str):
+    if status != QG_OK:
+        raise QGError(status, where)
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, dtype_bytes, name):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.element_size() != dtype_bytes:
+        raise ValueError(f"{name} must have {dtype_bytes}-byte elements")
+
+
+def set_pdl(enable: bool):
+    lib().qg_set_pdl(1 if enable else 0)
+
+
+def device_error(clear: bool = True) -> int:
+    code = ctypes.c_uint32(0)
+    lib().qg_device_error(ctypes.byref(code), 1 if clear else 0)
+    return code.value
+
+
+def qgemv_w4a16(wq, scales, biases, x, y=None, workspace=None, stream=None):
+    """y[n] = sum_k (s q + b) x[k]; wq int32 [N][K/8], scales/biases fp16
+    [N][K/64], x bf16 [K] -> y fp32 [N]."""
+    N, K8 = wq.shape
+    K = K8 * 8
+    for t, b, n in ((wq, 4, "wq"), (scales, 2, "scales"), (biases, 2, "biases"), (x, 2, "x")):
+        _need(t, b, n)
+    if y is None:
+        y = torch.empty(N, device=wq.device, dtype=torch.float32)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().qgemv_w4a16(_p(wq), _p(scales), _p(biases), _p(x), _p(y), N, K, K // scales.shape[1],
+                             _p(workspace), ws_bytes, _stream(stream)), "qgemv_w4a16")
+    return y
+
+
+def qgemm_w4a16_skinny(wq, scales, biases, x, y=None, workspace=None, stream=None):
+    """Y[m][n] = sum_k (s q + b) X[m][k]; X bf16 [M][K] -> Y fp32 [M][N]."""
+    N, K8 = wq.shape
+    K = K8 * 8
+    M = x.shape[0]
+    for t, b, n in ((wq, 4, "wq"), (scales, 2, "scales"), (biases, 2, "biases"), (x, 2, "x")):
+        _need(t, b, n)
+    if y is None:
+        y = torch.empty(M, N, device=wq.device, dtype=torch.float32)
+    need = lib().qg_skinny_workspace_size(M, N, K, K // scales.shape[1])
+    if workspace is None and need:
+        workspace = torch.empty(need, device=wq.device, dtype=torch.uint8)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().qgemm_w4a16_skinny(_p(wq), _p(scales), _p(biases), _p(x), _p(y), M, N, K,
+                                    K // scales.shape[1], _p(workspace), ws_bytes, _stream(stream)),
+           "qgemm_w4a16_skinny")
+    return y
+
+
+def moe_workspace_size(T, H, I, E, top_k):
+    return lib().qg_moe_workspace_size(T, H, I, E, top_k)
+
+
+def moe_workspace_h_offset(T, H, I, E, top_k):
+    return lib().qg_moe_workspace_h_offset(T, H, I, E, top_k)
+
+
+def moe_mxfp4_expert_forward(x, logits, gate_q, gate_s, up_q, up_s, down_q, down_s, top_k,
+                             y=None, topk_idx=None, topk_w=None, workspace=None, stream=None):
+    """Routed MXFP4 expert MoE. x bf16 [T][H], logits fp32 [T][E], gate/up codes
+    uint8 [E][I][H/2] + scales [E][I][H/32], down codes [E][H][I/2] + scales
+    [E][H][I/32]. Returns (y fp32 [T][H], topk_idx int32 [T][k], topk_w fp32)."""
+    T, H = x.shape
+    E = logits.shape[1]
+    I = gate_q.shape[1]
+    dev = x.device
+    if y is None:
+        y = torch.empty(T, H, device=dev, dtype=torch.float32)
+    if topk_idx is None:
+        topk_idx = torch.empty(T, top_k, device=dev, dtype=torch.int32)
+    if topk_w is None:
+        topk_w = torch.empty(T, top_k, device=dev, dtype=torch.float32)
+    need = moe_workspace_size(T, H, I, E, top_k)
+    if workspace is None:
+        workspace = torch.empty(need, device=dev, dtype=torch.uint8)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().moe_mxfp4_expert_forward(_p(x), _p(logits), _p(gate_q), _p(gate_s), _p(up_q), _p(up_s),
+                                          _p(down_q), _p(down_s), T, H, I, E, top_k, _p(y), _p(topk_idx),
+                                          _p(topk_w), _p(workspace), ws_bytes, _stream(stream)),
+           "moe_mxfp4_expert_forward")
+    return y, topk_idx, topk_w
+
+
+def hadamard32_quant_i8(x, sign_bits, q=None, scale=None, stream=None):
+    """x bf16 [M][K], sign_bits int32 [K/32] -> (q int8 [M][K], scale fp32 [M])."""
+    M, K = x.shape
+    _need(x, 2, "x")
+    _need(sign_bits, 4, "sign_bits")
+    if q is None:
+        q = torch.empty(M, K, device=x.device, dtype=torch.int8)
+    if scale is None:
+        scale = torch.empty(M, device=x.device, dtype=torch.float32)
+    _check(lib().hadamard32_quant_i8(_p(x), _p(sign_bits), _p(q), _p(scale), M, K, _stream(stream)),
+           "hadamard32_quant_i8")
+    return q, scale
+
+
+def gemm_w8a8_i32(a, w, c=None, stream=None):
+    """a int8 [M][K], w int8 [N][K] -> c int32 [M][N] = a @ w^T (exact)."""
+    M, K = a.shape
+    N = w.shape[0]
+    _need(a, 1, "a")
+    _need(w, 1, "w")
+    if c is None:
+        c = torch.empty(M, N, device=a.device, dtype=torch.int32)
+    _check(lib().gemm_w8a8_i32(_p(a), _p(w), _p(c), M, N, K, _stream(stream)), "gemm_w8a8_i32")
+    return c

@@ -1,0 +1,206 @@
+// C entry points of libqgemv (declared in include/qgemv.h): argument
+// validation, variant selection and launch on the caller's stream.
+//
+// Validation happens entirely on the host before any launch, following the
+// rule of "MLX Runner: An Inference Engine You Can Read", section "Untrusted
+// input, verified output": malformed requests are rejected with a clear error
+// and nothing reaches the GPU.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "qg_common.cuh"
+#include "qg_internal.h"
+#include "qgemv.h"
+
+namespace {
+
+// Sticky device error word (one per device context, static device memory).
+__device__ uint32_t g_qg_device_error;
+
+constexpr int kMaxDevices = 64;
+uint32_t* g_err_ptr[kMaxDevices] = {};
+std::mutex g_err_mu;
+
+// Device address of the error word for the current device (looked up once).
+uint32_t* err_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_err_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_qg_device_error) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+qg_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QG_OK : QG_ERR_CUDA; }
+
+bool g_pdl = false;  // programmatic dependent launch for every kernel (see qg_set_pdl)
+
+}  // namespace
+
+namespace qg {
+int device_sm_count() {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms;
+}
+}  // namespace qg
+
+extern "C" {
+
+const char* qg_status_string(qg_status s) {
+  switch (s) {
+    case QG_OK: return "QG_OK";
+    case QG_ERR_INVALID_ARG: return "QG_ERR_INVALID_ARG: null pointer, bad size or shape";
+    case QG_ERR_MISALIGNED: return "QG_ERR_MISALIGNED: a pointer is not 16-byte aligned";
+    case QG_ERR_UNSUPPORTED: return "QG_ERR_UNSUPPORTED: valid request this build does not handle";
+    case QG_ERR_WORKSPACE: return "QG_ERR_WORKSPACE: workspace missing or too small";
+    case QG_ERR_CUDA: return "QG_ERR_CUDA: a CUDA runtime call or kernel launch failed";
+    case QG_ERR_DEVICE_TIMEOUT: return "QG_ERR_DEVICE_TIMEOUT: a kernel's bounded wait gave up";
+  }
+  return "QG_ERR_UNKNOWN";
+}
+
+int qg_version(void) { return 100; }
+
+// Process-wide switch: launch kernels with programmatic dependent launch so a
+// kernel's weight streaming may overlap the tail of the previous kernel on the
+// stream. Activations and outputs are only touched after the dependency wait,
+// but WEIGHTS may be read early: enable only when no kernel immediately before
+// a call writes that call's weights. Off by default.
+void qg_set_pdl(int enable) { g_pdl = enable != 0; }
+
+size_t qg_gemv_workspace_size(int N, int K, int group_size) {
+  (void)N;
+  (void)K;
+  (void)group_size;
+  return 0;
+}
+
+size_t qg_skinny_workspace_size(int M, int N, int K, int group_size) {
+  (void)M;
+  (void)N;
+  (void)K;
+  (void)group_size;
+  return 0;
+}
+
+static qg_status check_w4(const uint32_t* wq, const uint16_t* s, const uint16_t* b, const uint16_t* x,
+                          const float* y, int M, int N, int K, int group) {
+  if (!wq || !s || !b || !x || !y) return QG_ERR_INVALID_ARG;
+  if (M < 1 || M > 32 || N < 1 || K < 1) return QG_ERR_INVALID_ARG;
+  if (group != 64) return group == 32 || group == 128 ? QG_ERR_UNSUPPORTED : QG_ERR_INVALID_ARG;
+  if (K % group != 0) return QG_ERR_INVALID_ARG;
+  if ((long long)N * (K / 8) >= (1LL << 40)) return QG_ERR_INVALID_ARG;
+  if (!aligned16(wq) || !aligned16(s) || !aligned16(b) || !aligned16(x) || !aligned16(y)) return QG_ERR_MISALIGNED;
+  return QG_OK;
+}
+
+static qg_status run_w4(const uint32_t* wq, const uint16_t* s, const uint16_t* b, const uint16_t* x, float* y,
+                        int M, int N, int K, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (qg::gemv_fast_path_ok(M, N, K)) {
+    uint32_t* err = err_word();
+    if (!err) return QG_ERR_CUDA;
+    e = qg::launch_w4a16_fast(wq, s, b, x, y, M, N, K, err, st, g_pdl);
+  } else {
+    e = qg::launch_w4a16_generic(wq, s, b, x, y, M, N, K, st, g_pdl);
+  }
+  return from_cuda(e);
+}
+
+qg_status qgemv_w4a16(const uint32_t* wq, const uint16_t* scales_f16, const uint16_t* biases_f16,
+                      const uint16_t* x_bf16, float* y, int N, int K, int group_size, void* workspace,
+                      size_t ws_bytes, void* stream) {
+  qg_status st = check_w4(wq, scales_f16, biases_f16, x_bf16, y, 1, N, K, group_size);
+  if (st != QG_OK) return st;
+  if (ws_bytes < qg_gemv_workspace_size(N, K, group_size)) return QG_ERR_WORKSPACE;
+  if (ws_bytes && !workspace) return QG_ERR_INVALID_ARG;
+  return run_w4(wq, scales_f16, biases_f16, x_bf16, y, 1, N, K, stream);
+}
+
+qg_status qgemm_w4a16_skinny(const uint32_t* wq, const uint16_t* scales_f16, const uint16_t* biases_f16,
+                             const uint16_t* x_bf16, float* y, int M, int N, int K, int group_size,
+                             void* workspace, size_t ws_bytes, void* stream) {
+  qg_status st = check_w4(wq, scales_f16, biases_f16, x_bf16, y, M, N, K, group_size);
+  if (st != QG_OK) return st;
+  if (ws_bytes < qg_skinny_workspace_size(M, N, K, group_size)) return QG_ERR_WORKSPACE;
+  if (ws_bytes && !workspace) return QG_ERR_INVALID_ARG;
+  if (workspace && !aligned16(workspace)) return QG_ERR_MISALIGNED;
+  return run_w4(wq, scales_f16, biases_f16, x_bf16, y, M, N, K, stream);
+}
+
+size_t qg_moe_workspace_size(int T, int H, int I, int E, int top_k) {
+  if (T < 1 || H < 1 || I < 1 || E < 1 || top_k < 1) return 0;
+  return qg::moe_layout(T, H, I, E, top_k).total;
+}
+
+size_t qg_moe_workspace_h_offset(int T, int H, int I, int E, int top_k) {
+  if (T < 1 || H < 1 || I < 1 || E < 1 || top_k < 1) return 0;
+  return qg::moe_layout(T, H, I, E, top_k).h;
+}
+
+qg_status moe_mxfp4_expert_forward(const uint16_t* x_bf16, const float* router_logits, const uint8_t* gate_q,
+                                   const uint8_t* gate_e8m0, const uint8_t* up_q, const uint8_t* up_e8m0,
+                                   const uint8_t* down_q, const uint8_t* down_e8m0, int T, int H, int I, int E,
+                                   int top_k, float* y, int32_t* topk_idx, float* topk_w, void* workspace,
+                                   size_t ws_bytes, void* stream) {
+  if (!x_bf16 || !router_logits || !gate_q || !gate_e8m0 || !up_q || !up_e8m0 || !down_q || !down_e8m0 || !y ||
+      !topk_idx || !topk_w)
+    return QG_ERR_INVALID_ARG;
+  if (T < 1 || H < 64 || I < 64 || E < 1 || top_k < 1) return QG_ERR_INVALID_ARG;
+  if (H % 64 != 0 || I % 64 != 0 || top_k > E) return QG_ERR_INVALID_ARG;
+  if (E > 1024 || top_k > 32 || (long long)T * top_k > 2048) return QG_ERR_UNSUPPORTED;
+  const void* ptrs[] = {x_bf16, router_logits, gate_q, gate_e8m0, up_q, up_e8m0, down_q, down_e8m0,
+                        y,      topk_idx,      topk_w};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return QG_ERR_MISALIGNED;
+  if (!workspace || ws_bytes < qg_moe_workspace_size(T, H, I, E, top_k)) return QG_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return QG_ERR_MISALIGNED;
+  uint32_t* err = err_word();
+  if (!err) return QG_ERR_CUDA;
+  return from_cuda(qg::launch_moe_mxfp4(x_bf16, router_logits, gate_q, gate_e8m0, up_q, up_e8m0, down_q,
+                                        down_e8m0, T, H, I, E, top_k, y, topk_idx, topk_w, workspace, err,
+                                        static_cast<cudaStream_t>(stream), g_pdl));
+}
+
+qg_status hadamard32_quant_i8(const uint16_t* x_bf16, const uint32_t* sign_bits, int8_t* q, float* scale, int M,
+                              int K, void* stream) {
+  if (!x_bf16 || !sign_bits || !q || !scale) return QG_ERR_INVALID_ARG;
+  if (M < 1 || K < 32 || K % 32 != 0) return QG_ERR_INVALID_ARG;
+  if (K > 49152) return QG_ERR_UNSUPPORTED;
+  if (!aligned16(x_bf16) || !aligned16(sign_bits) || !aligned16(q) || !aligned16(scale)) return QG_ERR_MISALIGNED;
+  return from_cuda(qg::launch_hadamard32_quant_i8(x_bf16, sign_bits, q, scale, M, K,
+                                                  static_cast<cudaStream_t>(stream), g_pdl));
+}
+
+qg_status gemm_w8a8_i32(const int8_t* a, const int8_t* w, int32_t* c, int M, int N, int K, void* stream) {
+  if (!a || !w || !c) return QG_ERR_INVALID_ARG;
+  if (M < 1 || M > 32 || N < 1 || K < 64 || K % 64 != 0) return QG_ERR_INVALID_ARG;
+  if ((long long)K * 127 * 128 >= (1LL << 31)) return QG_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(w) || !aligned16(c)) return QG_ERR_MISALIGNED;
+  return from_cuda(qg::launch_w8a8_i32(a, w, c, M, N, K, static_cast<cudaStream_t>(stream), g_pdl));
+}
+
+qg_status qg_device_error(uint32_t* code, int clear) {
+  uint32_t* p = err_word();
+  if (!p) return QG_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, p, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return QG_ERR_CUDA;
+  if (clear && v) {
+    const uint32_t z = 0;
+    if (cudaMemcpy(p, &z, sizeof z, cudaMemcpyHostToDevice) != cudaSuccess) return QG_ERR_CUDA;
+  }
+  if (code) *code = v;
+  return v ? QG_ERR_DEVICE_TIMEOUT : QG_OK;
+}
+
+}  // extern "C"

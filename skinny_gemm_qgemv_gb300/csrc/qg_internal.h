@@ -1,0 +1,60 @@
+// Host-side internals of libqgemv: kernel launchers shared between the
+// translation units and the C entry points in api.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace qg {
+
+// Launch with cudaLaunchKernelEx; with pdl the launch carries the
+// programmatic-stream-serialization attribute so the kernel may begin while the
+// previous kernel on the stream drains (kernels call griddepcontrol.wait before
+// touching activations or outputs).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                          bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+int device_sm_count();
+
+// W4A16 (w4a16_gemv.cu, w4a16_tc.cu)
+bool gemv_fast_path_ok(int M, int N, int K);
+cudaError_t launch_w4a16_fast(const uint32_t* wq, const uint16_t* sc, const uint16_t* bi, const uint16_t* x,
+                              float* y, int M, int N, int K, uint32_t* err, cudaStream_t stream, bool pdl);
+cudaError_t launch_w4a16_generic(const uint32_t* wq, const uint16_t* sc, const uint16_t* bi, const uint16_t* x,
+                                 float* y, int M, int N, int K, cudaStream_t stream, bool pdl);
+
+// Hadamard + int8 (hadamard_i8.cu)
+cudaError_t launch_hadamard32_quant_i8(const uint16_t* x, const uint32_t* sign_bits, int8_t* q, float* scale,
+                                       int M, int K, cudaStream_t stream, bool pdl);
+
+// W8A8 (w8a8_i32.cu)
+cudaError_t launch_w8a8_i32(const int8_t* a, const int8_t* w, int32_t* c, int M, int N, int K,
+                            cudaStream_t stream, bool pdl);
+
+// MXFP4 MoE (moe_mxfp4.cu)
+struct MoeLayout {
+  size_t pair_expert, pair_weight, counts, offsets, active, order, nactive, xh, xexp, h, hh, hexp, partial;
+  size_t total;
+};
+MoeLayout moe_layout(int T, int H, int I, int E, int top_k);
+cudaError_t launch_moe_mxfp4(const uint16_t* x, const float* logits, const uint8_t* gq, const uint8_t* gs,
+                             const uint8_t* uq, const uint8_t* us, const uint8_t* dq, const uint8_t* ds, int T,
+                             int H, int I, int E, int top_k, float* y, int32_t* idx, float* wts, void* ws,
+                             uint32_t* err, cudaStream_t stream, bool pdl);
+
+}  // namespace qg

@@ -83,10 +83,24 @@ def affine_w4_encode(w: torch.Tensor, group: int = 64):
     return words.to(torch.int32).contiguous(), scale.contiguous(), bias.contiguous()
 
 
+def _chunked(R, C, std, seed, slot, device, encode, max_elems=1 << 28):
+    """Draw [R][C] ~ N(0, std) in row chunks from one generator and encode each
+    chunk, so peak memory stays bounded for multi-GB weight sets."""
+    g = gen(seed, slot, device)
+    rows = max(1, min(R, max_elems // max(C, 1)))
+    outs = []
+    for r0 in range(0, R, rows):
+        r1 = min(R, r0 + rows)
+        w = torch.randn(r1 - r0, C, generator=g, device=device, dtype=torch.float32) * std
+        outs.append(encode(w))
+        del w
+    return tuple(torch.cat([o[i] for o in outs], dim=0) if len(outs) > 1 else outs[0][i]
+                 for i in range(len(outs[0])))
+
+
 def w4_weights(N, K, seed, slot, device="cpu", group=64, std=0.02):
     """Weights ~ N(0, std) encoded as affine uint4 (see affine_w4_encode)."""
-    w = normal_f32((N, K), std, seed, slot, device)
-    return affine_w4_encode(w, group)
+    return _chunked(N, K, std, seed, slot, device, lambda w: affine_w4_encode(w, group))
 
 
 # --------------------------------------------------------------------------
@@ -134,8 +148,8 @@ def mxfp4_encode(w: torch.Tensor):
 
 
 def mxfp4_weights(R, C, seed, slot, device="cpu", std=0.02):
-    w = normal_f32((R, C), std, seed, slot, device)
-    return mxfp4_encode(w)
+    """Weights ~ N(0, std) encoded as MXFP4 (see mxfp4_encode)."""
+    return _chunked(R, C, std, seed, slot, device, mxfp4_encode)
 
 
 def router_logits(T, E, seed, slot, device="cpu"):

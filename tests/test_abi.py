@@ -1,0 +1,92 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every symbol the header declares, and rejects malformed requests before any
+launch (validation returns a status without touching the device)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import skinny_gemm_qgemv_gb300 as q
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qgemv.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from skinny_gemm_qgemv_gb300 import build
+    build.build()
+    return q.lib()
+
+
+def header_functions():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"^QG_API\s+[\w\s\*]*?\b(\w+)\s*\(", src, re.M)))
+
+
+def test_header_declares_the_boundary():
+    fns = header_functions()
+    for name in ["qgemv_w4a16", "qgemm_w4a16_skinny", "moe_mxfp4_expert_forward",
+                 "hadamard32_quant_i8", "gemm_w8a8_i32"]:
+        assert name in fns
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in header_functions():
+        assert hasattr(L, name), name
+    assert set(header_functions()) == set(q.EXPORTS)
+
+
+def test_status_strings(L):
+    for s in range(7):
+        assert L.qg_status_string(s)
+    assert L.qg_status_string(0) == b"QG_OK"
+    assert L.qg_version() >= 100
+
+
+A = 0x10000   # fake, 16-byte-aligned "device" addresses: never dereferenced,
+B = 0x20010   # because every call below fails validation first
+P = ctypes.c_void_p
+
+
+def test_w4a16_validation(L):
+    f = L.qgemv_w4a16
+    assert f(None, P(A), P(A), P(A), P(A), 16, 128, 64, None, 0, None) == 1
+    assert f(P(A), P(A), P(A), P(A), P(A), 0, 128, 64, None, 0, None) == 1
+    assert f(P(A), P(A), P(A), P(A), P(A), 16, 100, 64, None, 0, None) == 1     # K % 64
+    assert f(P(A), P(A), P(A), P(A), P(A), 16, 128, 32, None, 0, None) == 3     # group 32 later
+    assert f(P(A), P(A), P(A), P(A), P(A), 16, 128, 48, None, 0, None) == 1
+    assert f(P(A + 4), P(A), P(A), P(A), P(A), 16, 128, 64, None, 0, None) == 2
+    g = L.qgemm_w4a16_skinny
+    assert g(P(A), P(A), P(A), P(A), P(A), 33, 16, 128, 64, None, 0, None) == 1  # M > 32
+    assert g(P(A), P(A), P(A), P(A), P(A), 0, 16, 128, 64, None, 0, None) == 1
+    assert g(P(A), P(A), P(A), P(B + 2), P(A), 4, 16, 128, 64, None, 0, None) == 2
+
+
+def test_moe_validation(L):
+    f = L.moe_mxfp4_expert_forward
+    ptrs = [P(A)] * 8
+    outs = [P(A)] * 3
+    ws = L.qg_moe_workspace_size(1, 128, 128, 8, 2)
+    assert ws > 0
+    assert L.qg_moe_workspace_h_offset(1, 128, 128, 8, 2) < ws
+    assert f(*ptrs, 1, 128, 128, 8, 9, *outs, P(A), ws, None) == 1        # top_k > E
+    assert f(*ptrs, 1, 100, 128, 8, 2, *outs, P(A), ws, None) == 1        # H % 64
+    assert f(*ptrs, 1, 128, 128, 8, 2, *outs, P(A), ws - 1, None) == 4    # workspace
+    assert f(*ptrs, 1, 128, 128, 8, 2, *outs, None, ws, None) == 4
+    assert f(*ptrs, 1, 128, 128, 2048, 2, *outs, P(A), 1 << 30, None) == 3  # E > 1024
+    assert f(*([P(A)] * 7 + [P(A + 8)]), 1, 128, 128, 8, 2, *outs, P(A), ws, None) == 2
+    assert f(*([None] + [P(A)] * 7), 1, 128, 128, 8, 2, *outs, P(A), ws, None) == 1
+
+
+def test_hadamard_and_w8a8_validation(L):
+    h = L.hadamard32_quant_i8
+    assert h(P(A), P(A), P(A), P(A), 4, 100, None) == 1     # K % 32
+    assert h(P(A), P(A), P(A), P(A), 0, 128, None) == 1
+    assert h(P(A), P(A + 4), P(A), P(A), 4, 128, None) == 2
+    g = L.gemm_w8a8_i32
+    assert g(P(A), P(A), P(A), 16, 64, 96, None) == 1        # K % 64
+    assert g(P(A), P(A), P(A), 33, 64, 128, None) == 1       # M > 32
+    assert g(P(A), P(A), P(A), 16, 64, 1 << 20, None) == 1   # K too large for int32
+    assert g(P(A + 1), P(A), P(A), 16, 64, 128, None) == 2
