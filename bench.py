@@ -1,0 +1,603 @@
+#!/usr/bin/env python
+"""Benchmark: W4A16 GEMV achieved HBM GB/s and % of the GB300 roofline.
+
+One step = one token's decode layer stack of a dense 9B-class decoder at
+M = 1: 36 layers x (q 4096x4096, k/v 1024x4096, o 4096x4096, gate+up
+24576x4096, down 4096x12288) plus a 151936x4096 lm_head, W4A16 affine g64,
+each projection with its own bf16 activation vector (217 GEMV launches,
+4.27 GB of weights, scales, activations and outputs), issued as one CUDA graph.
+`value` = algorithmic bytes of the step / step time (inputs resident in HBM;
+the 4.27 GB working set is 33x the L2, so every step streams from HBM).
+
+Also reported in the same JSON line: the M = 16 stack (skinny form), the MXFP4
+MoE layer at T = 1 and 16, the block-32 Hadamard + int8 path and the W8A8
+int32 GEMM at 4096x4096 / 12288x4096, the single 1024x1024 GEMV, the
+end-to-end number through the public API with host buffers, the roofline of
+the dominant kernel, the CPU baseline (the oracle on the host cores) and the
+SM clocks sampled during the timed region.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs an independent replica of the stack ("replicas
+only": the path has no exchange step); value = bytes of all ranks / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "W4A16 GEMV achieved HBM GB/s and % of GB300 peak at M=1 and M=16"
+FALLBACK_HBM = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extras", action="store_true", help="only the M=1 stack")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--case", default=None, help="run one kernel case a few times (for ncu): " + ", ".join(CASES))
+    ap.add_argument("--reps", type=int, default=3)
+    return ap.parse_args()
+
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 0.0)), "measured"
+    return FALLBACK_HBM, 1900.0, "fallback"
+
+
+def w4_bytes(N, K, M=1):
+    return N * K // 2 + 2 * N * (K // 64) * 2 + M * (K * 2 + N * 4)
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.samples = []
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for t, line in self.samples:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((t, float(parts[1]), float(parts[2]), parts))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        inside = [r for r in rows if self.t0 and self.t1 and self.t0 - 0.05 <= r[0] <= self.t1 + 0.05]
+        use = inside if inside else rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in use:
+            for i, n in enumerate(names):
+                if r[3][5 + i].lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": sorted(reasons), "samples": len(use), "in_timed_region": bool(inside)}
+
+
+# --------------------------------------------------------------------------- helpers
+
+def capture(graph_fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        graph_fn()
+    return g
+
+
+def replay_timed(g, iters, stream, warmup=2):
+    """Replay `g` on `stream` (warm-up, then `iters` timed replays bracketed by
+    CUDA events on the same stream); seconds per replay."""
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g.replay()
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(iters):
+            g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / iters * 1e-3
+
+
+def time_graph(graph_fn, iters, stream):
+    g = capture(graph_fn, stream)
+    return replay_timed(g, iters, stream), g
+
+
+def build_stack(q, dev, M, layers=36, seed=1):
+    """Weights of the layer stack (4.26 GB) plus per-projection inputs."""
+    shapes = synth.stack_layer_shapes(layers)
+    mats = []
+    for i, (name, N, K) in enumerate(shapes):
+        wq, s, b = synth.w4_weights(N, K, seed=seed, slot=10 + i, device=dev)
+        mats.append((name, N, K, wq, s, b))
+    return mats
+
+
+def stack_io(mats, dev, M, seed=1):
+    xs, ys = [], []
+    for i, (name, N, K, *_r) in enumerate(mats):
+        xs.append(synth.bf16_normal((M, K), seed=seed, slot=5000 + i, device=dev))
+        ys.append(torch.empty(M, N, device=dev, dtype=torch.float32))
+    return xs, ys
+
+
+def run_stack(q, mats, xs, ys, M, stream):
+    for (name, N, K, wq, s, b), x, y in zip(mats, xs, ys):
+        if M == 1:
+            q.qgemv_w4a16(wq, s, b, x[0], y[0], stream=stream)
+        else:
+            q.qgemm_w4a16_skinny(wq, s, b, x, y, stream=stream)
+
+
+def kernel_traffic(kind, alg_bytes_avg):
+    """Per-launch DRAM traffic from the committed ncu summary, scaled to the
+    average launch of the step; None if the kernel source changed since."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kind)
+    if not d:
+        return None
+    src = os.path.join(ROOT, d["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != d["source_sha256"]:
+        return None
+    return d["dram_bytes_per_alg_byte"] * alg_bytes_avg
+
+
+# --------------------------------------------------------------------------- CPU baseline
+
+def cpu_sample_stack(div, seed=1):
+    """Every projection of the stack with ceil(N/div) rows (rows are i.i.d.)."""
+    out = []
+    for i, (name, N, K) in enumerate(synth.stack_layer_shapes()):
+        n = max(1, -(-N // div))
+        wq, s, b = synth.w4_weights(n, K, seed=seed + 100, slot=i)
+        x = synth.bf16_normal((1, K), seed=seed + 100, slot=5000 + i)
+        out.append((n, K, wq.numpy().view("uint32"), s.view(torch.int16).numpy().view("uint16"),
+                    b.view(torch.int16).numpy().view("uint16"), x.view(torch.int16).numpy().view("uint16")))
+    return out
+
+
+def run_cpu_sample(sample, budget_s=None):
+    import oracle
+    t0 = time.perf_counter()
+    nbytes = 0
+    done = 0
+    for (n, K, wq, s, b, x) in sample:
+        oracle.w4a16(wq, s, b, x)
+        nbytes += w4_bytes(n, K)
+        done += 1
+        if budget_s is not None and time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return nbytes, dt, done
+
+
+def cpu_baseline(seconds, mats=None, xs=None, stride=8):
+    """The oracle on the host cores over every `stride`-th row of every
+    projection of the stack (rows copied from the device-resident weights),
+    repeated until `seconds` of CPU time have elapsed."""
+    import oracle
+    oracle.build()
+    if mats is None:
+        sample = cpu_sample_stack(16)
+    else:
+        sample = []
+        for (name, N, K, wq, s, b), x in zip(mats, xs):
+            sel = torch.arange(0, N, stride, device=wq.device)
+            sample.append((len(sel), K, wq[sel].cpu().numpy().view("uint32"),
+                           s[sel].cpu().view(torch.int16).numpy().view("uint16"),
+                           b[sel].cpu().view(torch.int16).numpy().view("uint16"),
+                           x[:1].cpu().view(torch.int16).numpy().view("uint16")))
+    nbytes, dt, passes, done = 0, 0.0, 0, 0
+    while dt < seconds:
+        b, t, d = run_cpu_sample(sample, budget_s=seconds - dt)
+        nbytes += b
+        dt += t
+        done += d
+        passes += 1
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"float64 C oracle, every {stride}th output row of all 217 stack projections "
+                      f"({done} projection passes, {nbytes / 1e6:.0f} MB of algorithmic bytes in {dt:.1f} s)"}
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    div = 64
+    sample = cpu_sample_stack(div)
+    for _ in range(args.warmup):
+        run_cpu_sample(sample[:6])
+    total_b, total_t = 0, 0.0
+    for _ in range(args.steps):
+        b, t, _ = run_cpu_sample(sample)
+        total_b += b
+        total_t += t
+    v = total_b / total_t / 1e9
+    sample_desc = (f"each step: the float64 C oracle over all 217 projections of the stack with rows cut to "
+                   f"ceil(N/{div}) ({total_b / args.steps / 1e6:.0f} MB of algorithmic bytes)")
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_t / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "decode layer stack, 9B-class dense, W4A16 g64, M=1 (row-sampled)"},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
+                             "sample": sample_desc},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- extras
+
+def bench_single_gemv(q, dev, stream, l2_bytes):
+    N = K = 1024
+    per = w4_bytes(N, K)
+    copies = max(8, (4 * l2_bytes) // per + 1)
+    mats = [synth.w4_weights(N, K, seed=0, slot=i, device=dev) for i in range(copies)]
+    x = synth.bf16_normal((K,), 0, 99999, dev)
+    y = torch.empty(N, device=dev)
+
+    def fn():
+        for wq, s, b in mats:
+            q.qgemv_w4a16(wq, s, b, x, y, stream=stream)
+    t, _ = time_graph(fn, 5, stream)
+    t /= copies
+    return {"us_per_call": t * 1e6, "GB_per_s": per / t / 1e9, "weight_copies_rotated": int(copies)}
+
+
+def bench_moe(q, dev, stream, T, moe_w):
+    E, H, I, k = 384, 7168, 2048, 16
+    x = synth.bf16_normal((T, H), 3, 0, dev)
+    lg = synth.router_logits(T, E, 3, 1, dev)
+    ws = torch.empty(q.moe_workspace_size(T, H, I, E, k), dtype=torch.uint8, device=dev)
+    y = torch.empty(T, H, device=dev)
+    idx = torch.empty(T, k, dtype=torch.int32, device=dev)
+    wt = torch.empty(T, k, device=dev)
+
+    def fn():
+        q.moe_mxfp4_expert_forward(x, lg, *moe_w, top_k=k, y=y, topk_idx=idx, topk_w=wt, workspace=ws,
+                                   stream=stream)
+    t, _ = time_graph(fn, 20, stream)
+    D = int(torch.unique(idx).numel())
+    per_expert = 3 * (H * I // 2 + H * I // 32)
+    nbytes = D * per_expert + T * (2 * H + 4 * E + 4 * H)
+    return {"us_per_call": t * 1e6, "GB_per_s": nbytes / t / 1e9, "distinct_experts": D,
+            "algorithmic_bytes": nbytes}
+
+
+def bench_w8a8(q, dev, stream, N, l2_bytes):
+    K, M = 4096, 16
+    wf = synth.normal_f32((N, K), 0.02, 4, 20, dev).to(torch.bfloat16)
+    sb = synth.sign_bits(K, 4, 5, dev)
+    wq, _ = q.hadamard32_quant_i8(wf, sb)
+    copies = max(4, (4 * l2_bytes) // (N * K) + 1)
+    ws = [wq.clone() for _ in range(copies)]
+    xa = synth.outlier_activations(M, K, 4, 0, dev)
+    qa, sa = q.hadamard32_quant_i8(xa, sb)
+    c = torch.empty(M, N, dtype=torch.int32, device=dev)
+
+    def fn():
+        for w in ws:
+            q.gemm_w8a8_i32(qa, w, c, stream=stream)
+    t, _ = time_graph(fn, 5, stream)
+    t /= copies
+    nbytes = N * K + M * K + M * N * 4
+
+    def fh():
+        for _ in range(50):
+            q.hadamard32_quant_i8(xa, sb, qa, sa, stream=stream)
+    th, _ = time_graph(fh, 3, stream)
+    return {"us_per_call": t * 1e6, "GB_per_s": nbytes / t / 1e9, "weight_copies_rotated": int(copies),
+            "hadamard_quant_us_per_call": th / 50 * 1e6}
+
+
+# --------------------------------------------------------------------------- single cases (profiling)
+
+CASES = ["gemv_lm_head", "gemv_down", "gemv_q", "skinny16_gate_up", "skinny16_down", "moe_T1", "moe_T16",
+         "w8a8_12288", "hadamard_16x4096"]
+
+
+def run_case(args):
+    """One kernel on one full-size (or, for the MoE, reduced-E) input; warm-up
+    launches then `reps` launches. Small device footprint, for ncu captures."""
+    import skinny_gemm_qgemv_gb300 as q
+    q.lib()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    c = args.case
+    if c.startswith("gemv_") or c.startswith("skinny16_"):
+        shape = {"lm_head": (151936, 4096), "down": (4096, 12288), "q": (4096, 4096),
+                 "gate_up": (24576, 4096)}[c.split("_", 1)[1]]
+        M = 1 if c.startswith("gemv_") else 16
+        N, K = shape
+        wq, s, b = synth.w4_weights(N, K, 1, 0, dev)
+        x = synth.bf16_normal((M, K), 1, 1, dev)
+        y = torch.empty(M, N, device=dev)
+        f = (lambda: q.qgemv_w4a16(wq, s, b, x[0], y[0])) if M == 1 else \
+            (lambda: q.qgemm_w4a16_skinny(wq, s, b, x, y))
+        nbytes = w4_bytes(N, K, M)
+    elif c.startswith("moe_"):
+        T = int(c[5:])
+        E, H, I, k = 64, 7168, 2048, 16
+        gq, gs = synth.mxfp4_weights(E * I, H, 3, 2, dev)
+        uq, us = synth.mxfp4_weights(E * I, H, 3, 3, dev)
+        dq, ds = synth.mxfp4_weights(E * H, I, 3, 4, dev)
+        w = [t.reshape(E, r, -1) for t, r in ((gq, I), (gs, I), (uq, I), (us, I), (dq, H), (ds, H))]
+        x = synth.bf16_normal((T, H), 3, 0, dev)
+        lg = synth.router_logits(T, E, 3, 1, dev)
+        f = lambda: q.moe_mxfp4_expert_forward(x, lg, *w, top_k=k)  # noqa: E731
+        nbytes = None
+    elif c == "w8a8_12288":
+        N, K = 12288, 4096
+        a = torch.randint(-127, 128, (16, K), dtype=torch.int8, device=dev)
+        w = torch.randint(-127, 128, (N, K), dtype=torch.int8, device=dev)
+        f = lambda: q.gemm_w8a8_i32(a, w)  # noqa: E731
+        nbytes = N * K + 16 * K + 16 * N * 4
+    elif c == "hadamard_16x4096":
+        x = synth.outlier_activations(16, 4096, 4, 0, dev)
+        sb = synth.sign_bits(4096, 4, 5, dev)
+        f = lambda: q.hadamard32_quant_i8(x, sb)  # noqa: E731
+        nbytes = 16 * 4096 * 3
+    else:
+        raise SystemExit(f"unknown case {c}")
+    for _ in range(3):
+        f()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.reps):
+        f()
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) * 1e-3 / args.reps
+    print(json.dumps({"case": c, "us_per_call": t * 1e6,
+                      "GB_per_s": None if nbytes is None else nbytes / t / 1e9}), flush=True)
+    assert q.device_error() == 0
+
+
+# --------------------------------------------------------------------------- main
+
+def main():
+    args = parse()
+    if args.case:
+        return run_case(args)
+    rank, world, local = dist_info()
+    if world > 1 and not torch.distributed.is_initialized():
+        backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
+        torch.distributed.init_process_group(backend)
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    import skinny_gemm_qgemv_gb300 as q
+    q.lib()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    hbm_peak, _, peak_src = peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    q.set_pdl(True)
+
+    # ---------------- config: the M = 1 layer stack
+    with torch.cuda.stream(stream):
+        mats = build_stack(q, dev, 1)
+        xs, ys = stack_io(mats, dev, 1)
+    torch.cuda.synchronize()
+    step_bytes = sum(w4_bytes(N, K) for (_, N, K, *_r) in mats)
+    launches = len(mats)
+
+    g = capture(lambda: run_stack(q, mats, xs, ys, 1, stream), stream)
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            g.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    clocks.mark("t0")
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    clocks.mark("t1")
+    if world > 1:
+        torch.distributed.barrier()
+    t_step = e0.elapsed_time(e1) * 1e-3 / args.steps
+    time.sleep(0.25)
+    clocks.stop()
+    tmax = torch.tensor([t_step], device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(tmax, op=torch.distributed.ReduceOp.MAX)
+    t_step = float(tmax.item())
+    value = world * step_bytes / t_step / 1e9
+
+    # ---------------- roofline of the dominant kernel. Every launch of the step
+    # is w4a16_gemv_kernel<1,64>, so its average launch duration is the
+    # event-timed step time / launches (the graph has no other node). Per-shape
+    # durations come from graphs holding the 36 launches of one projection kind.
+    per_shape = {}
+    for kind in ("q", "k", "o", "gate_up", "down", "lm_head"):
+        sel = [i for i, m in enumerate(mats) if m[0].split(".")[-1] == kind]
+        gk = capture(lambda: run_stack(q, [mats[i] for i in sel], [xs[i] for i in sel], [ys[i] for i in sel],
+                                       1, stream), stream)
+        tk = replay_timed(gk, 10, stream) / len(sel)
+        N, K = mats[sel[0]][1], mats[sel[0]][2]
+        per_shape[kind] = {"N": N, "K": K, "us_per_launch": tk * 1e6, "GB_per_s": w4_bytes(N, K) / tk / 1e9}
+        del gk
+    k_time = t_step
+    achieved = step_bytes / k_time / 1e9
+    traffic = kernel_traffic("w4a16_gemv_m1", step_bytes / launches)
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak, "traffic": traffic,
+                "kernel": "w4a16_gemv_kernel<1,64> (all 217 launches of the step)",
+                "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)" if peak_src == "measured"
+                else "fallback 6.8 TB/s",
+                "avg_launch_us": k_time / launches * 1e6,
+                "alg_bytes_per_launch": step_bytes / launches, "per_shape": per_shape}
+
+    # ---------------- e2e through the public API with host buffers
+    xh = torch.empty(sum(x.numel() for x in xs), dtype=torch.bfloat16).pin_memory()
+    yh = torch.empty(sum(y.numel() for y in ys), dtype=torch.float32).pin_memory()
+    xd = torch.empty(xh.numel(), dtype=torch.bfloat16, device=dev)
+    yd = torch.empty(yh.numel(), dtype=torch.float32, device=dev)
+    xv, yv, o1, o2 = [], [], 0, 0
+    for x, y in zip(xs, ys):
+        xv.append(xd[o1:o1 + x.numel()].view_as(x))
+        yv.append(yd[o2:o2 + y.numel()].view_as(y))
+        o1 += x.numel()
+        o2 += y.numel()
+    xh.copy_(torch.cat([x.reshape(-1) for x in xs]).cpu())
+
+    def e2e_step():
+        xd.copy_(xh, non_blocking=True)
+        run_stack(q, mats, xv, yv, 1, stream)
+        yh.copy_(yd, non_blocking=True)
+    ge = capture(e2e_step, stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            ge.replay()
+        stream.synchronize()
+        n_e2e = max(10, min(args.steps, 500))
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            ge.replay()
+            stream.synchronize()
+        t_e2e = (time.perf_counter() - t0) / n_e2e
+    e2e = {"value": world * step_bytes / t_e2e / 1e9, "unit": "GB/s", "h2d_bytes_per_step": xh.numel() * 2,
+           "d2h_bytes_per_step": yh.numel() * 4,
+           "how": "pinned host x -> device, 217 C-ABI GEMV calls, device y -> pinned host, one CUDA graph per "
+                  "step, host-timed including the final synchronize"}
+
+    extras = {}
+    if not args.no_extras and rank == 0:
+        # M = 16 stack (skinny form), same weights
+        xs16, ys16 = stack_io(mats, dev, 16)
+        step16 = sum(w4_bytes(N, K, 16) for (_, N, K, *_r) in mats)
+        t16, _ = time_graph(lambda: run_stack(q, mats, xs16, ys16, 16, stream), 20, stream)
+        extras["m16_stack"] = {"value": step16 / t16 / 1e9, "unit": "GB/s", "frac": step16 / t16 / 1e9 / hbm_peak,
+                               "ms_per_step": t16 * 1e3, "tokens_per_s": 16 / t16, "bytes_per_step": step16}
+        del xs16, ys16
+        extras["m1_stack_tokens_per_s"] = 1.0 / t_step
+        extras["single_gemv_1024"] = bench_single_gemv(q, dev, stream, l2)
+        torch.cuda.empty_cache()
+        E, H, I = 384, 7168, 2048
+        with torch.cuda.stream(stream):
+            gq, gs = synth.mxfp4_weights(E * I, H, 3, 2, dev)
+            uq, us = synth.mxfp4_weights(E * I, H, 3, 3, dev)
+            dq, ds = synth.mxfp4_weights(E * H, I, 3, 4, dev)
+        moe_w = [t.reshape(E, r, -1) for t, r in ((gq, I), (gs, I), (uq, I), (us, I), (dq, H), (ds, H))]
+        torch.cuda.synchronize()
+        for T in (1, 16):
+            r = bench_moe(q, dev, stream, T, moe_w)
+            r["frac"] = r["GB_per_s"] / hbm_peak
+            extras[f"moe_mxfp4_T{T}"] = r
+        del moe_w, gq, gs, uq, us, dq, ds
+        torch.cuda.empty_cache()
+        for N in (4096, 12288):
+            r = bench_w8a8(q, dev, stream, N, l2)
+            r["frac"] = r["GB_per_s"] / hbm_peak
+            extras[f"w8a8_{N}x4096"] = r
+
+    cpu = cpu_baseline(args.cpu_seconds, mats, xs) if rank == 0 else None
+    assert q.device_error() == 0, "a kernel reported a bounded-wait timeout"
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "decode layer stack of a dense 9B-class decoder, M=1: 36 x (q, k, v, o, "
+                                   "gate+up, down) + lm_head 151936x4096, W4A16 affine g64, 217 GEMVs per step",
+                       "bytes_per_step": step_bytes, "launches_per_step": launches,
+                       "l2": f"inputs {step_bytes / 1e9:.2f} GB > L2 {l2 / 1e6:.0f} MB (no flush needed)",
+                       "parallelism": f"replicas x{world}", "frac_of_peak": value / world / hbm_peak,
+                       "tokens_per_s": world / t_step},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks.summary(),
+            "gpu_launches": launches * args.steps, "extras": extras,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -45,6 +45,13 @@ bool g_pdl = false;  // programmatic dependent launch for every kernel (see qg_s
 }  // namespace
 
 namespace qg {
+int device_max_smem_optin() {
+  int dev = 0, v = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  return v;
+}
+
 int device_sm_count() {
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);

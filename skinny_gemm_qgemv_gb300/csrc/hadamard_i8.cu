@@ -65,8 +65,7 @@ __global__ void __launch_bounds__(256) hadamard32_quant_i8_kernel(const uint16_t
 cudaError_t launch_hadamard32_quant_i8(const uint16_t* x, const uint32_t* sign_bits, int8_t* q, float* scale,
                                        int M, int K, cudaStream_t stream, bool pdl) {
   const size_t smem = sizeof(float) * (size_t)K;
-  cudaError_t e =
-      cudaFuncSetAttribute(hadamard32_quant_i8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = allow_max_smem(hadamard32_quant_i8_kernel);
   if (e != cudaSuccess) return e;
   return launch_kernel(hadamard32_quant_i8_kernel, dim3(M), dim3(256), smem, stream, pdl, x, sign_bits, q, scale,
                        K);

@@ -410,7 +410,7 @@ cudaError_t launch_moe_mxfp4(const uint16_t* x, const float* logits, const uint8
                     reinterpret_cast<uint16_t*>(base + L.hh), I32(L.hexp));
   if (e != cudaSuccess) return e;
   const size_t smem = sizeof(float) * (size_t)P * 8;
-  e = cudaFuncSetAttribute(moe_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  e = allow_max_smem(moe_down_kernel);
   if (e != cudaSuccess) return e;
   e = launch_kernel(moe_down_kernel, dim3((H + 7) / 8), dim3(256), smem, stream, pdl, dq, ds,
                     (const uint16_t*)(base + L.hh), (const int32_t*)I32(L.hexp), (const float*)wts,

@@ -31,8 +31,35 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 
 int device_sm_count();
 
+// Largest dynamic shared memory one CTA may opt into on the current device.
+int device_max_smem_optin();
+
+// Raise a kernel's dynamic shared-memory limit to the device maximum. The
+// value is the same for every call, so launches captured into a CUDA graph
+// (or replayed one by one by a profiler) never see a limit set for another
+// shape.
+template <typename... KArgs>
+cudaError_t allow_max_smem(void (*kernel)(KArgs...)) {
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              device_max_smem_optin() - static_cast<int>(fa.sharedSizeBytes));
+}
+
 // W4A16 (w4a16_gemv.cu, w4a16_tc.cu)
+struct GemvConfig {
+  int kpl;            // consecutive k per lane (32 or 64)
+  int rpw;            // rows per consumer warp per tile (2, 4, 8)
+  int rg;             // row groups per CTA
+  int ctas_per_sm;    // grid = min(tiles, ctas_per_sm * SMs)
+  size_t smem_budget; // shared memory for the stage ring
+};
 bool gemv_fast_path_ok(int M, int N, int K);
+GemvConfig gemv_pick_config(int M, int N, int K, int sms);
+cudaError_t launch_w4a16_fast_cfg(const uint32_t* wq, const uint16_t* sc, const uint16_t* bi, const uint16_t* x,
+                                  float* y, int M, int N, int K, const GemvConfig& cfg, uint32_t* err,
+                                  cudaStream_t stream, bool pdl);
 cudaError_t launch_w4a16_fast(const uint32_t* wq, const uint16_t* sc, const uint16_t* bi, const uint16_t* x,
                               float* y, int M, int N, int K, uint32_t* err, cudaStream_t stream, bool pdl);
 cudaError_t launch_w4a16_generic(const uint32_t* wq, const uint16_t* sc, const uint16_t* bi, const uint16_t* x,

@@ -48,10 +48,46 @@ struct GemvArgs {
   uint32_t* err;
 };
 
-constexpr int kRPW = 2;  // rows per consumer warp per tile
+// Sum R per-lane values over the 32 lanes of a warp with a transposed
+// butterfly: at offsets 16, 8, ... each lane keeps half of its remaining values
+// and adds its partner's copy of that half, so R values cost about
+// R - 1 + log2(32 / R) shuffles instead of 5 R. Afterwards lane L holds the
+// total of value transposed_row<R>(L).
+template <int R>
+__device__ __forceinline__ float transposed_warp_sum(float (&v)[R], int lane) {
+  int cnt = R;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    if (cnt > 1) {
+      const int half = cnt / 2;
+      const bool upper = lane & o;
+#pragma unroll
+      for (int i = 0; i < R / 2; ++i) {
+        if (i < half) {
+          const float keep = upper ? v[i + half] : v[i];
+          const float send = upper ? v[i] : v[i + half];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+      }
+      cnt = half;
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+    }
+  }
+  return v[0];
+}
 
-template <int M, int KPL>
-__global__ void __launch_bounds__(288, 2) w4a16_gemv_kernel(const GemvArgs a) {
+template <int R>
+__device__ __forceinline__ int transposed_row(int lane) {
+  int row = 0, half = R / 2;
+#pragma unroll
+  for (int o = 16; o >= 1 && half >= 1; o >>= 1, half >>= 1)
+    if (lane & o) row += half;
+  return row;
+}
+
+template <int M, int KPL, int kRPW, int MINB>
+__global__ void __launch_bounds__(288, MINB) w4a16_gemv_kernel(const GemvArgs a) {
   constexpr int WPL = KPL / 8;  // 32-bit code words per lane per row
   extern __shared__ __align__(128) uint8_t smem[];
   const int NC = a.S * a.RG;
@@ -76,6 +112,7 @@ __global__ void __launch_bounds__(288, 2) w4a16_gemv_kernel(const GemvArgs a) {
     fence_mbar_init();
   }
   __syncthreads();
+  pdl_launch_dependents();
 
   if (warp == NC) {
     // ------------------------------------------------------------ producer
@@ -104,7 +141,6 @@ __global__ void __launch_bounds__(288, 2) w4a16_gemv_kernel(const GemvArgs a) {
       for (int j = max(0, issued - a.ST); j < issued; ++j)
         mbar_wait(&full[j % a.ST], (j / a.ST) & 1, a.err, kErrGemvDrain);
     }
-    pdl_launch_dependents();
     return;
   }
 
@@ -193,21 +229,19 @@ __global__ void __launch_bounds__(288, 2) w4a16_gemv_kernel(const GemvArgs a) {
       }
     }
     __syncwarp();
-    // transposed butterfly over 32 lanes: lanes [16h, 16h+16) end with row h
     float v[M];
 #pragma unroll
     for (int m = 0; m < M; ++m) {
-      const bool hi = lane & 16;
-      float keep = hi ? part[1][m] : part[0][m];
-      float send = hi ? part[0][m] : part[1][m];
-      keep += __shfl_xor_sync(0xffffffffu, send, 16);
+      float col[kRPW];
 #pragma unroll
-      for (int o = 8; o > 0; o >>= 1) keep += __shfl_xor_sync(0xffffffffu, keep, o);
-      v[m] = keep;
+      for (int i = 0; i < kRPW; ++i) col[i] = part[i][m];
+      v[m] = transposed_warp_sum<kRPW>(col, lane);
     }
-    const int myrow = rg * kRPW + (lane >> 4);
+    constexpr int kLanesPerRow = 32 / kRPW;
+    const bool writer = (lane & (kLanesPerRow - 1)) == 0;
+    const int myrow = rg * kRPW + transposed_row<kRPW>(lane);
     if (a.S == 1) {
-      if ((lane & 15) == 0 && myrow < rows) {
+      if (writer && myrow < rows) {
 #pragma unroll
         for (int m = 0; m < M; ++m) a.y[(size_t)m * N + r0 + myrow] = v[m];
       }
@@ -215,7 +249,7 @@ __global__ void __launch_bounds__(288, 2) w4a16_gemv_kernel(const GemvArgs a) {
     } else {
       float* rb = red + (size_t)st * a.S * a.R * M;
       if (s != 0) {
-        if ((lane & 15) == 0) {
+        if (writer) {
 #pragma unroll
           for (int m = 0; m < M; ++m) rb[(s * a.R + myrow) * M + m] = v[m];
         }
@@ -226,7 +260,7 @@ __global__ void __launch_bounds__(288, 2) w4a16_gemv_kernel(const GemvArgs a) {
         }
       } else {
         if (!mbar_wait(&redfull[st], par, a.err, kErrGemvFullWait)) break;
-        if ((lane & 15) == 0 && myrow < rows) {
+        if (writer && myrow < rows) {
 #pragma unroll
           for (int m = 0; m < M; ++m) {
             float tot = v[m];
@@ -239,7 +273,6 @@ __global__ void __launch_bounds__(288, 2) w4a16_gemv_kernel(const GemvArgs a) {
       }
     }
   }
-  pdl_launch_dependents();
 }
 
 // ---------------------------------------------------------------------------
@@ -286,16 +319,39 @@ __global__ void __launch_bounds__(256) w4a16_generic_kernel(const uint32_t* __re
 // Host side
 // ---------------------------------------------------------------------------
 bool gemv_fast_path_ok(int M, int N, int K) {
-  if (M < 1 || M > 2) return false;
-  if (K % 1024 != 0) return false;
-  const int KPL = (M == 1 && K % 2048 == 0) ? 64 : 32;
-  const int S = K / (32 * KPL);
-  return S >= 1 && S <= 8 && N >= 1;
+  if (M < 1 || M > 2 || N < 1 || K % 1024 != 0) return false;
+  // at most eight consumer warps cover one row (S <= 8)
+  const int slices = (M == 1 && K % 2048 == 0) ? K / 2048 : K / 1024;
+  return slices <= 8;
 }
 
-template <int M, int KPL>
+// Shape -> launch configuration of the fast kernel. Lanes cover KPL
+// consecutive k, so one warp covers a K-slice of 32 * KPL and S = K / (32 KPL)
+// warps cover a row; RG row groups of RPW rows each make a tile of R = RG * RPW
+// rows. More rows per warp amortize the lane reduction and give independent
+// FMA chains; small N trade rows per warp for enough tiles to fill the SMs.
+GemvConfig gemv_pick_config(int M, int N, int K, int sms) {
+  // Chosen from a sweep on GB300 (152 SMs) over the decode shapes: two CTAs of
+  // at most nine warps per SM; 64 k per lane and 4 rows per warp for very
+  // tall matrices and for K = 12288 (fewer K-slices per row), otherwise 32 k
+  // per lane and up to 8 rows per warp, reduced until every CTA slot has a tile.
+  GemvConfig c;
+  const bool tall = N >= 65536;
+  c.kpl = (M == 1 && K % 2048 == 0 && (tall || K / 1024 > 8)) ? 64 : 32;
+  const int S = K / (32 * c.kpl);
+  c.rg = S >= 8 ? 1 : 8 / S;
+  c.ctas_per_sm = 2;
+  c.smem_budget = 74 * 1024;
+  c.rpw = (M == 1 && c.kpl == 32) ? 8 : 4;
+  while (c.rpw > 2 && (N + c.rg * c.rpw - 1) / (c.rg * c.rpw) < c.ctas_per_sm * sms) c.rpw /= 2;
+  while (c.rg > 1 && (N + c.rg * c.rpw - 1) / (c.rg * c.rpw) < c.ctas_per_sm * sms) c.rg /= 2;
+  return c;
+}
+
+template <int M, int KPL, int RPW, int MINB>
 static cudaError_t launch_fast(const uint32_t* wq, const uint16_t* sc, const uint16_t* bi, const uint16_t* x,
-                               float* y, int N, int K, uint32_t* err, cudaStream_t stream, bool pdl) {
+                               float* y, int N, int K, const GemvConfig& cfg, uint32_t* err, cudaStream_t stream,
+                               bool pdl) {
   GemvArgs a;
   a.wq = wq;
   a.scales = sc;
@@ -305,38 +361,60 @@ static cudaError_t launch_fast(const uint32_t* wq, const uint16_t* sc, const uin
   a.N = N;
   a.K = K;
   a.S = K / (32 * KPL);
-  a.RG = std::max(1, 8 / a.S);
-  a.R = a.RG * kRPW;
+  a.RG = cfg.rg;
+  a.R = a.RG * RPW;
   a.ntiles = (N + a.R - 1) / a.R;
   const uint32_t row_bytes = K / 2 + K / 16;
   a.stage_bytes = (uint32_t)a.R * row_bytes;  // multiple of 16 since K % 512 == 0
   const int NC = a.S * a.RG;
-  // two CTAs per SM: keep each CTA's shared memory under ~110 KB
-  const size_t budget = 110 * 1024;
-  int ST = (int)(budget / (a.stage_bytes + sizeof(float) * a.S * a.R * M + 24));
+  if ((NC + 1) * 32 > 288) return cudaErrorInvalidConfiguration;
+  int ST = (int)(cfg.smem_budget / (a.stage_bytes + sizeof(float) * a.S * a.R * M + 24));
   ST = std::max(2, std::min(ST, 8));
   a.ST = ST;
   a.err = err;
   const size_t smem = (size_t)ST * a.stage_bytes + sizeof(float) * (size_t)ST * a.S * a.R * M + 3 * 8 * ST;
-  static_assert(sizeof(GemvArgs) < 4096, "kernel params");
-
-  auto kern = w4a16_gemv_kernel<M, KPL>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kern = w4a16_gemv_kernel<M, KPL, RPW, MINB>;
+  cudaError_t e = allow_max_smem(kern);
   if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int grid = std::min(a.ntiles, 2 * sms);
+  const int grid = std::min(a.ntiles, cfg.ctas_per_sm * device_sm_count());
   return launch_kernel(kern, dim3(grid), dim3((NC + 1) * 32), smem, stream, pdl, a);
+}
+
+template <int M, int KPL>
+static cudaError_t launch_rpw(const uint32_t* wq, const uint16_t* sc, const uint16_t* bi, const uint16_t* x,
+                              float* y, int N, int K, const GemvConfig& cfg, uint32_t* err, cudaStream_t stream,
+                              bool pdl) {
+  // MINB (CTAs per SM the register allocation is sized for) follows ctas_per_sm
+#define QG_RPW_CASE(R)                                                                              \
+  case R:                                                                                           \
+    if (cfg.ctas_per_sm >= 4) return launch_fast<M, KPL, R, 4>(wq, sc, bi, x, y, N, K, cfg, err, stream, pdl); \
+    if (cfg.ctas_per_sm == 3) return launch_fast<M, KPL, R, 3>(wq, sc, bi, x, y, N, K, cfg, err, stream, pdl); \
+    return launch_fast<M, KPL, R, 2>(wq, sc, bi, x, y, N, K, cfg, err, stream, pdl);
+  switch (cfg.rpw) {
+    QG_RPW_CASE(2)
+    QG_RPW_CASE(4)
+    QG_RPW_CASE(8)
+    default: return cudaErrorInvalidValue;
+  }
+#undef QG_RPW_CASE
+}
+
+cudaError_t launch_w4a16_fast_cfg(const uint32_t* wq, const uint16_t* sc, const uint16_t* bi, const uint16_t* x,
+                                  float* y, int M, int N, int K, const GemvConfig& cfg, uint32_t* err,
+                                  cudaStream_t stream, bool pdl) {
+  if (K % (32 * cfg.kpl) != 0) return cudaErrorInvalidValue;
+  if (M == 1) {
+    if (cfg.kpl == 64) return launch_rpw<1, 64>(wq, sc, bi, x, y, N, K, cfg, err, stream, pdl);
+    return launch_rpw<1, 32>(wq, sc, bi, x, y, N, K, cfg, err, stream, pdl);
+  }
+  if (cfg.kpl != 32) return cudaErrorInvalidValue;
+  return launch_rpw<2, 32>(wq, sc, bi, x, y, N, K, cfg, err, stream, pdl);
 }
 
 cudaError_t launch_w4a16_fast(const uint32_t* wq, const uint16_t* sc, const uint16_t* bi, const uint16_t* x,
                               float* y, int M, int N, int K, uint32_t* err, cudaStream_t stream, bool pdl) {
-  if (M == 1) {
-    if (K % 2048 == 0) return launch_fast<1, 64>(wq, sc, bi, x, y, N, K, err, stream, pdl);
-    return launch_fast<1, 32>(wq, sc, bi, x, y, N, K, err, stream, pdl);
-  }
-  return launch_fast<2, 32>(wq, sc, bi, x, y, N, K, err, stream, pdl);
+  const GemvConfig cfg = gemv_pick_config(M, N, K, device_sm_count());
+  return launch_w4a16_fast_cfg(wq, sc, bi, x, y, M, N, K, cfg, err, stream, pdl);
 }
 
 cudaError_t launch_w4a16_generic(const uint32_t* wq, const uint16_t* sc, const uint16_t* bi, const uint16_t* x,
