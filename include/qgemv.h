@@ -163,6 +163,46 @@ QG_API size_t qg_moe_workspace_size(int T, int H, int I, int E, int top_k);
 QG_API size_t qg_moe_workspace_h_offset(int T, int H, int I, int E, int top_k);
 
 /*
+ * moe_mxfp4_expert_forward_noalloc -- the same computation, arguments, layouts
+ * and results as moe_mxfp4_expert_forward, for callers that cannot allocate
+ * device memory when they run the layer: for example a plugin inside a host
+ * inference server that is handed only its input and output buffers, a
+ * runtime that reserves all device memory as one pool at start-up, or code
+ * recorded while a CUDA graph is being captured (cudaMalloc is not allowed
+ * during capture). The pages have no counterpart; this is a library service.
+ *
+ * Instead of a caller workspace it uses a scratch array of
+ * QG_MOE_NOALLOC_MAX_BYTES bytes that is part of the library's device image:
+ * every GPU that loads the library holds it until the process exits. The call
+ * itself allocates nothing (no cudaMalloc, cudaFree or allocating library
+ * routine).
+ *   - Problems whose workspace (qg_moe_workspace_size) exceeds
+ *     QG_MOE_NOALLOC_MAX_BYTES are refused with QG_ERR_WORKSPACE before any
+ *     launch; with 384 experts of 7168 x 2048 and top-16 routing that admits
+ *     up to T = 39 tokens.
+ *   - The first call on a device looks up the scratch array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture begins.
+ *   - All calls on a device share the one array and it keeps the previous
+ *     call's contents; every stage writes what it later reads, so nothing has
+ *     to start zeroed. Calls that may run at the same time on the GPU (on
+ *     different streams, or from different threads without ordering) race on
+ *     the array: order them on one stream.
+ *   - Launches never use programmatic dependent launch (qg_set_pdl is
+ *     ignored here).
+ */
+#define QG_MOE_NOALLOC_MAX_BYTES ((size_t)8 << 20)
+
+QG_API qg_status moe_mxfp4_expert_forward_noalloc(
+    const uint16_t *x_bf16, const float *router_logits, const uint8_t *gate_q,
+    const uint8_t *gate_e8m0, const uint8_t *up_q, const uint8_t *up_e8m0,
+    const uint8_t *down_q, const uint8_t *down_e8m0, int T, int H, int I, int E,
+    int top_k, float *y, int32_t *topk_idx, float *topk_w, void *stream);
+
+/* QG_MOE_NOALLOC_MAX_BYTES as compiled into the library. */
+QG_API size_t qg_moe_noalloc_max_bytes(void);
+
+/*
  * hadamard32_quant_i8 -- block-32 randomized Walsh-Hadamard transform and
  * per-row symmetric int8 quantization (Uzu article, "How Uzu optimizes bytes
  * and tokens per pass").

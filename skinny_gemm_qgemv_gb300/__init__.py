@@ -27,6 +27,7 @@ EXPORTS = [
     "qg_status_string", "qg_version", "qgemv_w4a16", "qg_gemv_workspace_size", "qgemm_w4a16_skinny",
     "qg_skinny_workspace_size", "moe_mxfp4_expert_forward", "qg_moe_workspace_size",
     "qg_moe_workspace_h_offset", "hadamard32_quant_i8", "gemm_w8a8_i32", "qg_set_pdl", "qg_device_error",
+    "moe_mxfp4_expert_forward_noalloc", "qg_moe_noalloc_max_bytes",
 ]
 
 
@@ -73,6 +74,10 @@ def lib() -> ctypes.CDLL:
         L.qg_set_pdl.argtypes = [I]
         L.qg_device_error.restype = I
         L.qg_device_error.argtypes = [P, I]
+        L.moe_mxfp4_expert_forward_noalloc.restype = I
+        L.moe_mxfp4_expert_forward_noalloc.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, P, P, P, P]
+        L.qg_moe_noalloc_max_bytes.restype = Z
+        L.qg_moe_noalloc_max_bytes.argtypes = []
         _lib = L
     return _lib
 
