@@ -92,11 +92,8 @@ size_t qg_gemv_workspace_size(int N, int K, int group_size) {
 }
 
 size_t qg_skinny_workspace_size(int M, int N, int K, int group_size) {
-  (void)M;
-  (void)N;
-  (void)K;
-  (void)group_size;
-  return 0;
+  if (group_size != 64 || M < 1 || M > 32 || N < 1 || K < 1) return 0;
+  return qg::gemv_fast_path_ok(M, N, K) ? 0 : qg::tc_workspace_size(M, N, K);
 }
 
 static qg_status check_w4(const uint32_t* wq, const uint16_t* s, const uint16_t* b, const uint16_t* x,
@@ -111,13 +108,17 @@ static qg_status check_w4(const uint32_t* wq, const uint16_t* s, const uint16_t*
 }
 
 static qg_status run_w4(const uint32_t* wq, const uint16_t* s, const uint16_t* b, const uint16_t* x, float* y,
-                        int M, int N, int K, void* stream) {
+                        int M, int N, int K, void* ws, size_t ws_bytes, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (qg::gemv_fast_path_ok(M, N, K)) {
     uint32_t* err = err_word();
     if (!err) return QG_ERR_CUDA;
     e = qg::launch_w4a16_fast(wq, s, b, x, y, M, N, K, err, st, g_pdl);
+  } else if (qg::tc_path_ok(M, N, K)) {
+    uint32_t* err = err_word();
+    if (!err) return QG_ERR_CUDA;
+    e = qg::launch_w4a16_tc(wq, s, b, x, y, M, N, K, ws, ws_bytes, err, st, g_pdl);
   } else {
     e = qg::launch_w4a16_generic(wq, s, b, x, y, M, N, K, st, g_pdl);
   }
@@ -131,7 +132,7 @@ qg_status qgemv_w4a16(const uint32_t* wq, const uint16_t* scales_f16, const uint
   if (st != QG_OK) return st;
   if (ws_bytes < qg_gemv_workspace_size(N, K, group_size)) return QG_ERR_WORKSPACE;
   if (ws_bytes && !workspace) return QG_ERR_INVALID_ARG;
-  return run_w4(wq, scales_f16, biases_f16, x_bf16, y, 1, N, K, stream);
+  return run_w4(wq, scales_f16, biases_f16, x_bf16, y, 1, N, K, workspace, ws_bytes, stream);
 }
 
 qg_status qgemm_w4a16_skinny(const uint32_t* wq, const uint16_t* scales_f16, const uint16_t* biases_f16,
@@ -142,7 +143,7 @@ qg_status qgemm_w4a16_skinny(const uint32_t* wq, const uint16_t* scales_f16, con
   if (ws_bytes < qg_skinny_workspace_size(M, N, K, group_size)) return QG_ERR_WORKSPACE;
   if (ws_bytes && !workspace) return QG_ERR_INVALID_ARG;
   if (workspace && !aligned16(workspace)) return QG_ERR_MISALIGNED;
-  return run_w4(wq, scales_f16, biases_f16, x_bf16, y, M, N, K, stream);
+  return run_w4(wq, scales_f16, biases_f16, x_bf16, y, M, N, K, workspace, ws_bytes, stream);
 }
 
 size_t qg_moe_workspace_size(int T, int H, int I, int E, int top_k) {

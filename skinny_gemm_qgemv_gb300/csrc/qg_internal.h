@@ -62,6 +62,11 @@ cudaError_t launch_w4a16_fast_cfg(const uint32_t* wq, const uint16_t* sc, const 
                                   cudaStream_t stream, bool pdl);
 cudaError_t launch_w4a16_fast(const uint32_t* wq, const uint16_t* sc, const uint16_t* bi, const uint16_t* x,
                               float* y, int M, int N, int K, uint32_t* err, cudaStream_t stream, bool pdl);
+bool tc_path_ok(int M, int N, int K);
+size_t tc_workspace_size(int M, int N, int K);
+cudaError_t launch_w4a16_tc(const uint32_t* wq, const uint16_t* sc, const uint16_t* bi, const uint16_t* x,
+                            float* y, int M, int N, int K, void* ws, size_t ws_bytes, uint32_t* err,
+                            cudaStream_t stream, bool pdl);
 cudaError_t launch_w4a16_generic(const uint32_t* wq, const uint16_t* sc, const uint16_t* bi, const uint16_t* x,
                                  float* y, int M, int N, int K, cudaStream_t stream, bool pdl);
 
