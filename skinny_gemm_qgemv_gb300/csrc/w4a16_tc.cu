@@ -7,26 +7,32 @@
 // and a 16-token verify batch gives the matrix units 16 rows of work (Uzu
 // article, section "Producing several tokens from one model pass").
 //
-// GB300 design (one persistent CTA per SM, 10 warps):
-//  warp 0      producer: TMA tensor loads per 512-k stage -- the X tile (bf16,
-//              128B-swizzled, one box per 64-k group), the 4-bit codes of 128
-//              weight rows (two 128B-swizzled boxes) and their fp16 scales and
-//              biases -- into a ring of shared-memory stages (mbarrier tx).
-//  warp 1      MMA issuer: per 64-k group, four tcgen05.mma.kind::f16
-//              (M = 128 weight rows, N = 16 or 32 activation rows, K = 16) into a
-//              fresh TMEM accumulator; owns the TMEM allocation.
-//  warps 2..5  converters: decode each code word into eight bf16 values 128 + q
-//              (exact) in natural k order and store them in the canonical
-//              128B-swizzled K-major layout the MMA reads (A operand).
-//  warps 6..9  epilogue: one weight row per thread (its TMEM lane); per group
-//              it reads the accumulator (tcgen05.ld) and folds
-//              y += s * acc + (b - 128 s) * sum_{k in g} x, the group-factored
-//              affine dot product, in fp32. The weights are never rounded to
-//              bf16: products are exact and only the fp32 sums round.
-// Short matrices are split along K; the CTA finishing a row tile last (atomic
-// counter, no waiting) adds the partial tiles in split order (deterministic).
-// Every mbarrier wait is bounded; a timeout sets the device error word and a
-// shared abort flag so all roles finish quickly and TMEM is released.
+// GB300 design (one persistent CTA per SM, 16 warps). The roles hand work to
+// each other in chunks of 256 k (four 64-k groups): every mbarrier operation
+// costs tens to hundreds of cycles under load, so one hand-off per group would
+// pace the whole pipeline.
+//  warp 0       producer: TMA tensor loads per 512-k stage -- the X tile (bf16,
+//               128B-swizzled, one box per 64-k group), the 4-bit codes of 128
+//               weight rows (two 128B-swizzled boxes, one per chunk) and their
+//               fp16 scales and biases -- into a ring of shared-memory stages.
+//  warps 1, 2   MMA issuers (even / odd chunks): per group four
+//               tcgen05.mma.kind::f16 (M = 128 weight rows, N = 16 or 32
+//               activation rows, K = 16) with A read from TMEM, each group into
+//               its own accumulator; one commit per chunk.
+//  warps 3..10  converters, all on every chunk (warps 3..6 its groups 0-1,
+//               7..10 groups 2-3): decode each code word into eight bf16 values
+//               128 + q (exact) in natural k order and store them into TMEM as
+//               the A operand (row = lane); two A buffers let the next chunk be
+//               decoded while the MMAs read the current one.
+//  warps 11..14 epilogue: one weight row per thread (its TMEM lane); per chunk
+//               it reads the four accumulators (tcgen05.ld) and folds
+//               y += s * acc + (b - 128 s) * sum_{k in g} x, the group-factored
+//               affine dot product, in fp32. The weights are never rounded to
+//               bf16: products are exact and only the fp32 sums round.
+//  warp 15      x sums: sum_{k in g} x per group and activation row, from the
+//               X tile of each landed stage, into a small ring beside it.
+// TMEM: columns 0..255 hold the accumulators (chunk buffers of 4 x N columns),
+// 256..511 two A chunk buffers of 4 x 32 columns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -44,10 +50,14 @@ namespace {
 constexpr int kRows = 128;          // weight rows per tile = MMA M = TMEM lanes
 constexpr int kStageK = 512;        // k per pipeline stage
 constexpr int kGroupsPerStage = 8;  // 64-k groups per stage
-constexpr int kNA = 8;              // A (converted weights) buffers in TMEM, 32 columns each
-constexpr uint32_t kAccCols = 128;  // TMEM columns for accumulators: 128 / N buffers of N columns
-constexpr uint32_t kTmemCols = 512; // accumulators at column 0, A buffers from column 128
-constexpr int kThreads = 480;  // 1 producer + 2 MMA + 2 x 4 converter + 4 epilogue warps
+constexpr int kChunkK = 256;        // k per hand-off between the roles: one 128-byte row of codes
+constexpr int kChunkGroups = 4;     // 64-k groups per chunk
+constexpr int kChunksPerStage = kStageK / kChunkK;
+constexpr int kNAB = 2;             // A (converted weights) chunk buffers in TMEM, 128 columns each
+constexpr uint32_t kAccCols = 256;  // TMEM columns for accumulators: chunk buffers of 4 x N columns
+constexpr uint32_t kACol = 256;     // first TMEM column of the A buffers
+constexpr uint32_t kTmemCols = 512;
+constexpr int kThreads = 512;  // 1 producer + 2 MMA + 8 converter + 4 epilogue + 1 x-sum warps
 
 struct TcArgs {
   int N, K, M;
@@ -77,14 +87,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
       : "memory");
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
-}
-
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm, int x, int y, int z, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
@@ -101,8 +103,8 @@ __device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
 
-// 32 consecutive 32-bit TMEM columns of this thread's lane <- registers
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+// 32 consecutive 32-bit TMEM columns of this thread's lane <- registers (no wait)
+__device__ __forceinline__ void tmem_st32_nowait(uint32_t taddr, const uint32_t (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
       "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
@@ -111,8 +113,9 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
       "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
@@ -122,32 +125,28 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-template <int N>
-__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[N]);
-
-template <>
-__device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
+// G groups x N accumulator columns of this thread's lane (G * N = 64): sixteen
+// columns per load, one wait for all of them; the values are only touched
+// after the wait.
+template <int G, int N>
+__device__ __forceinline__ void tmem_ld_groups(uint32_t taddr, uint32_t (&r)[G][N]) {
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+#pragma unroll
+    for (int h = 0; h < N / 16; ++h) {
+      uint32_t* o = &r[j][16 * h];
+      asm volatile(
+          "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+          : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3]), "=r"(o[4]), "=r"(o[5]), "=r"(o[6]), "=r"(o[7]),
+            "=r"(o[8]), "=r"(o[9]), "=r"(o[10]), "=r"(o[11]), "=r"(o[12]), "=r"(o[13]), "=r"(o[14]), "=r"(o[15])
+          : "r"(taddr + j * N + 16 * h));
+    }
+  }
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-template <>
-__device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, float (&v)[32]) {
-  float a[16], b[16];
-  tmem_ld<16>(taddr, a);
-  tmem_ld<16>(taddr + 16, b);
+  for (int j = 0; j < G; ++j)
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    v[i] = a[i];
-    v[16 + i] = b[i];
-  }
+    for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[j][i]));
 }
 
 // Eight 4-bit codes (code i in bits 4i..4i+3) -> four bf16x2 registers in
@@ -190,26 +189,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     w4a16_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scales,
                     const __grid_constant__ CUtensorMap tm_biases, const __grid_constant__ CUtensorMap tm_x,
                     const TcArgs a) {
-  constexpr int NB = (int)kAccCols / NT;  // TMEM accumulator buffers
+  constexpr int NACC = (int)kAccCols / (kChunkGroups * NT);  // accumulator chunk buffers in TMEM
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const gbase = smem_raw + (base - raw);
-  // shared layout: stages | sx [K/64][NT] f32 | barriers
+  // shared layout: stages | sx [ST][8 groups][NT] f32 | barriers
   const uint32_t s_stages = base;
-  const int ngroups = a.kper / 64;
+  const int nchunk = a.kper / kChunkK;
   const int nstage = a.kper / kStageK;
-  const int gtotal = a.K / 64;
   float* sx = reinterpret_cast<float*>(gbase + a.ST * a.stage_bytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(
-      gbase + ((a.ST * a.stage_bytes + sizeof(float) * gtotal * NT + 7) & ~(size_t)7));
+      gbase + ((a.ST * a.stage_bytes + sizeof(float) * a.ST * kGroupsPerStage * NT + 7) & ~(size_t)7));
   uint64_t* full = bars;
   uint64_t* empty = full + a.ST;
-  uint64_t* afull = empty + a.ST;     // converted A of a group is in TMEM
-  uint64_t* mmadone = afull + kNA;    // the MMAs of a group completed (A buffer free, accumulator ready)
-  uint64_t* accempty = mmadone + kNA; // the epilogue has read an accumulator
-  uint64_t* done = accempty + NB;     // [2] all MMAs of an issuing warp completed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 2);
+  uint64_t* afull = empty + a.ST;      // a chunk of converted A is in TMEM
+  uint64_t* accfull = afull + kNAB;    // the MMAs of a chunk completed: accumulators ready, A buffer free
+  uint64_t* accempty = accfull + NACC; // the epilogue has read a chunk's accumulators
+  uint64_t* done = accempty + NACC;    // [2] all MMAs of an issuing warp completed
+  uint64_t* sxfull = done + 2;         // [ST] the x sums of a stage are in sx
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sxfull + a.ST);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   volatile uint32_t* is_last = tmem_slot + 2;
 
@@ -220,13 +219,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.ST; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 12);  // 8 converter warps + 4 epilogue warps
+      mbar_init(&empty[i], 13);  // 8 converter warps + 4 epilogue warps + the x-sum warp
+      mbar_init(&sxfull[i], 1);
     }
-    for (int i = 0; i < kNA; ++i) {
-      mbar_init(&afull[i], 4);
-      mbar_init(&mmadone[i], 1);
+    for (int i = 0; i < kNAB; ++i) mbar_init(&afull[i], 8);
+    for (int i = 0; i < NACC; ++i) {
+      mbar_init(&accfull[i], 1);
+      mbar_init(&accempty[i], 4);
     }
-    for (int i = 0; i < NB; ++i) mbar_init(&accempty[i], 4);
     mbar_init(&done[0], 1);
     mbar_init(&done[1], 1);
     *abort_flag = 0u;
@@ -237,26 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                  "r"(kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
-  // sum of x over every 64-k group of the whole K, per activation row, once
-  // per CTA (all threads; the activations may come from the previous kernel)
+  // the activations may come from the previous kernel
   pdl_wait();
-  for (int idx = threadIdx.x; idx < gtotal * NT; idx += kThreads) {
-    const int g = idx / NT, m = idx % NT;
-    float t = 0.f;
-    if (m < a.M) {
-      const uint4* xp = reinterpret_cast<const uint4*>(a.x + (size_t)m * a.K + 64 * g);
-      uint4 c[8];
-#pragma unroll
-      for (int v = 0; v < 8; ++v) c[v] = xp[v];
-#pragma unroll
-      for (int v = 0; v < 8; ++v) {
-        const uint32_t e[4] = {c[v].x, c[v].y, c[v].z, c[v].w};
-#pragma unroll
-        for (int h = 0; h < 4; ++h) t += bf16_bits_to_f32(e[h] & 0xFFFFu) + bf16_bits_to_f32(e[h] >> 16);
-      }
-    }
-    sx[idx] = t;
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -278,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&full[st], a.stage_bytes);
           const int kk = k0 + s * kStageK;
           // X viewed as {64 k, rows, K/64}: one box = the stage's eight [NT][128 B] tiles;
-          // codes viewed as {128 B, rows, K/256}: one box = two [128][128 B] tiles
+          // codes viewed as {128 B, rows, K/256}: one box = two [128][128 B] tiles (one per chunk)
           tma_load_3d(sb + x_off, &tm_x, 0, 0, kk / 64, &full[st]);
           tma_load_3d(sb + c_off, &tm_codes, 0, n0, kk / 256, &full[st]);
           tma_load_2d(sb + s_off, &tm_scales, kk / 64, n0, &full[st]);
@@ -291,112 +273,144 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(&full[j % a.ST], (j / a.ST) & 1, a.err, kErrTcDrain);
     }
   } else if (warp <= 2) {
-    // ------------------------------------------------- MMA issuers: warp 1 even groups, warp 2 odd
+    // ------------------------------------------- MMA issuers: warp 1 even chunks, warp 2 odd chunks
     if (lane == 0) {
-      const int parity_set = warp - 1;
+      const int cset = warp - 1;
       const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NT >> 3) << 17) |
                              ((uint32_t)(kRows >> 4) << 24);
       bool ok = true;
       for (int ui = 0, u = blockIdx.x; u < a.nunits && ok; ++ui, u += gridDim.x) {
-        for (int g = parity_set; g < ngroups && ok; g += 2) {
-          const int gg = ui * ngroups + g;
-          const int sg = ui * nstage + g / kGroupsPerStage, st = sg % a.ST;
-          const int ab = gg % kNA, nb = gg % NB;
+        for (int c = cset; c < nchunk && ok; c += 2) {
+          const int gc = ui * nchunk + c;
+          const int sg = ui * nstage + c / kChunksPerStage, st = sg % a.ST;
+          const int ab = gc % kNAB, nb = gc % NACC;
           ok = wait_or_abort<false>(&full[st], (sg / a.ST) & 1, abort_flag, a.err, kErrTcFullWait);
-          ok = ok && wait_or_abort<false>(&afull[ab], (gg / kNA) & 1, abort_flag, a.err, kErrTcMmaWait);
-          if (ok && gg >= NB)
-            ok = wait_or_abort<false>(&accempty[nb], ((gg / NB) & 1) ^ 1, abort_flag, a.err, kErrTcAccWait);
+          ok = ok && wait_or_abort<false>(&afull[ab], (gc / kNAB) & 1, abort_flag, a.err, kErrTcMmaWait);
+          if (ok && gc >= NACC)
+            ok = wait_or_abort<false>(&accempty[nb], ((gc / NACC) & 1) ^ 1, abort_flag, a.err, kErrTcAccWait);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t at = tbase + kAccCols + ab * 32;
-          const uint64_t bd = sw128_desc(s_stages + st * a.stage_bytes + x_off + (g % kGroupsPerStage) * NT * 128);
+          const uint32_t xs = s_stages + st * a.stage_bytes + x_off;
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) mma_bf16_tmem_a(tbase + nb * NT, at + 8 * ks, bd + 2 * ks, idesc, ks > 0);
-          mma_commit(&mmadone[ab]);
+          for (int j = 0; j < kChunkGroups; ++j) {
+            const int gi = (c % kChunksPerStage) * kChunkGroups + j;  // group within the stage
+            const uint32_t at = tbase + kACol + ab * (kChunkGroups * 32) + j * 32;
+            const uint32_t dt = tbase + nb * (kChunkGroups * NT) + j * NT;
+            const uint64_t bd = sw128_desc(xs + gi * NT * 128);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) mma_bf16_tmem_a(dt, at + 8 * ks, bd + 2 * ks, idesc, ks > 0);
+          }
+          mma_commit(&accfull[nb]);
         }
       }
-      mma_commit(&done[parity_set]);
-      mbar_wait(&done[parity_set], 0, a.err, kErrTcDrain);
+      mma_commit(&done[cset]);
+      mbar_wait(&done[cset], 0, a.err, kErrTcDrain);
     }
   } else if (warp < 11) {
-    // ------------------------------------- converters: warps 3..6 even groups, 7..10 odd groups
-    // a warp may only touch TMEM lanes 32 * (warp % 4) .. + 31: row = its lane
-    const int set = (warp - 3) >> 2;
+    // ------------------------------------------ converters: warps 3..10, every chunk
+    // a warp may only touch TMEM lanes 32 * (warp % 4) .. + 31: row = its lane;
+    // warps 3..6 decode groups 0, 1 of a chunk, warps 7..10 groups 2, 3
+    const int h = (warp - 3) >> 2;
     const int r = (warp & 3) * 32 + lane;  // weight row of the tile, 0..127
     const uint32_t rsw = r & 7;
-    const uint32_t tlane = tbase + ((uint32_t)((warp & 3) * 32) << 16) + kAccCols;
+    const uint32_t tlane = tbase + ((uint32_t)((warp & 3) * 32) << 16) + kACol;
     for (int ui = 0, u = blockIdx.x; u < a.nunits; ++ui, u += gridDim.x) {
-      for (int g = set; g < ngroups; g += 2) {
-        const int gg = ui * ngroups + g;
-        const int sg = ui * nstage + g / kGroupsPerStage, st = sg % a.ST;
-        const int ab = gg % kNA;
-        if (!*abort_flag && g % kGroupsPerStage <= 1)
+      for (int c = 0; c < nchunk; ++c) {
+        const int gc = ui * nchunk + c;
+        const int sg = ui * nstage + c / kChunksPerStage, st = sg % a.ST;
+        const int ab = gc % kNAB;
+        if (!*abort_flag && c % kChunksPerStage == 0)
           wait_or_abort<true>(&full[st], (sg / a.ST) & 1, abort_flag, a.err, kErrTcFullWait);
-        if (!*abort_flag && gg >= kNA)
-          wait_or_abort<true>(&mmadone[ab], ((gg / kNA) & 1) ^ 1, abort_flag, a.err, kErrTcMmaWait);
+        // the A buffer is free once the MMAs of chunk gc - kNAB completed
+        if (!*abort_flag && gc >= kNAB) {
+          const int pc = gc - kNAB;
+          wait_or_abort<true>(&accfull[pc % NACC], (pc / NACC) & 1, abort_flag, a.err, kErrTcMmaWait);
+        }
         tc_fence_after();
         if (!*abort_flag) {
-          const int j = g % kGroupsPerStage;
-          const uint32_t row = s_stages + st * a.stage_bytes + c_off + (j >> 2) * 16384 + r * 128;
-          const uint32_t c0 = 2 * (j & 3);
-          const uint4 lo = lds128(row + ((c0 ^ rsw) << 4));
-          const uint4 hi = lds128(row + (((c0 + 1) ^ rsw) << 4));
-          const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-          uint32_t o[32];
+          // the chunk's 256 k of this row: one 128-byte swizzled row of the codes tile
+          const uint32_t row = s_stages + st * a.stage_bytes + c_off + (c % kChunksPerStage) * 16384 + r * 128;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            uint32_t t4[4];
-            nib8_to_bf16x2_natural(w[i], t4);
+          for (int jj = 0; jj < kChunkGroups / 2; ++jj) {
+            const int j = 2 * h + jj;
+            const uint32_t c0 = 2 * j;
+            const uint4 lo = lds128(row + ((c0 ^ rsw) << 4));
+            const uint4 hi = lds128(row + (((c0 + 1) ^ rsw) << 4));
+            const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+            uint32_t o[32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) o[4 * i + c] = t4[c];
+            for (int i = 0; i < 8; ++i) {
+              uint32_t t4[4];
+              nib8_to_bf16x2_natural(w[i], t4);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) o[4 * i + q] = t4[q];
+            }
+            tmem_st32_nowait(tlane + ab * (kChunkGroups * 32) + j * 32, o);
           }
-          tmem_st32(tlane + ab * 32, o);
+          tmem_wait_st();
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&afull[ab]);
-          // this set's last group of the stage
-          if (g % kGroupsPerStage >= kGroupsPerStage - 2 || g + 2 >= ngroups) mbar_arrive(&empty[st]);
+          if (c % kChunksPerStage == kChunksPerStage - 1) mbar_arrive(&empty[st]);
         }
       }
     }
-  } else {
+  } else if (warp < 15) {
     // ---------------------------------------------------------------- epilogue (warps 11..14)
     const int q = warp & 3;
     const int row = q * 32 + lane;
-    const int et = threadIdx.x - 352;  // 0..127
+    const int et = threadIdx.x - 352;  // 0..127 (warps 11..14)
     const uint32_t tlane = tbase + ((uint32_t)(q * 32) << 16);
     for (int ui = 0, u = blockIdx.x; u < a.nunits; ++ui, u += gridDim.x) {
-      const int tile = u / a.splits, split = u % a.splits;
+      const int tile = u / a.splits;
       const int n0 = tile * kRows;
-      const float* sxu = sx + (size_t)(split * ngroups) * NT;
       float yacc[NT];
 #pragma unroll
       for (int m = 0; m < NT; ++m) yacc[m] = 0.f;
-      for (int g = 0; g < ngroups; ++g) {
-        const int gg = ui * ngroups + g;
-        const int sg = ui * nstage + g / kGroupsPerStage, st = sg % a.ST;
-        const int nb = gg % NB, ab = gg % kNA;
+      for (int c = 0; c < nchunk; ++c) {
+        const int gc = ui * nchunk + c;
+        const int sg = ui * nstage + c / kChunksPerStage, st = sg % a.ST;
+        const int nb = gc % NACC;
         // the epilogue releases accumulators on the MMA critical path: no backoff
-        if (!*abort_flag && g % kGroupsPerStage == 0)
+        if (!*abort_flag && c % kChunksPerStage == 0) {
           wait_or_abort<false>(&full[st], (sg / a.ST) & 1, abort_flag, a.err, kErrTcFullWait);
-        if (!*abort_flag) wait_or_abort<false>(&mmadone[ab], (gg / kNA) & 1, abort_flag, a.err, kErrTcAccWait);
+          wait_or_abort<false>(&sxfull[st], (sg / a.ST) & 1, abort_flag, a.err, kErrTcFullWait);
+        }
+        if (!*abort_flag) wait_or_abort<false>(&accfull[nb], (gc / NACC) & 1, abort_flag, a.err, kErrTcAccWait);
         tc_fence_after();
-        float acc[NT];
-        tmem_ld<NT>(tlane + nb * NT, acc);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&accempty[nb]);
         const uint32_t sb = s_stages + st * a.stage_bytes;
-        const int j = g % kGroupsPerStage;
-        const float s = f16_bits_to_f32(lds16(sb + s_off + row * 16 + 2 * j));
-        const float b = f16_bits_to_f32(lds16(sb + b_off + row * 16 + 2 * j));
-        const float c = fmaf(-128.f, s, b);
+        const int j0 = (c % kChunksPerStage) * kChunkGroups;  // first group of the chunk within the stage
+        const uint2 s4 = lds64(sb + s_off + row * 16 + 2 * j0);
+        const uint2 b4 = lds64(sb + b_off + row * 16 + 2 * j0);
+        const uint32_t sv[2] = {s4.x, s4.y}, bv[2] = {b4.x, b4.y};
+        // 64 accumulator columns per batch: all four groups (N = 16) or two (N = 32)
+        constexpr int G = 64 / NT;
 #pragma unroll
-        for (int m = 0; m < NT; ++m) yacc[m] = fmaf(s, acc[m], fmaf(c, sxu[g * NT + m], yacc[m]));
-        __syncwarp();
-        if (lane == 0 && (j == kGroupsPerStage - 1 || g == ngroups - 1)) mbar_arrive(&empty[st]);
+        for (int j1 = 0; j1 < kChunkGroups; j1 += G) {
+          uint32_t acc[G][NT];
+          tmem_ld_groups<G, NT>(tlane + nb * (kChunkGroups * NT) + j1 * NT, acc);
+          if (j1 + G == kChunkGroups) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&accempty[nb]);
+          }
+#pragma unroll
+          for (int jj = 0; jj < G; ++jj) {
+            const int j = j1 + jj;
+            const float s = f16_bits_to_f32((sv[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
+            const float b = f16_bits_to_f32((bv[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
+            const float cc = fmaf(-128.f, s, b);
+            const float* sxg = sx + (size_t)(st * kGroupsPerStage + j0 + j) * NT;
+#pragma unroll
+            for (int m = 0; m < NT; ++m) yacc[m] = fmaf(s, __uint_as_float(acc[jj][m]), fmaf(cc, sxg[m], yacc[m]));
+          }
+        }
+        if (c % kChunksPerStage == kChunksPerStage - 1) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[st]);
+        }
       }
       const int n = n0 + row;
       if (a.splits == 1) {
@@ -416,16 +430,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (*is_last) {
           __threadfence();
           if (n < a.N) {
-            for (int m = 0; m < a.M; ++m) {
-              float t = 0.f;
-              for (int s2 = 0; s2 < a.splits; ++s2)
-                t += __ldcg(a.partial + ((size_t)(tile * a.splits + s2) * NT + m) * kRows + row);
-              a.y[(size_t)m * a.N + n] = t;
+            // eight activation rows at a time: eight independent loads per split
+            for (int m0 = 0; m0 < a.M; m0 += 8) {
+              float t[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) t[i] = 0.f;
+              for (int s2 = 0; s2 < a.splits; ++s2) {
+                const float* ps = a.partial + ((size_t)(tile * a.splits + s2) * NT + m0) * kRows + row;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                  if (m0 + i < NT) t[i] += __ldcg(ps + i * kRows);
+              }
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                if (m0 + i < a.M) a.y[(size_t)(m0 + i) * a.N + n] = t[i];
             }
           }
           if (et == 0) a.counters[tile] = 0u;
         }
         epi_bar();
+      }
+    }
+  }
+
+  if (warp == 15) {
+    // ---------------------------------------------------------------- x sums (warp 15)
+    // sum of x over each 64-k group of a landed stage, per activation row, from
+    // the X tile in shared memory (the row's 128 bytes in any order)
+    for (int ui = 0, u = blockIdx.x; u < a.nunits; ++ui, u += gridDim.x) {
+      for (int s = 0; s < nstage; ++s) {
+        const int sg = ui * nstage + s, st = sg % a.ST;
+        if (!*abort_flag) wait_or_abort<true>(&full[st], (sg / a.ST) & 1, abort_flag, a.err, kErrTcFullWait);
+        const uint32_t xs = s_stages + st * a.stage_bytes + x_off;
+        for (int it = lane; it < kGroupsPerStage * NT; it += 32) {  // it = group * NT + row
+          const uint32_t src = xs + it * 128;
+          float t = 0.f;
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            const uint4 c4 = lds128(src + 16 * v);
+            const uint32_t e[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+            for (int hh = 0; hh < 4; ++hh) t += bf16_bits_to_f32(e[hh] & 0xFFFFu) + bf16_bits_to_f32(e[hh] >> 16);
+          }
+          sx[st * kGroupsPerStage * NT + it] = t;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&sxfull[st]);
+          mbar_arrive(&empty[st]);
+        }
       }
     }
   }
@@ -503,10 +556,11 @@ TcPlan tc_plan(int M, int N, int K, int sms) {
   p.kper = K / p.splits;
   p.nunits = p.ntiles * p.splits;
   p.stage_bytes = (uint32_t)(p.NT * 1024 + 36864);
-  const size_t fixed = 1024 + sizeof(float) * (size_t)(K / 64) * p.NT + 256;
+  const size_t fixed = 1024 + 256;  // alignment slack, barriers
   const size_t budget = 224 * 1024;
-  p.ST = (int)std::min<size_t>(4, (budget - fixed) / p.stage_bytes);
-  p.smem = fixed + (size_t)p.ST * p.stage_bytes;
+  const size_t per_stage = p.stage_bytes + sizeof(float) * kGroupsPerStage * p.NT;  // + x sums
+  p.ST = (int)std::min<size_t>(4, (budget - fixed) / per_stage);
+  p.smem = fixed + (size_t)p.ST * per_stage;
   p.ws_partial = p.splits > 1 ? sizeof(float) * (size_t)p.nunits * p.NT * kRows : 0;
   p.ws_counters = p.splits > 1 ? sizeof(uint32_t) * (size_t)p.ntiles : 0;
   return p;
