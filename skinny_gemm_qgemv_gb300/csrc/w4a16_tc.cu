@@ -7,7 +7,7 @@
 // and a 16-token verify batch gives the matrix units 16 rows of work (Uzu
 // article, section "Producing several tokens from one model pass").
 //
-// GB300 design (one persistent CTA per SM, 16 warps). The roles hand work to
+// GB300 design (one persistent CTA per SM, 15 warps). The roles hand work to
 // each other in chunks of 256 k (four 64-k groups): every mbarrier operation
 // costs tens to hundreds of cycles under load, so one hand-off per group would
 // pace the whole pipeline.
@@ -15,7 +15,7 @@
 //               128B-swizzled, one box per 64-k group), the 4-bit codes of 128
 //               weight rows (two 128B-swizzled boxes, one per chunk) and their
 //               fp16 scales and biases -- into a ring of shared-memory stages.
-//  warps 1, 2   MMA issuers (even / odd chunks): per group four
+//  warps 1, 2   MMA issuers (groups 0-1 / 2-3 of every chunk): per group four
 //               tcgen05.mma.kind::f16 (M = 128 weight rows, N = 16 or 32
 //               activation rows, K = 16) with A read from TMEM, each group into
 //               its own accumulator; one commit per chunk.
@@ -28,9 +28,9 @@
 //               it reads the four accumulators (tcgen05.ld) and folds
 //               y += s * acc + (b - 128 s) * sum_{k in g} x, the group-factored
 //               affine dot product, in fp32. The weights are never rounded to
-//               bf16: products are exact and only the fp32 sums round.
-//  warp 15      x sums: sum_{k in g} x per group and activation row, from the
-//               X tile of each landed stage, into a small ring beside it.
+//               bf16: products are exact and only the fp32 sums round. The
+//               sums of x per group come from the landed X tile, computed by
+//               the same warps while the chunk's MMAs run.
 // TMEM: columns 0..255 hold the accumulators (chunk buffers of 4 x N columns),
 // 256..511 two A chunk buffers of 4 x 32 columns.
 #include <cuda.h>
@@ -57,7 +57,7 @@ constexpr int kNAB = 2;             // A (converted weights) chunk buffers in TM
 constexpr uint32_t kAccCols = 256;  // TMEM columns for accumulators: chunk buffers of 4 x N columns
 constexpr uint32_t kACol = 256;     // first TMEM column of the A buffers
 constexpr uint32_t kTmemCols = 512;
-constexpr int kThreads = 512;  // 1 producer + 2 MMA + 8 converter + 4 epilogue + 1 x-sum warps
+constexpr int kThreads = 480;  // 1 producer + 2 MMA + 8 converter + 4 epilogue warps
 
 struct TcArgs {
   int N, K, M;
@@ -164,6 +164,24 @@ __device__ __forceinline__ void nib8_to_bf16x2_natural(uint32_t w, uint32_t (&o)
   o[3] = __byte_perm(t1, kMagic, 0x7352);
 }
 
+// two fp32 lanes in one 64-bit register, for the paired fp32 FMA (fma.rn.f32x2)
+__device__ __forceinline__ uint64_t pair2(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpair2(uint64_t v, float& lo, float& hi) {
+  uint32_t a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(a), "=r"(b) : "l"(v));
+  lo = __uint_as_float(a);
+  hi = __uint_as_float(b);
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 // Bounded wait that also honours the CTA-wide abort flag. Waiters off the
@@ -194,21 +212,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const gbase = smem_raw + (base - raw);
-  // shared layout: stages | sx [ST][8 groups][NT] f32 | barriers
+  // shared layout: stages | sx [2][4 groups][NT] f32 (x sums of a chunk) | barriers
   const uint32_t s_stages = base;
   const int nchunk = a.kper / kChunkK;
   const int nstage = a.kper / kStageK;
   float* sx = reinterpret_cast<float*>(gbase + a.ST * a.stage_bytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(
-      gbase + ((a.ST * a.stage_bytes + sizeof(float) * a.ST * kGroupsPerStage * NT + 7) & ~(size_t)7));
+      gbase + ((a.ST * a.stage_bytes + sizeof(float) * 2 * kChunkGroups * NT + 7) & ~(size_t)7));
   uint64_t* full = bars;
   uint64_t* empty = full + a.ST;
-  uint64_t* afull = empty + a.ST;      // a chunk of converted A is in TMEM
-  uint64_t* accfull = afull + kNAB;    // the MMAs of a chunk completed: accumulators ready, A buffer free
+  uint64_t* afull = empty + a.ST;      // [kNAB][2] half a chunk (two groups) of converted A is in TMEM
+  uint64_t* accfull = afull + 2 * kNAB;  // the MMAs of a chunk completed: accumulators ready, A buffer free
   uint64_t* accempty = accfull + NACC; // the epilogue has read a chunk's accumulators
   uint64_t* done = accempty + NACC;    // [2] all MMAs of an issuing warp completed
-  uint64_t* sxfull = done + 2;         // [ST] the x sums of a stage are in sx
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sxfull + a.ST);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 2);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   volatile uint32_t* is_last = tmem_slot + 2;
 
@@ -219,12 +236,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.ST; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 13);  // 8 converter warps + 4 epilogue warps + the x-sum warp
-      mbar_init(&sxfull[i], 1);
+      mbar_init(&empty[i], 12);  // 8 converter warps + 4 epilogue warps
     }
-    for (int i = 0; i < kNAB; ++i) mbar_init(&afull[i], 8);
+    for (int i = 0; i < 2 * kNAB; ++i) mbar_init(&afull[i], 4);
     for (int i = 0; i < NACC; ++i) {
-      mbar_init(&accfull[i], 1);
+      mbar_init(&accfull[i], 2);  // one commit per MMA warp
       mbar_init(&accempty[i], 4);
     }
     mbar_init(&done[0], 1);
@@ -273,26 +289,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(&full[j % a.ST], (j / a.ST) & 1, a.err, kErrTcDrain);
     }
   } else if (warp <= 2) {
-    // ------------------------------------------- MMA issuers: warp 1 even chunks, warp 2 odd chunks
+    // ------------------------- MMA issuers: warp 1 groups 0, 1 of every chunk, warp 2 groups 2, 3
     if (lane == 0) {
-      const int cset = warp - 1;
+      const int h = warp - 1;
       const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NT >> 3) << 17) |
                              ((uint32_t)(kRows >> 4) << 24);
       bool ok = true;
       for (int ui = 0, u = blockIdx.x; u < a.nunits && ok; ++ui, u += gridDim.x) {
-        for (int c = cset; c < nchunk && ok; c += 2) {
+        for (int c = 0; c < nchunk && ok; ++c) {
           const int gc = ui * nchunk + c;
           const int sg = ui * nstage + c / kChunksPerStage, st = sg % a.ST;
           const int ab = gc % kNAB, nb = gc % NACC;
-          ok = wait_or_abort<false>(&full[st], (sg / a.ST) & 1, abort_flag, a.err, kErrTcFullWait);
-          ok = ok && wait_or_abort<false>(&afull[ab], (gc / kNAB) & 1, abort_flag, a.err, kErrTcMmaWait);
+          if (c % kChunksPerStage == 0)
+            ok = wait_or_abort<false>(&full[st], (sg / a.ST) & 1, abort_flag, a.err, kErrTcFullWait);
+          ok = ok && wait_or_abort<false>(&afull[2 * ab + h], (gc / kNAB) & 1, abort_flag, a.err, kErrTcMmaWait);
           if (ok && gc >= NACC)
             ok = wait_or_abort<false>(&accempty[nb], ((gc / NACC) & 1) ^ 1, abort_flag, a.err, kErrTcAccWait);
           if (!ok) break;
           tc_fence_after();
           const uint32_t xs = s_stages + st * a.stage_bytes + x_off;
 #pragma unroll
-          for (int j = 0; j < kChunkGroups; ++j) {
+          for (int jj = 0; jj < kChunkGroups / 2; ++jj) {
+            const int j = 2 * h + jj;
             const int gi = (c % kChunksPerStage) * kChunkGroups + j;  // group within the stage
             const uint32_t at = tbase + kACol + ab * (kChunkGroups * 32) + j * 32;
             const uint32_t dt = tbase + nb * (kChunkGroups * NT) + j * NT;
@@ -303,8 +321,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(&accfull[nb]);
         }
       }
-      mma_commit(&done[cset]);
-      mbar_wait(&done[cset], 0, a.err, kErrTcDrain);
+      mma_commit(&done[h]);
+      mbar_wait(&done[h], 0, a.err, kErrTcDrain);
     }
   } else if (warp < 11) {
     // ------------------------------------------ converters: warps 3..10, every chunk
@@ -352,12 +370,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&afull[ab]);
+          mbar_arrive(&afull[2 * ab + h]);
           if (c % kChunksPerStage == kChunksPerStage - 1) mbar_arrive(&empty[st]);
         }
       }
     }
-  } else if (warp < 15) {
+  } else {
     // ---------------------------------------------------------------- epilogue (warps 11..14)
     const int q = warp & 3;
     const int row = q * 32 + lane;
@@ -366,22 +384,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int ui = 0, u = blockIdx.x; u < a.nunits; ++ui, u += gridDim.x) {
       const int tile = u / a.splits;
       const int n0 = tile * kRows;
-      float yacc[NT];
+      uint64_t yacc2[NT / 2];  // activation rows (2p, 2p + 1)
 #pragma unroll
-      for (int m = 0; m < NT; ++m) yacc[m] = 0.f;
+      for (int q2 = 0; q2 < NT / 2; ++q2) yacc2[q2] = 0ull;
       for (int c = 0; c < nchunk; ++c) {
         const int gc = ui * nchunk + c;
         const int sg = ui * nstage + c / kChunksPerStage, st = sg % a.ST;
         const int nb = gc % NACC;
         // the epilogue releases accumulators on the MMA critical path: no backoff
-        if (!*abort_flag && c % kChunksPerStage == 0) {
+        if (!*abort_flag && c % kChunksPerStage == 0)
           wait_or_abort<false>(&full[st], (sg / a.ST) & 1, abort_flag, a.err, kErrTcFullWait);
-          wait_or_abort<false>(&sxfull[st], (sg / a.ST) & 1, abort_flag, a.err, kErrTcFullWait);
+        const int j0 = (c % kChunksPerStage) * kChunkGroups;  // first group of the chunk within the stage
+        float* sxc = sx + (c & 1) * (kChunkGroups * NT);
+        {
+          // x sums of the chunk's groups while its MMAs run: a (group, activation
+          // row) pair per thread (N = 32) or per two threads (N = 16), from the
+          // row's 128 bytes of the landed X tile in any order
+          constexpr int kPer = 128 / (kChunkGroups * NT);  // threads per sum: 2 or 1
+          const int p = et / kPer, part = et % kPer;
+          const uint32_t src = s_stages + st * a.stage_bytes + x_off + ((j0 + p / NT) * NT + p % NT) * 128 +
+                               part * (128 / kPer);
+          float t0 = 0.f, t1 = 0.f;
+#pragma unroll
+          for (int v = 0; v < 8 / kPer; ++v) {
+            const uint4 c4 = lds128(src + 16 * v);
+            t0 += bf16_bits_to_f32(c4.x & 0xFFFFu) + bf16_bits_to_f32(c4.x >> 16);
+            t1 += bf16_bits_to_f32(c4.y & 0xFFFFu) + bf16_bits_to_f32(c4.y >> 16);
+            t0 += bf16_bits_to_f32(c4.z & 0xFFFFu) + bf16_bits_to_f32(c4.z >> 16);
+            t1 += bf16_bits_to_f32(c4.w & 0xFFFFu) + bf16_bits_to_f32(c4.w >> 16);
+          }
+          float t = t0 + t1;
+          if (kPer == 2) t += __shfl_xor_sync(0xFFFFFFFFu, t, 1);
+          if (part == 0) sxc[p] = t;
+          epi_bar();
         }
         if (!*abort_flag) wait_or_abort<false>(&accfull[nb], (gc / NACC) & 1, abort_flag, a.err, kErrTcAccWait);
         tc_fence_after();
         const uint32_t sb = s_stages + st * a.stage_bytes;
-        const int j0 = (c % kChunksPerStage) * kChunkGroups;  // first group of the chunk within the stage
         const uint2 s4 = lds64(sb + s_off + row * 16 + 2 * j0);
         const uint2 b4 = lds64(sb + b_off + row * 16 + 2 * j0);
         const uint32_t sv[2] = {s4.x, s4.y}, bv[2] = {b4.x, b4.y};
@@ -402,9 +441,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float s = f16_bits_to_f32((sv[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
             const float b = f16_bits_to_f32((bv[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
             const float cc = fmaf(-128.f, s, b);
-            const float* sxg = sx + (size_t)(st * kGroupsPerStage + j0 + j) * NT;
+            const uint64_t s2 = pair2(__float_as_uint(s), __float_as_uint(s));
+            const uint64_t c2 = pair2(__float_as_uint(cc), __float_as_uint(cc));
+            const uint64_t* sxg = reinterpret_cast<const uint64_t*>(sxc + j * NT);
 #pragma unroll
-            for (int m = 0; m < NT; ++m) yacc[m] = fmaf(s, __uint_as_float(acc[jj][m]), fmaf(cc, sxg[m], yacc[m]));
+            for (int q2 = 0; q2 < NT / 2; ++q2)
+              yacc2[q2] = ffma2(s2, pair2(acc[jj][2 * q2], acc[jj][2 * q2 + 1]), ffma2(c2, sxg[q2], yacc2[q2]));
           }
         }
         if (c % kChunksPerStage == kChunksPerStage - 1) {
@@ -412,6 +454,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(&empty[st]);
         }
       }
+      float yacc[NT];
+#pragma unroll
+      for (int q2 = 0; q2 < NT / 2; ++q2) unpair2(yacc2[q2], yacc[2 * q2], yacc[2 * q2 + 1]);
       const int n = n0 + row;
       if (a.splits == 1) {
         if (n < a.N) {
@@ -449,36 +494,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (et == 0) a.counters[tile] = 0u;
         }
         epi_bar();
-      }
-    }
-  }
-
-  if (warp == 15) {
-    // ---------------------------------------------------------------- x sums (warp 15)
-    // sum of x over each 64-k group of a landed stage, per activation row, from
-    // the X tile in shared memory (the row's 128 bytes in any order)
-    for (int ui = 0, u = blockIdx.x; u < a.nunits; ++ui, u += gridDim.x) {
-      for (int s = 0; s < nstage; ++s) {
-        const int sg = ui * nstage + s, st = sg % a.ST;
-        if (!*abort_flag) wait_or_abort<true>(&full[st], (sg / a.ST) & 1, abort_flag, a.err, kErrTcFullWait);
-        const uint32_t xs = s_stages + st * a.stage_bytes + x_off;
-        for (int it = lane; it < kGroupsPerStage * NT; it += 32) {  // it = group * NT + row
-          const uint32_t src = xs + it * 128;
-          float t = 0.f;
-#pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            const uint4 c4 = lds128(src + 16 * v);
-            const uint32_t e[4] = {c4.x, c4.y, c4.z, c4.w};
-#pragma unroll
-            for (int hh = 0; hh < 4; ++hh) t += bf16_bits_to_f32(e[hh] & 0xFFFFu) + bf16_bits_to_f32(e[hh] >> 16);
-          }
-          sx[st * kGroupsPerStage * NT + it] = t;
-        }
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&sxfull[st]);
-          mbar_arrive(&empty[st]);
-        }
       }
     }
   }
@@ -558,9 +573,9 @@ TcPlan tc_plan(int M, int N, int K, int sms) {
   p.stage_bytes = (uint32_t)(p.NT * 1024 + 36864);
   const size_t fixed = 1024 + 256;  // alignment slack, barriers
   const size_t budget = 224 * 1024;
-  const size_t per_stage = p.stage_bytes + sizeof(float) * kGroupsPerStage * p.NT;  // + x sums
-  p.ST = (int)std::min<size_t>(4, (budget - fixed) / per_stage);
-  p.smem = fixed + (size_t)p.ST * per_stage;
+  const size_t sx_bytes = sizeof(float) * 2 * kChunkGroups * p.NT;
+  p.ST = (int)std::min<size_t>(4, (budget - fixed - sx_bytes) / p.stage_bytes);
+  p.smem = fixed + sx_bytes + (size_t)p.ST * p.stage_bytes;
   p.ws_partial = p.splits > 1 ? sizeof(float) * (size_t)p.nunits * p.NT * kRows : 0;
   p.ws_counters = p.splits > 1 ? sizeof(uint32_t) * (size_t)p.ntiles : 0;
   return p;
