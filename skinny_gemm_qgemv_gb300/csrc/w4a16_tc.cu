@@ -402,12 +402,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           // row's 128 bytes of the landed X tile in any order
           constexpr int kPer = 128 / (kChunkGroups * NT);  // threads per sum: 2 or 1
           const int p = et / kPer, part = et % kPer;
-          const uint32_t src = s_stages + st * a.stage_bytes + x_off + ((j0 + p / NT) * NT + p % NT) * 128 +
-                               part * (128 / kPer);
+          const uint32_t src = s_stages + st * a.stage_bytes + x_off + ((j0 + p / NT) * NT + p % NT) * 128;
+          const uint32_t sw = (uint32_t)(p % NT) & 7;  // the tile's 128-byte swizzle of this row
           float t0 = 0.f, t1 = 0.f;
 #pragma unroll
           for (int v = 0; v < 8 / kPer; ++v) {
-            const uint4 c4 = lds128(src + 16 * v);
+            // physical 16-byte units part * 4 + v, spread over the banks by the swizzle
+            const uint4 c4 = lds128(src + ((((uint32_t)(part * (8 / kPer) + v)) ^ sw) << 4));
             t0 += bf16_bits_to_f32(c4.x & 0xFFFFu) + bf16_bits_to_f32(c4.x >> 16);
             t1 += bf16_bits_to_f32(c4.y & 0xFFFFu) + bf16_bits_to_f32(c4.y >> 16);
             t0 += bf16_bits_to_f32(c4.z & 0xFFFFu) + bf16_bits_to_f32(c4.z >> 16);
