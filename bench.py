@@ -491,8 +491,9 @@ def main():
     value = world * step_bytes / t_step / 1e9
 
     # ---------------- roofline of the dominant kernel. Every launch of the step
-    # is w4a16_gemv_kernel<1,64>, so its average launch duration is the
-    # event-timed step time / launches (the graph has no other node). Per-shape
+    # is an instance of w4a16_gemv_kernel<1, ...> (the row and k split per lane
+    # is picked per shape), so its average launch duration is the event-timed
+    # step time / launches (the graph has no other node). Per-shape
     # durations come from graphs holding the 36 launches of one projection kind.
     per_shape = {}
     for kind in ("q", "k", "o", "gate_up", "down", "lm_head"):
@@ -508,7 +509,7 @@ def main():
     traffic = kernel_traffic("w4a16_gemv_m1", step_bytes / launches)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                 "frac": achieved / hbm_peak, "traffic": traffic,
-                "kernel": "w4a16_gemv_kernel<1,64> (all 217 launches of the step)",
+                "kernel": "w4a16_gemv_kernel<1, ...> (all 217 launches of the step)",
                 "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)" if peak_src == "measured"
                 else "fallback 6.8 TB/s",
                 "avg_launch_us": k_time / launches * 1e6,
