@@ -59,17 +59,12 @@ MoeLayout moe_layout(int T, int H, int I, int E, int top_k) {
   L.h = take(sizeof(float) * P * I);
   L.hh = take(sizeof(uint16_t) * P * I);
   L.hexp = take(sizeof(int32_t) * P);
+  L.vexp = take(sizeof(int32_t) * (size_t)moe_nvirt_max(T, E, top_k) * kMxVexpInts);
+  L.nvirt = take(sizeof(int32_t) * 4);
+  L.hmax = take(sizeof(uint32_t) * P);
   L.partial = take(0);
   L.total = off;
   return L;
-}
-
-// power-of-two exponent sigma such that max|v| * 2^-sigma lies in [2^14, 2^15)
-__device__ __forceinline__ int fp16_prescale_exp(float amax) {
-  if (!(amax > 0.f)) return 0;
-  int e;
-  frexpf(amax, &e);  // amax = f * 2^e, f in [0.5, 1)
-  return e - 15;
 }
 
 // ---------------------------------------------------------------------------
@@ -385,12 +380,24 @@ cudaError_t launch_moe_mxfp4(const uint16_t* x, const float* logits, const uint8
                              const uint8_t* uq, const uint8_t* us, const uint8_t* dq, const uint8_t* ds, int T,
                              int H, int I, int E, int top_k, float* y, int32_t* idx, float* wts, void* ws,
                              uint32_t* err, cudaStream_t stream, bool pdl) {
-  (void)err;
   const MoeLayout L = moe_layout(T, H, I, E, top_k);
   uint8_t* base = static_cast<uint8_t*>(ws);
   auto I32 = [&](size_t off) { return reinterpret_cast<int32_t*>(base + off); };
   const int P = T * top_k;
   cudaError_t e;
+  const bool aligned = ((reinterpret_cast<uintptr_t>(gq) | reinterpret_cast<uintptr_t>(gs) |
+                         reinterpret_cast<uintptr_t>(uq) | reinterpret_cast<uintptr_t>(us) |
+                         reinterpret_cast<uintptr_t>(dq) | reinterpret_cast<uintptr_t>(ds)) & 15u) == 0;
+  if (aligned && P <= 1024 && moe_mx_tiles_ok(T, H, I, E, top_k)) {
+    // main path: routing + grouping in one CTA, then the two streamed expert GEMVs
+    e = launch_moe_mx_route(logits, x, T, H, E, top_k, idx, wts, I32(L.xexp), I32(L.order), I32(L.vexp),
+                            I32(L.nvirt), reinterpret_cast<uint32_t*>(base + L.hmax), stream, pdl);
+    if (e != cudaSuccess) return e;
+    return launch_moe_mx_tiles(gq, gs, uq, us, dq, ds, x, I32(L.xexp), I32(L.vexp), I32(L.nvirt), wts,
+                               reinterpret_cast<float*>(base + L.h), reinterpret_cast<uint32_t*>(base + L.hmax), y, T,
+                               H, I, E, top_k, err, stream, pdl);
+  }
+  // shapes outside the main path's tiling: one warp per row
   e = launch_kernel(moe_router_kernel, dim3(T), dim3(256), 0, stream, pdl, logits, x, H, E, top_k, idx, wts,
                     reinterpret_cast<uint16_t*>(base + L.xh), I32(L.xexp));
   if (e != cudaSuccess) return e;

@@ -122,6 +122,16 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 // ---------------------------------------------------------------------------
 // Shared-memory vector loads
 // ---------------------------------------------------------------------------
+// TMA tiled load of a 2D box into shared memory, completing on an mbarrier
+// (the box's innermost coordinate x must be 16-byte aligned).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tm, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
@@ -228,6 +238,53 @@ __device__ __forceinline__ void nib8_to_bf16x2_biased(uint32_t w, uint32_t (&o)[
 
 // Pack two bf16 bit patterns (low, high) into one register.
 __device__ __forceinline__ uint32_t pack2(uint32_t lo16, uint32_t hi16) { return (lo16 & 0xFFFFu) | (hi16 << 16); }
+
+// Sum R per-lane values over the 32 lanes of a warp with a transposed
+// butterfly: at offsets 16, 8, ... each lane keeps half of its remaining values
+// and adds its partner's copy of that half, so R values cost about
+// R - 1 + log2(32 / R) shuffles instead of 5 R. Afterwards lane L holds the
+// total of value transposed_row<R>(L).
+template <int R>
+__device__ __forceinline__ float transposed_warp_sum(float (&v)[R], int lane) {
+  int cnt = R;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    if (cnt > 1) {
+      const int half = cnt / 2;
+      const bool upper = lane & o;
+#pragma unroll
+      for (int i = 0; i < R / 2; ++i) {
+        if (i < half) {
+          const float keep = upper ? v[i + half] : v[i];
+          const float send = upper ? v[i] : v[i + half];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+      }
+      cnt = half;
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+    }
+  }
+  return v[0];
+}
+
+template <int R>
+__device__ __forceinline__ int transposed_row(int lane) {
+  int row = 0, half = R / 2;
+#pragma unroll
+  for (int o = 16; o >= 1 && half >= 1; o >>= 1, half >>= 1)
+    if (lane & o) row += half;
+  return row;
+}
+
+// power-of-two exponent sigma such that max|v| * 2^-sigma lies in [2^14, 2^15):
+// activations scaled by 2^-sigma fit fp16's range with the largest exponent
+__device__ __forceinline__ int fp16_prescale_exp(float amax) {
+  if (!(amax > 0.f)) return 0;
+  int e;
+  frexpf(amax, &e);  // amax = f * 2^e, f in [0.5, 1)
+  return e - 15;
+}
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

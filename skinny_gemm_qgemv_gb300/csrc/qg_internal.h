@@ -2,6 +2,7 @@
 // translation units and the C entry points in api.cu.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -78,12 +79,38 @@ cudaError_t launch_hadamard32_quant_i8(const uint16_t* x, const uint32_t* sign_b
 cudaError_t launch_w8a8_i32(const int8_t* a, const int8_t* w, int32_t* c, int M, int N, int K,
                             cudaStream_t stream, bool pdl);
 
-// MXFP4 MoE (moe_mxfp4.cu)
+// TMA tensor maps (tmap.cu): 2D {inner, outer} with a row stride, 3D
+// {inner, rows, chunks} with row and chunk strides; false if encoding fails.
+bool tmap_2d(CUtensorMap* tm, CUtensorMapDataType dt, const void* ptr, uint64_t inner, uint64_t outer,
+             uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);
+bool tmap_3d(CUtensorMap* tm, CUtensorMapDataType dt, const void* ptr, uint64_t inner, uint64_t rows,
+             uint64_t chunks, uint64_t row_bytes, uint64_t chunk_bytes, uint32_t box_inner, uint32_t box_rows,
+             uint32_t box_chunks);
+
+// MXFP4 MoE (moe_mxfp4.cu, moe_mx_tiles.cu)
+constexpr int kMxTC = 2;                // pairs of one virtual expert (held in registers)
+constexpr int kMxVexpInts = 2 + kMxTC;  // virtual-expert table entry: expert, pair count, pairs
+// upper bound of the virtual experts of a batch: every active expert once, plus
+// one more for every further kMxTC pairs
+inline int moe_nvirt_max(int T, int E, int top_k) {
+  const int P = T * top_k;
+  return (P < E ? P : E) + P / kMxTC;
+}
 struct MoeLayout {
   size_t pair_expert, pair_weight, counts, offsets, active, order, nactive, xh, xexp, h, hh, hexp, partial;
+  size_t vexp, nvirt, hmax;
   size_t total;
 };
 MoeLayout moe_layout(int T, int H, int I, int E, int top_k);
+bool moe_mx_tiles_ok(int T, int H, int I, int E, int top_k);
+cudaError_t launch_moe_mx_route(const float* logits, const uint16_t* x, int T, int H, int E, int top_k, int32_t* idx,
+                                float* wts, int32_t* xexp, int32_t* order, int32_t* vexp, int32_t* nvirt,
+                                uint32_t* hmax, cudaStream_t stream, bool pdl);
+cudaError_t launch_moe_mx_tiles(const uint8_t* gq, const uint8_t* gs, const uint8_t* uq, const uint8_t* us,
+                                const uint8_t* dq, const uint8_t* ds, const uint16_t* x, const int32_t* xexp,
+                                const int32_t* vexp, const int32_t* nvirt, const float* wts, float* h,
+                                uint32_t* hmax, float* y, int T, int H, int I, int E, int top_k, uint32_t* err,
+                                cudaStream_t stream, bool pdl);
 cudaError_t launch_moe_mxfp4(const uint16_t* x, const float* logits, const uint8_t* gq, const uint8_t* gs,
                              const uint8_t* uq, const uint8_t* us, const uint8_t* dq, const uint8_t* ds, int T,
                              int H, int I, int E, int top_k, float* y, int32_t* idx, float* wts, void* ws,

@@ -48,44 +48,6 @@ struct GemvArgs {
   uint32_t* err;
 };
 
-// Sum R per-lane values over the 32 lanes of a warp with a transposed
-// butterfly: at offsets 16, 8, ... each lane keeps half of its remaining values
-// and adds its partner's copy of that half, so R values cost about
-// R - 1 + log2(32 / R) shuffles instead of 5 R. Afterwards lane L holds the
-// total of value transposed_row<R>(L).
-template <int R>
-__device__ __forceinline__ float transposed_warp_sum(float (&v)[R], int lane) {
-  int cnt = R;
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    if (cnt > 1) {
-      const int half = cnt / 2;
-      const bool upper = lane & o;
-#pragma unroll
-      for (int i = 0; i < R / 2; ++i) {
-        if (i < half) {
-          const float keep = upper ? v[i + half] : v[i];
-          const float send = upper ? v[i] : v[i + half];
-          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-        }
-      }
-      cnt = half;
-    } else {
-      v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
-    }
-  }
-  return v[0];
-}
-
-template <int R>
-__device__ __forceinline__ int transposed_row(int lane) {
-  int row = 0, half = R / 2;
-#pragma unroll
-  for (int o = 16; o >= 1 && half >= 1; o >>= 1, half >>= 1)
-    if (lane & o) row += half;
-  return row;
-}
-
 template <int M, int KPL, int kRPW, int MINB>
 __global__ void __launch_bounds__(288, MINB) w4a16_gemv_kernel(const GemvArgs a) {
   constexpr int WPL = KPL / 8;  // 32-bit code words per lane per row
