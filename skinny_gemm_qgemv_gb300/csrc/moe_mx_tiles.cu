@@ -41,14 +41,14 @@ namespace qg {
 namespace {
 
 constexpr unsigned kFull = 0xFFFFFFFFu;
-constexpr int kGuWarps = 14;                       // gate/up consumer warps
-constexpr int kGuThreads = 32 * (kGuWarps + 1);
-constexpr int kDnWarps = 12;                       // down consumer warps
-constexpr int kDnThreads = 32 * (kDnWarps + 1);
 constexpr size_t kSmemBudget = 224 * 1024;
-// rows per consumer warp: more when a virtual expert holds a single pair (T = 1)
+// Consumer warps and rows per warp. With one pair per virtual expert (T = 1)
+// the activations take 16 registers, so more warps fit the register file.
+constexpr int gu_warps(int tc) { return tc == 1 ? 21 : 14; }
+constexpr int dn_warps(int tc) { return tc == 1 ? 24 : 12; }
 constexpr int gu_rpw(int) { return 4; }
-constexpr int dn_rpw(int tc) { return tc == 1 ? 8 : 4; }
+constexpr int dn_rpw(int) { return 4; }
+constexpr int kMaxSlices = 12;  // K / 1024 of either matrix (one 32-k block per lane)
 
 struct MxGateUpArgs {
   const uint8_t* gq;
@@ -280,7 +280,8 @@ __global__ void __launch_bounds__(1024) moe_mx_route_kernel(const float* __restr
 // TC: pairs per virtual expert held in registers (1 when every virtual expert
 // has one pair, else kMxTC); the tile is RG x RPW rows
 template <int TC>
-__global__ void __launch_bounds__(kGuThreads, 1) moe_mx_gateup_kernel(const MxGateUpArgs a) {
+__global__ void __launch_bounds__(32 * (gu_warps(TC) + 1), 1) moe_mx_gateup_kernel(const MxGateUpArgs a) {
+  constexpr int kGuWarps = gu_warps(TC);
   constexpr int RPW = gu_rpw(TC);
   constexpr int V = RPW * TC * 2;  // values per lane: rows x pairs x {gate, up}
   extern __shared__ __align__(128) uint8_t smem[];
@@ -447,8 +448,9 @@ __global__ void __launch_bounds__(kGuThreads, 1) moe_mx_gateup_kernel(const MxGa
 // down + routing-weighted combine
 // ---------------------------------------------------------------------------
 template <int TC>
-__global__ void __launch_bounds__(kDnThreads, 1)
+__global__ void __launch_bounds__(32 * (dn_warps(TC) + 1), 1)
     moe_mx_down_kernel(const __grid_constant__ CUtensorMap tm_h, const MxDownArgs a) {
+  constexpr int kDnWarps = dn_warps(TC);
   constexpr int RPW = dn_rpw(TC);
   constexpr int V = RPW * TC;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -630,7 +632,7 @@ struct MxPlan {
 MxPlan plan_gateup(int H, int I, int tc) {
   MxPlan p{};
   p.S = (H / 32 + 31) / 32;
-  p.RG = kGuWarps / p.S;
+  p.RG = gu_warps(tc) / p.S;
   p.R = p.RG * gu_rpw(tc);
   p.stage_bytes = (uint32_t)(2 * p.R * (H / 2 + H / 32));
   const size_t fixed = sizeof(float) * ((size_t)4 * p.S * p.RG * 32 + p.RG * 32) + 3 * 4 * 8 + 64;
@@ -644,7 +646,7 @@ MxPlan plan_gateup(int H, int I, int tc) {
 MxPlan plan_down(int T, int H, int I, int E, int top_k, int tc) {
   MxPlan p{};
   p.S = (I / 32 + 31) / 32;
-  p.RG = kDnWarps / p.S;
+  p.RG = dn_warps(tc) / p.S;
   p.R = p.RG * dn_rpw(tc);
   const uint32_t o_h = (uint32_t)((p.R * (I / 2 + I / 32) + 1023) & ~1023);
   p.stage_bytes = (uint32_t)((o_h + tc * I * 4 + 1023) & ~1023);
@@ -664,7 +666,7 @@ MxPlan plan_down(int T, int H, int I, int E, int top_k, int tc) {
 bool moe_mx_tiles_ok(int T, int H, int I, int E, int top_k) {
   if (H % 512 || I % 512) return false;       // 16-byte aligned rows of E8M0 scales
   if (E > kRouteLogits || T * top_k > 1024) return false;  // routing in one CTA
-  if (H / 1024 > kGuWarps || I / 1024 > kDnWarps) return false;
+  if (H / 1024 > kMaxSlices || I / 1024 > kMaxSlices) return false;
   if (I / 32 > 256) return false;  // one TMA box of h per pair
   const int tc = T == 1 ? 1 : kMxTC;
   if (plan_gateup(H, I, tc).ST < 2) return false;
@@ -694,7 +696,7 @@ static cudaError_t launch_mx_tc(const uint8_t* gq, const uint8_t* gs, const uint
                   pg.S, pg.RG, pg.R, pg.ST, pg.count, pg.stage_bytes, err};
   cudaError_t e = allow_max_smem(moe_mx_gateup_kernel<TC>);
   if (e != cudaSuccess) return e;
-  e = launch_kernel(moe_mx_gateup_kernel<TC>, dim3(sms), dim3(kGuThreads), pg.smem, stream, pdl, ga);
+  e = launch_kernel(moe_mx_gateup_kernel<TC>, dim3(sms), dim3(32 * (gu_warps(TC) + 1)), pg.smem, stream, pdl, ga);
   if (e != cudaSuccess) return e;
   const MxPlan pd = plan_down(T, H, I, E, top_k, TC);
   MxDownArgs da{dq, ds, h, hmax, wts, vexp, nvirt, y, T, H, I, top_k,
@@ -706,8 +708,8 @@ static cudaError_t launch_mx_tc(const uint8_t* gq, const uint8_t* gs, const uint
     return cudaErrorInvalidValue;
   e = allow_max_smem(moe_mx_down_kernel<TC>);
   if (e != cudaSuccess) return e;
-  return launch_kernel(moe_mx_down_kernel<TC>, dim3(std::min(sms, pd.count)), dim3(kDnThreads), pd.smem, stream,
-                       pdl, tm_h, da);
+  return launch_kernel(moe_mx_down_kernel<TC>, dim3(std::min(sms, pd.count)), dim3(32 * (dn_warps(TC) + 1)), pd.smem,
+                       stream, pdl, tm_h, da);
 }
 
 cudaError_t launch_moe_mx_tiles(const uint8_t* gq, const uint8_t* gs, const uint8_t* uq, const uint8_t* us,
