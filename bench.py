@@ -455,7 +455,11 @@ def main():
     step_bytes = sum(w4_bytes(N, K) for (_, N, K, *_r) in mats)
     launches = len(mats)
 
-    g = capture(lambda: run_stack(q, mats, xs, ys, 1, stream), stream)
+    # The step as one persistent grouped launch over the 217 projections (each
+    # has its own activation vector, so they are independent); the same step
+    # as 217 separate launches is measured below for comparison.
+    grp = q.GemvGroup([(wq, s, b, x[0], y[0]) for (_, N, K, wq, s, b), x, y in zip(mats, xs, ys)])
+    g = capture(lambda: grp.run(stream), stream)
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
             g.replay()
@@ -490,11 +494,15 @@ def main():
     t_step = float(tmax.item())
     value = world * step_bytes / t_step / 1e9
 
-    # ---------------- roofline of the dominant kernel. Every launch of the step
-    # is an instance of w4a16_gemv_kernel<1, ...> (the row and k split per lane
-    # is picked per shape), so its average launch duration is the event-timed
-    # step time / launches (the graph has no other node). Per-shape
-    # durations come from graphs holding the 36 launches of one projection kind.
+    # ---------------- the same step as 217 launches (one per projection) in one graph
+    g217 = capture(lambda: run_stack(q, mats, xs, ys, 1, stream), stream)
+    t217 = replay_timed(g217, max(20, min(args.steps, 500)), stream)
+    del g217
+
+    # ---------------- roofline of the dominant kernel: the step is one launch of
+    # w4a16_group_kernel (the graph has no other node), so its launch duration
+    # is the event-timed step time. Per-shape durations of the per-projection
+    # kernel come from graphs holding the 36 launches of one projection kind.
     per_shape = {}
     for kind in ("q", "k", "o", "gate_up", "down", "lm_head"):
         sel = [i for i, m in enumerate(mats) if m[0].split(".")[-1] == kind]
@@ -506,14 +514,17 @@ def main():
         del gk
     k_time = t_step
     achieved = step_bytes / k_time / 1e9
-    traffic = kernel_traffic("w4a16_gemv_m1", step_bytes / launches)
+    traffic = kernel_traffic("w4a16_group_m1", step_bytes)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                 "frac": achieved / hbm_peak, "traffic": traffic,
-                "kernel": "w4a16_gemv_kernel<1, ...> (all 217 launches of the step)",
+                "kernel": "w4a16_group_kernel (one launch per step over the 217 projections)",
                 "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)" if peak_src == "measured"
                 else "fallback 6.8 TB/s",
-                "avg_launch_us": k_time / launches * 1e6,
-                "alg_bytes_per_launch": step_bytes / launches, "per_shape": per_shape}
+                "avg_launch_us": k_time * 1e6, "alg_bytes_per_launch": step_bytes,
+                "per_launch_form": {"kernel": "w4a16_gemv_kernel<1, ...>", "launches_per_step": launches,
+                                    "GB_per_s": world * step_bytes / t217 / 1e9,
+                                    "frac": step_bytes / t217 / 1e9 / hbm_peak, "ms_per_step": t217 * 1e3,
+                                    "per_shape": per_shape}}
 
     # ---------------- e2e through the public API with host buffers
     xh = torch.empty(sum(x.numel() for x in xs), dtype=torch.bfloat16).pin_memory()
@@ -528,9 +539,11 @@ def main():
         o2 += y.numel()
     xh.copy_(torch.cat([x.reshape(-1) for x in xs]).cpu())
 
+    grp_e2e = q.GemvGroup([(wq, s, b, x[0], y[0]) for (_, N, K, wq, s, b), x, y in zip(mats, xv, yv)])
+
     def e2e_step():
         xd.copy_(xh, non_blocking=True)
-        run_stack(q, mats, xv, yv, 1, stream)
+        grp_e2e.run(stream)
         yh.copy_(yd, non_blocking=True)
     ge = capture(e2e_step, stream)
     with torch.cuda.stream(stream):
@@ -545,8 +558,8 @@ def main():
         t_e2e = (time.perf_counter() - t0) / n_e2e
     e2e = {"value": world * step_bytes / t_e2e / 1e9, "unit": "GB/s", "h2d_bytes_per_step": xh.numel() * 2,
            "d2h_bytes_per_step": yh.numel() * 4,
-           "how": "pinned host x -> device, 217 C-ABI GEMV calls, device y -> pinned host, one CUDA graph per "
-                  "step, host-timed including the final synchronize"}
+           "how": "pinned host x -> device, one C-ABI grouped GEMV run over the 217 projections, device y -> "
+                  "pinned host, one CUDA graph per step, host-timed including the final synchronize"}
 
     extras = {}
     if not args.no_extras and rank == 0:
@@ -588,12 +601,15 @@ def main():
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": "decode layer stack of a dense 9B-class decoder, M=1: 36 x (q, k, v, o, "
                                    "gate+up, down) + lm_head 151936x4096, W4A16 affine g64, 217 GEMVs per step",
-                       "bytes_per_step": step_bytes, "launches_per_step": launches,
+                       "bytes_per_step": step_bytes, "gemvs_per_step": launches,
+                       "issue": "one persistent grouped launch over the 217 independent projections (each with "
+                                "its own activation vector); roofline.per_launch_form has the same step as 217 "
+                                "launches",
                        "l2": f"inputs {step_bytes / 1e9:.2f} GB > L2 {l2 / 1e6:.0f} MB (no flush needed)",
                        "parallelism": f"replicas x{world}", "frac_of_peak": value / world / hbm_peak,
                        "tokens_per_s": world / t_step},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks.summary(),
-            "gpu_launches": launches * args.steps, "extras": extras,
+            "gpu_launches": args.steps, "extras": extras,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

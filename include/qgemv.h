@@ -107,6 +107,52 @@ QG_API qg_status qgemv_w4a16(const uint32_t *wq, const uint16_t *scales_f16,
 QG_API size_t qg_gemv_workspace_size(int N, int K, int group_size);
 
 /*
+ * qgemv_w4a16_group_* -- many independent M = 1 projections (each y_i = W_i x_i
+ * as in qgemv_w4a16) in one persistent launch. "MLX Runner ...", section
+ * "Architecture: one command buffer per token", issues all of a token's work
+ * as one unit; here the row tiles of every projection in the group are streamed
+ * back to back by one kernel, so the weight stream does not stop between
+ * projections. The projections must not depend on each other: a launch reads
+ * every x_i and writes every y_i in no particular order.
+ *
+ *   qg_w4_gemv_desc  one projection: the arguments of qgemv_w4a16 with the
+ *                    same layouts (wq uint32 [N][K/8], scales/biases fp16
+ *                    [N][K/64], x bf16 [K], y fp32 [N]); every pointer 16-byte
+ *                    aligned device memory of the current device; N >= 1;
+ *                    K a multiple of 2048 and at most 16384 (other K return
+ *                    QG_ERR_UNSUPPORTED).
+ *   qgemv_w4a16_group_create  validates the count descriptors (group_size 64),
+ *                    splits the tiles of all projections into one range per
+ *                    CTA with equal bytes, and copies that plan to device
+ *                    memory it allocates (cudaMalloc, synchronous copies).
+ *                    The descriptors' buffers are used by every later run:
+ *                    they must stay allocated until the group is destroyed.
+ *                    *group is set on QG_OK.
+ *   qgemv_w4a16_group_run     one launch on stream computing every y_i from
+ *                    the current contents of x_i and W_i; stream-ordered, no
+ *                    allocation, capturable in a CUDA graph. Run it on the
+ *                    device that was current at create.
+ *   qgemv_w4a16_group_destroy frees the plan (NULL is ignored); no run of the
+ *                    group may be pending.
+ */
+typedef struct qg_w4_gemv_desc {
+  const uint32_t *wq;
+  const uint16_t *scales_f16;
+  const uint16_t *biases_f16;
+  const uint16_t *x_bf16;
+  float *y;
+  int N;
+  int K;
+} qg_w4_gemv_desc;
+
+typedef struct qg_w4_group qg_w4_group;
+
+QG_API qg_status qgemv_w4a16_group_create(const qg_w4_gemv_desc *descs, int count, int group_size,
+                                          qg_w4_group **group);
+QG_API qg_status qgemv_w4a16_group_run(const qg_w4_group *group, void *stream);
+QG_API void qgemv_w4a16_group_destroy(qg_w4_group *group);
+
+/*
  * qgemm_w4a16_skinny -- Y = X W^T for a few activation rows, each weight read
  * once for all rows ("Krill Teardown", "Core mechanisms"; Uzu article,
  * "Producing several tokens from one model pass").

@@ -7,7 +7,7 @@ there is no fallback path. PyTorch only supplies device memory and streams.
 
 Entry points (same names as the C ABI):
   qgemv_w4a16, qgemm_w4a16_skinny, moe_mxfp4_expert_forward,
-  hadamard32_quant_i8, gemm_w8a8_i32
+  hadamard32_quant_i8, gemm_w8a8_i32; GemvGroup wraps qgemv_w4a16_group_*
 """
 from __future__ import annotations
 
@@ -28,7 +28,13 @@ EXPORTS = [
     "qg_skinny_workspace_size", "moe_mxfp4_expert_forward", "qg_moe_workspace_size",
     "qg_moe_workspace_h_offset", "hadamard32_quant_i8", "gemm_w8a8_i32", "qg_set_pdl", "qg_device_error",
     "moe_mxfp4_expert_forward_noalloc", "qg_moe_noalloc_max_bytes",
+    "qgemv_w4a16_group_create", "qgemv_w4a16_group_run", "qgemv_w4a16_group_destroy",
 ]
+
+
+class _GemvDesc(ctypes.Structure):
+    _fields_ = [("wq", ctypes.c_void_p), ("scales_f16", ctypes.c_void_p), ("biases_f16", ctypes.c_void_p),
+                ("x_bf16", ctypes.c_void_p), ("y", ctypes.c_void_p), ("N", ctypes.c_int), ("K", ctypes.c_int)]
 
 
 class QGError(RuntimeError):
@@ -78,6 +84,12 @@ def lib() -> ctypes.CDLL:
         L.moe_mxfp4_expert_forward_noalloc.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, P, P, P, P]
         L.qg_moe_noalloc_max_bytes.restype = Z
         L.qg_moe_noalloc_max_bytes.argtypes = []
+        L.qgemv_w4a16_group_create.restype = I
+        L.qgemv_w4a16_group_create.argtypes = [ctypes.POINTER(_GemvDesc), I, I, ctypes.POINTER(P)]
+        L.qgemv_w4a16_group_run.restype = I
+        L.qgemv_w4a16_group_run.argtypes = [P, P]
+        L.qgemv_w4a16_group_destroy.restype = None
+        L.qgemv_w4a16_group_destroy.argtypes = [P]
         _lib = L
     return _lib
 
@@ -148,6 +160,41 @@ def qgemm_w4a16_skinny(wq, scales, biases, x, y=None, workspace=None, stream=Non
                                     K // scales.shape[1], _p(workspace), ws_bytes, _stream(stream)),
            "qgemm_w4a16_skinny")
     return y
+
+
+class GemvGroup:
+    """Many independent M = 1 projections run as one persistent launch.
+
+    `items` is a list of (wq, scales, biases, x, y) CUDA tensors with the
+    layouts of qgemv_w4a16 (y preallocated, fp32 [N]). The tensors are held
+    by the group: every run reads the x's and writes the y's in place."""
+
+    def __init__(self, items):
+        descs = (_GemvDesc * len(items))()
+        for d, (wq, s, b, x, y) in zip(descs, items):
+            for t, nb, n in ((wq, 4, "wq"), (s, 2, "scales"), (b, 2, "biases"), (x, 2, "x"), (y, 4, "y")):
+                _need(t, nb, n)
+            d.wq, d.scales_f16, d.biases_f16 = wq.data_ptr(), s.data_ptr(), b.data_ptr()
+            d.x_bf16, d.y = x.data_ptr(), y.data_ptr()
+            d.N, d.K = wq.shape[0], wq.shape[1] * 8
+        self._items = list(items)
+        self._h = ctypes.c_void_p()
+        _check(lib().qgemv_w4a16_group_create(descs, len(items), 64, ctypes.byref(self._h)),
+               "qgemv_w4a16_group_create")
+
+    def run(self, stream=None):
+        _check(lib().qgemv_w4a16_group_run(self._h, _stream(stream)), "qgemv_w4a16_group_run")
+
+    def close(self):
+        if self._h:
+            lib().qgemv_w4a16_group_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def moe_workspace_size(T, H, I, E, top_k):

@@ -9,6 +9,8 @@
 
 #include <cstdint>
 #include <mutex>
+#include <new>
+#include <vector>
 
 #include "qg_common.cuh"
 #include "qg_internal.h"
@@ -133,6 +135,51 @@ qg_status qgemv_w4a16(const uint32_t* wq, const uint16_t* scales_f16, const uint
   if (ws_bytes < qg_gemv_workspace_size(N, K, group_size)) return QG_ERR_WORKSPACE;
   if (ws_bytes && !workspace) return QG_ERR_INVALID_ARG;
   return run_w4(wq, scales_f16, biases_f16, x_bf16, y, 1, N, K, workspace, ws_bytes, stream);
+}
+
+struct qg_w4_group {
+  qg::GroupPlan plan;
+};
+
+qg_status qgemv_w4a16_group_create(const qg_w4_gemv_desc* descs, int count, int group_size, qg_w4_group** group) {
+  if (!descs || !group || count < 1) return QG_ERR_INVALID_ARG;
+  std::vector<qg::GroupGemv> list(count);
+  for (int i = 0; i < count; ++i) {
+    const qg_w4_gemv_desc& d = descs[i];
+    qg_status st = check_w4(d.wq, d.scales_f16, d.biases_f16, d.x_bf16, d.y, 1, d.N, d.K, group_size);
+    if (st != QG_OK) return st;
+    if (!qg::group_gemv_ok(d.N, d.K)) return QG_ERR_UNSUPPORTED;
+    qg::GroupGemv g{};
+    g.wq = d.wq;
+    g.scales = d.scales_f16;
+    g.biases = d.biases_f16;
+    g.x = d.x_bf16;
+    g.y = d.y;
+    g.N = d.N;
+    g.K = d.K;
+    list[i] = g;
+  }
+  auto* out = new (std::nothrow) qg_w4_group();
+  if (!out) return QG_ERR_CUDA;
+  if (qg::group_plan_build(list.data(), count, qg::device_sm_count(), &out->plan) != cudaSuccess) {
+    delete out;
+    return QG_ERR_CUDA;
+  }
+  *group = out;
+  return QG_OK;
+}
+
+qg_status qgemv_w4a16_group_run(const qg_w4_group* group, void* stream) {
+  if (!group) return QG_ERR_INVALID_ARG;
+  uint32_t* err = err_word();
+  if (!err) return QG_ERR_CUDA;
+  return from_cuda(qg::group_launch(group->plan, err, static_cast<cudaStream_t>(stream), g_pdl));
+}
+
+void qgemv_w4a16_group_destroy(qg_w4_group* group) {
+  if (!group) return;
+  qg::group_plan_free(&group->plan);
+  delete group;
 }
 
 qg_status qgemm_w4a16_skinny(const uint32_t* wq, const uint16_t* scales_f16, const uint16_t* biases_f16,

@@ -79,6 +79,32 @@ cudaError_t launch_hadamard32_quant_i8(const uint16_t* x, const uint32_t* sign_b
 cudaError_t launch_w8a8_i32(const int8_t* a, const int8_t* w, int32_t* c, int M, int N, int K,
                             cudaStream_t stream, bool pdl);
 
+// Grouped M = 1 W4A16 GEMV (w4a16_group.cu): one persistent launch over a list
+// of independent projections. The caller fills wq, scales, biases, x, y, N, K;
+// group_plan_build fills the tiling fields and uploads the list.
+struct GroupGemv {
+  const uint32_t* wq;
+  const uint16_t* scales;
+  const uint16_t* biases;
+  const uint16_t* x;
+  float* y;
+  int N, K;
+  int S, RG, R;          // K-slices, row groups, rows per tile
+  int tile0, tile_end;   // the projection's tiles in the group's tile list
+  int pad;
+};
+struct GroupPlan {
+  GroupGemv* d_gemvs;
+  int* d_cta;  // [grid + 1] first tile of each CTA
+  int ngemv, grid, ST;
+  uint32_t stage_bytes;
+  size_t smem;
+};
+bool group_gemv_ok(int N, int K);
+cudaError_t group_plan_build(const GroupGemv* list, int n, int sms, GroupPlan* out);
+void group_plan_free(GroupPlan* p);
+cudaError_t group_launch(const GroupPlan& p, uint32_t* err, cudaStream_t stream, bool pdl);
+
 // TMA tensor maps (tmap.cu): 2D {inner, outer} with a row stride, 3D
 // {inner, rows, chunks} with row and chunk strides; false if encoding fails.
 bool tmap_2d(CUtensorMap* tm, CUtensorMapDataType dt, const void* ptr, uint64_t inner, uint64_t outer,

@@ -90,3 +90,27 @@ def test_hadamard_and_w8a8_validation(L):
     assert g(P(A), P(A), P(A), 33, 64, 128, None) == 1       # M > 32
     assert g(P(A), P(A), P(A), 16, 64, 1 << 20, None) == 1   # K too large for int32
     assert g(P(A + 1), P(A), P(A), 16, 64, 128, None) == 2
+
+
+def test_gemv_group_validation(L):
+    Desc = q._GemvDesc
+    out = P()
+
+    def make(*shapes, ptr=A):
+        ds = (Desc * len(shapes))()
+        for d, (N, K) in zip(ds, shapes):
+            d.wq = d.scales_f16 = d.biases_f16 = d.x_bf16 = d.y = ptr
+            d.N, d.K = N, K
+        return ds
+
+    f = L.qgemv_w4a16_group_create
+    assert f(make((16, 4096)), 0, 64, ctypes.byref(out)) == 1               # empty group
+    assert f(None, 1, 64, ctypes.byref(out)) == 1
+    assert f(make((16, 4096)), 1, 64, None) == 1
+    assert f(make((16, 4096), (0, 4096)), 2, 64, ctypes.byref(out)) == 1    # N < 1
+    assert f(make((16, 4096), (8, 1024)), 2, 64, ctypes.byref(out)) == 3    # K % 2048
+    assert f(make((16, 32768)), 1, 64, ctypes.byref(out)) == 3              # K > 16384
+    assert f(make((16, 4096)), 1, 32, ctypes.byref(out)) == 3               # group 32
+    assert f(make((16, 4096), ptr=A + 4), 1, 64, ctypes.byref(out)) == 2   # misaligned
+    assert L.qgemv_w4a16_group_run(None, None) == 1
+    L.qgemv_w4a16_group_destroy(None)
