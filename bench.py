@@ -361,7 +361,7 @@ def bench_w8a8(q, dev, stream, N, l2_bytes):
 # --------------------------------------------------------------------------- single cases (profiling)
 
 CASES = ["gemv_lm_head", "gemv_down", "gemv_q", "skinny16_gate_up", "skinny16_down", "moe_T1", "moe_T16",
-         "w8a8_12288", "hadamard_16x4096"]
+         "w8a8_12288", "hadamard_16x4096", "gemv_group_4layers"]
 
 
 def run_case(args):
@@ -383,6 +383,13 @@ def run_case(args):
         f = (lambda: q.qgemv_w4a16(wq, s, b, x[0], y[0])) if M == 1 else \
             (lambda: q.qgemm_w4a16_skinny(wq, s, b, x, y))
         nbytes = w4_bytes(N, K, M)
+    elif c == "gemv_group_4layers":
+        # the grouped launch over 4 decoder layers + the lm_head (0.78 GB)
+        mats = build_stack(q, dev, 1, layers=4)
+        xs, ys = stack_io(mats, dev, 1)
+        grp = q.GemvGroup([(wq, s, b, x[0], y[0]) for (_, N, K, wq, s, b), x, y in zip(mats, xs, ys)])
+        f = grp.run
+        nbytes = sum(w4_bytes(N, K) for (_, N, K, *_r) in mats)
     elif c.startswith("moe_"):
         T = int(c[5:])
         E, H, I, k = 64, 7168, 2048, 16

@@ -10,12 +10,14 @@
 //
 // Design (same per-tile arithmetic as the M = 1 kernel in w4a16_gemv.cu):
 //  * The row tiles of all projections form one list; the host splits it into
-//    one contiguous range per CTA with equal bytes (two CTAs per SM). A CTA's
+//    one contiguous range per CTA with equal cost (two CTAs per SM; a tile's
+//    cost is its bytes over the fraction of consumer warps it keeps busy). A CTA's
 //    producer warp streams its range (codes, scales, biases of R whole rows,
 //    three contiguous byte ranges) with cp.async.bulk into a ring of shared
 //    memory stages; the HBM addresses of a CTA are sequential.
-//  * Eight consumer warps: lane l of K-slice s covers 64 consecutive k, so a
-//    projection with K = 2048 S uses S slices and 8 / S row groups of 4 rows.
+//  * Twelve consumer warps: lane l of K-slice s covers 64 consecutive k, so a
+//    projection with K = 2048 S uses S slices and 12 / S row groups of 4 rows
+//    (every tile then holds 96 K-rows' worth of codes, 55 KB).
 //    When the range crosses into the next projection the consumers reload
 //    their activations (x is small and stays in L2).
 //  * Dequant and fold as in the single GEMV: (word >> 4j) & 0x000F000F |
@@ -36,10 +38,15 @@ namespace {
 
 constexpr int kGrpKPL = 64;               // k per lane
 constexpr int kGrpRPW = 4;                // rows per warp
-constexpr int kGrpWarps = 8;              // consumer warps
+// 12 consumer warps: K = 2048 S with S = 1, 2, 3, 4, 6 slices keeps every
+// warp busy (S = 6 is the K = 12288 down projection); two CTAs per SM.
+constexpr int kGrpWarps = 12;             // consumer warps
+constexpr int kGrpCtasPerSm = 2;
+constexpr size_t kGrpSmemBudget = 111 * 1024;
+constexpr int kGrpMaxSlices = 8;          // K <= 16384
 constexpr int kGrpThreads = 32 * (kGrpWarps + 1);
 constexpr int kGrpWPL = kGrpKPL / 8;      // code words per lane per row
-constexpr int kGrpRed = kGrpWarps * kGrpRPW;  // red floats per stage: S * R <= 8 * RPW
+constexpr int kGrpRed = kGrpWarps * kGrpRPW;  // red floats per stage: S * R <= warps * RPW
 
 struct GroupArgs {
   const GroupGemv* gemvs;
@@ -52,7 +59,7 @@ struct GroupArgs {
 
 }  // namespace
 
-__global__ void __launch_bounds__(kGrpThreads, 2) w4a16_group_kernel(const GroupArgs a) {
+__global__ void __launch_bounds__(kGrpThreads, kGrpCtasPerSm) w4a16_group_kernel(const GroupArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // shared layout: [ST stages][stage_bytes] | red [ST][kGrpRed] f32 | barriers
@@ -215,7 +222,7 @@ __global__ void __launch_bounds__(kGrpThreads, 2) w4a16_group_kernel(const Group
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-bool group_gemv_ok(int N, int K) { return N >= 1 && K >= 2048 && K % 2048 == 0 && K / 2048 <= kGrpWarps; }
+bool group_gemv_ok(int N, int K) { return N >= 1 && K >= 2048 && K % 2048 == 0 && K / 2048 <= kGrpMaxSlices; }
 
 cudaError_t group_plan_build(const GroupGemv* list, int n, int sms, GroupPlan* out) {
   GroupPlan p{};
@@ -233,14 +240,16 @@ cudaError_t group_plan_build(const GroupGemv* list, int n, int sms, GroupPlan* o
     d.tile_end = (int)tiles;
     stage_bytes = std::max(stage_bytes, (uint32_t)d.R * (uint32_t)(d.K / 2 + d.K / 16));
   }
-  // one contiguous tile range per CTA, two CTAs per SM, equal bytes per range
-  const int grid = (int)std::max<long long>(1, std::min<long long>(2LL * sms, tiles));
+  // one contiguous tile range per CTA, equal cost per range:
+  // a tile costs its bytes, scaled up when fewer than all consumer warps work
+  // on it (K / 2048 slices that do not divide the eight warps)
+  const int grid = (int)std::max<long long>(1, std::min<long long>((long long)kGrpCtasPerSm * sms, tiles));
   std::vector<long long> cum(tiles + 1, 0);
   for (const auto& d : g) {
-    const long long row_bytes = d.K / 2 + d.K / 16;
+    const long long row_cost = (long long)(d.K / 2 + d.K / 16) * kGrpWarps / (d.S * d.RG);
     for (int t = d.tile0; t < d.tile_end; ++t) {
       const int rows = std::min(d.R, d.N - (t - d.tile0) * d.R);
-      cum[t + 1] = cum[t] + rows * row_bytes;
+      cum[t + 1] = cum[t] + rows * row_cost;
     }
   }
   std::vector<int> cta(grid + 1);
@@ -254,7 +263,7 @@ cudaError_t group_plan_build(const GroupGemv* list, int n, int sms, GroupPlan* o
   p.ngemv = n;
   p.grid = grid;
   p.stage_bytes = stage_bytes;  // a multiple of 16: K % 2048 == 0
-  const size_t budget = 74 * 1024;
+  const size_t budget = kGrpSmemBudget;
   p.ST = (int)std::max<size_t>(2, std::min<size_t>(8, budget / (stage_bytes + sizeof(float) * kGrpRed + 24)));
   p.smem = (size_t)p.ST * stage_bytes + sizeof(float) * (size_t)p.ST * kGrpRed + 3 * 8 * (size_t)p.ST;
   cudaError_t e = cudaMalloc(&p.d_gemvs, sizeof(GroupGemv) * n);
