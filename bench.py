@@ -372,7 +372,14 @@ def run_case(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     c = args.case
-    if c.startswith("gemv_") or c.startswith("skinny16_"):
+    if c == "gemv_group_4layers":
+        # the grouped launch over 4 decoder layers + the lm_head (0.78 GB)
+        mats = build_stack(q, dev, 1, layers=4)
+        xs, ys = stack_io(mats, dev, 1)
+        grp = q.GemvGroup([(wq, s, b, x[0], y[0]) for (_, N, K, wq, s, b), x, y in zip(mats, xs, ys)])
+        f = grp.run
+        nbytes = sum(w4_bytes(N, K) for (_, N, K, *_r) in mats)
+    elif c.startswith("gemv_") or c.startswith("skinny16_"):
         shape = {"lm_head": (151936, 4096), "down": (4096, 12288), "q": (4096, 4096),
                  "gate_up": (24576, 4096)}[c.split("_", 1)[1]]
         M = 1 if c.startswith("gemv_") else 16
@@ -383,13 +390,6 @@ def run_case(args):
         f = (lambda: q.qgemv_w4a16(wq, s, b, x[0], y[0])) if M == 1 else \
             (lambda: q.qgemm_w4a16_skinny(wq, s, b, x, y))
         nbytes = w4_bytes(N, K, M)
-    elif c == "gemv_group_4layers":
-        # the grouped launch over 4 decoder layers + the lm_head (0.78 GB)
-        mats = build_stack(q, dev, 1, layers=4)
-        xs, ys = stack_io(mats, dev, 1)
-        grp = q.GemvGroup([(wq, s, b, x[0], y[0]) for (_, N, K, wq, s, b), x, y in zip(mats, xs, ys)])
-        f = grp.run
-        nbytes = sum(w4_bytes(N, K) for (_, N, K, *_r) in mats)
     elif c.startswith("moe_"):
         T = int(c[5:])
         E, H, I, k = 64, 7168, 2048, 16
