@@ -194,6 +194,15 @@ __device__ __forceinline__ float fma_bf16_hi_hi(uint32_t a, uint32_t b, float ac
       : "r"(a), "r"(b));
   return acc;
 }
+// acc += a.lo * b.lo + a.hi * b.hi (bf16 x bf16 products, two fp32 roundings),
+// both halves unpacked in one block.
+__device__ __forceinline__ float fma_bf16x2_dot(uint32_t a, uint32_t b, float acc) {
+  asm("{.reg .b16 al, ah, bl, bh; mov.b32 {al, ah}, %1; mov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, al, bl, %0;\n\tfma.rn.f32.bf16 %0, ah, bh, %0;}"
+      : "+f"(acc)
+      : "r"(a), "r"(b));
+  return acc;
+}
 __device__ __forceinline__ float fma_f16_lo_lo(uint32_t a, uint32_t b, float acc) {
   asm("{.reg .b16 al, ah, bl, bh; mov.b32 {al, ah}, %1; mov.b32 {bl, bh}, %2;\n\t"
       "fma.rn.f32.f16 %0, al, bl, %0;}"

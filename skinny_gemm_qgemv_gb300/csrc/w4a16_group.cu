@@ -189,10 +189,7 @@ __global__ void __launch_bounds__(kGrpThreads, kGrpCtasPerSm) w4a16_group_kernel
           uint32_t q[4];
           nib8_to_bf16x2_biased(w[i2], q);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            acc[j] = fma_bf16_lo_lo(q[j], xr[i2][j], acc[j]);
-            acc[j] = fma_bf16_hi_hi(q[j], xr[i2][j], acc[j]);
-          }
+          for (int j = 0; j < 4; ++j) acc[j] = fma_bf16x2_dot(q[j], xr[i2][j], acc[j]);
         }
         const float t = (acc[0] + acc[1]) + (acc[2] + acc[3]);
         part[i] = fmaf(sc, t, bi * sx);
