@@ -162,8 +162,12 @@ QG_API void qgemv_w4a16_group_destroy(qg_w4_group *group);
  *   y       fp32 [M][N] (output): y[m][n] = sum_k (s q[n][k] + b) x[m][k].
  *   M       1..32 (M = 1 is the same result as qgemv_w4a16).
  *   workspace / ws_bytes: at least qg_skinny_workspace_size(M, N, K,
- *           group_size) bytes of device memory, 16-byte aligned; the
- *           contents need no initialization and are clobbered.
+ *           group_size) bytes of device memory, 16-byte aligned, zero-filled
+ *           before its first use. Every completed call leaves it zero-filled
+ *           again (it holds split-K partial sums and arrival counters), so one
+ *           workspace serves any sequence of calls ordered on one stream;
+ *           calls that may overlap need separate workspaces. After a call that
+ *           reported a device error (qg_device_error) zero-fill it again.
  */
 QG_API qg_status qgemm_w4a16_skinny(const uint32_t *wq, const uint16_t *scales_f16,
                              const uint16_t *biases_f16, const uint16_t *x_bf16,

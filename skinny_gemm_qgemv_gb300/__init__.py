@@ -143,6 +143,25 @@ def qgemv_w4a16(wq, scales, biases, x, y=None, workspace=None, stream=None):
     return y
 
 
+_WS = {}
+
+
+def skinny_workspace(nbytes, device):
+    """A zero-filled workspace for qgemm_w4a16_skinny, cached per device and
+    reused (every call leaves it zero-filled). Calls sharing it must be
+    ordered on one stream. Inside a stream capture a fresh one is made (the
+    zero fill is captured too) and not cached."""
+    key = (str(device), )
+    ws = _WS.get(key)
+    if ws is not None and ws.numel() >= nbytes:
+        return ws
+    if torch.cuda.is_current_stream_capturing():
+        return torch.zeros(nbytes, device=device, dtype=torch.uint8)
+    ws = torch.zeros(max(nbytes, 1 << 20), device=device, dtype=torch.uint8)
+    _WS[key] = ws
+    return ws
+
+
 def qgemm_w4a16_skinny(wq, scales, biases, x, y=None, workspace=None, stream=None):
     """Y[m][n] = sum_k (s q + b) X[m][k]; X bf16 [M][K] -> Y fp32 [M][N]."""
     N, K8 = wq.shape
@@ -154,7 +173,7 @@ def qgemm_w4a16_skinny(wq, scales, biases, x, y=None, workspace=None, stream=Non
         y = torch.empty(M, N, device=wq.device, dtype=torch.float32)
     need = lib().qg_skinny_workspace_size(M, N, K, K // scales.shape[1])
     if workspace is None and need:
-        workspace = torch.empty(need, device=wq.device, dtype=torch.uint8)
+        workspace = skinny_workspace(need, wq.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().qgemm_w4a16_skinny(_p(wq), _p(scales), _p(biases), _p(x), _p(y), M, N, K,
                                     K // scales.shape[1], _p(workspace), ws_bytes, _stream(stream)),

@@ -33,6 +33,11 @@
 //               the same warps while the chunk's MMAs run.
 // TMEM: columns 0..255 hold the accumulators (chunk buffers of 4 x N columns),
 // 256..511 two A chunk buffers of 4 x 32 columns.
+// Short matrices are split along K while twice the units still fit the SMs
+// (each unit then pipelines several stages); the CTA finishing a row tile last
+// (atomic counter, no waiting) adds the partial tiles in split order
+// (deterministic) and resets the counter, so the workspace needs clearing only
+// before its first use.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -507,6 +512,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 namespace {
 
+// split-K happens only while 2 x tiles <= SMs, so a few hundred counters cover it
+constexpr size_t kCounterBytes = 1024;
+
 struct TcPlan {
   int NT, ntiles, splits, kper, nunits, ST;
   uint32_t stage_bytes;
@@ -520,7 +528,7 @@ TcPlan tc_plan(int M, int N, int K, int sms) {
   const int kstages = K / kStageK;
   // split K until every SM has a unit, keeping each split a whole number of stages
   p.splits = 1;
-  while (p.ntiles * p.splits < sms && p.splits * 2 <= kstages && kstages % (p.splits * 2) == 0) p.splits *= 2;
+  while (p.ntiles * p.splits * 2 <= sms && p.splits * 2 <= kstages && kstages % (p.splits * 2) == 0) p.splits *= 2;
   p.kper = K / p.splits;
   p.nunits = p.ntiles * p.splits;
   p.stage_bytes = (uint32_t)(p.NT * 1024 + 36864);
@@ -530,7 +538,9 @@ TcPlan tc_plan(int M, int N, int K, int sms) {
   p.ST = (int)std::min<size_t>(4, (budget - fixed - sx_bytes) / p.stage_bytes);
   p.smem = fixed + sx_bytes + (size_t)p.ST * p.stage_bytes;
   p.ws_partial = p.splits > 1 ? sizeof(float) * (size_t)p.nunits * p.NT * kRows : 0;
-  p.ws_counters = p.splits > 1 ? sizeof(uint32_t) * (size_t)p.ntiles : 0;
+  // the counters sit at a fixed place (the workspace's first bytes) for every
+  // shape, so a later call never finds partial sums of another shape there
+  p.ws_counters = p.splits > 1 ? kCounterBytes : 0;
   return p;
 }
 
@@ -543,7 +553,7 @@ bool tc_path_ok(int M, int N, int K) {
 size_t tc_workspace_size(int M, int N, int K) {
   if (!tc_path_ok(M, N, K)) return 0;
   const TcPlan p = tc_plan(M, N, K, device_sm_count());
-  return p.ws_partial + ((p.ws_counters + 255) & ~(size_t)255) + (p.ws_partial ? 256 : 0);
+  return p.ws_counters + p.ws_partial;
 }
 
 template <int NT>
@@ -585,13 +595,11 @@ cudaError_t launch_w4a16_tc(const uint32_t* wq, const uint16_t* sc, const uint16
   a.stage_bytes = p.stage_bytes;
   a.y = y;
   a.x = x;
-  a.partial = p.splits > 1 ? static_cast<float*>(ws) : nullptr;
-  a.counters = p.splits > 1 ? reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + p.ws_partial) : nullptr;
+  a.counters = p.splits > 1 ? static_cast<uint32_t*>(ws) : nullptr;
+  a.partial = p.splits > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kCounterBytes) : nullptr;
   a.err = err;
-  if (p.splits > 1) {
-    cudaError_t e = cudaMemsetAsync(a.counters, 0, p.ws_counters, stream);
-    if (e != cudaSuccess) return e;
-  }
+  // the counters start at zero (caller contract) and the last arriver of every
+  // tile resets its counter, so no clearing launch is needed between calls
   const int grid = std::min(p.nunits, sms);
   if (p.NT == 16) return launch_tc_nt<16>(maps, a, p, grid, stream, pdl);
   return launch_tc_nt<32>(maps, a, p, grid, stream, pdl);
