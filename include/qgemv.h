@@ -177,6 +177,56 @@ QG_API qg_status qgemm_w4a16_skinny(const uint32_t *wq, const uint16_t *scales_f
 QG_API size_t qg_skinny_workspace_size(int M, int N, int K, int group_size);
 
 /*
+ * qgemm_w4a16_skinny_group_* -- many independent skinny projections (each
+ * Y_i = X_i W_i^T as in qgemm_w4a16_skinny) in one persistent launch on the
+ * tensor cores: the M = 16 verify batch of the Uzu article ("Producing several
+ * tokens from one model pass") run over a whole list of weight matrices, the
+ * row tiles of all of them streamed back to back ("MLX Runner ...",
+ * "Architecture: one command buffer per token"). The projections must not
+ * depend on each other: a launch reads every X_i and writes every Y_i in no
+ * particular order.
+ *
+ *   qg_w4_gemm_desc  one projection: wq uint32 [N][K/8], scales/biases fp16
+ *                    [N][K/64], x bf16 [M][K], y fp32 [M][N]; every pointer
+ *                    16-byte aligned device memory of the current device;
+ *                    3 <= M <= 32, N >= 1, K a multiple of 512 and at most
+ *                    32768. All M of one group lie in one class, 3..16 or
+ *                    17..32 (other shapes, and mixed classes, return
+ *                    QG_ERR_UNSUPPORTED).
+ *   qgemm_w4a16_skinny_group_create  validates the count descriptors
+ *                    (group_size 64), encodes their TMA descriptors, splits
+ *                    the row tiles of all projections into one contiguous
+ *                    range per SM with equal work, and copies that plan to
+ *                    device memory it allocates (cudaMalloc, synchronous
+ *                    copies). The descriptors' buffers are used by every later
+ *                    run: they must stay allocated until the group is
+ *                    destroyed. *group is set on QG_OK.
+ *   qgemm_w4a16_skinny_group_run     one launch on stream computing every Y_i
+ *                    from the current contents of X_i and W_i; no workspace,
+ *                    stream-ordered, no allocation, capturable in a CUDA
+ *                    graph. Run it on the device that was current at create.
+ *   qgemm_w4a16_skinny_group_destroy frees the plan (NULL is ignored); no run
+ *                    of the group may be pending.
+ */
+typedef struct qg_w4_gemm_desc {
+  const uint32_t *wq;
+  const uint16_t *scales_f16;
+  const uint16_t *biases_f16;
+  const uint16_t *x_bf16;
+  float *y;
+  int M;
+  int N;
+  int K;
+} qg_w4_gemm_desc;
+
+typedef struct qg_w4_skinny_group qg_w4_skinny_group;
+
+QG_API qg_status qgemm_w4a16_skinny_group_create(const qg_w4_gemm_desc *descs, int count, int group_size,
+                                                 qg_w4_skinny_group **group);
+QG_API qg_status qgemm_w4a16_skinny_group_run(const qg_w4_skinny_group *group, void *stream);
+QG_API void qgemm_w4a16_skinny_group_destroy(qg_w4_skinny_group *group);
+
+/*
  * moe_mxfp4_expert_forward -- routed-expert MoE layer with MXFP4 experts
  * ("Running Kimi K3 ...", "How it works" and "Technical approach / compute").
  *

@@ -7,7 +7,8 @@ there is no fallback path. PyTorch only supplies device memory and streams.
 
 Entry points (same names as the C ABI):
   qgemv_w4a16, qgemm_w4a16_skinny, moe_mxfp4_expert_forward,
-  hadamard32_quant_i8, gemm_w8a8_i32; GemvGroup wraps qgemv_w4a16_group_*
+  hadamard32_quant_i8, gemm_w8a8_i32; GemvGroup wraps qgemv_w4a16_group_* and
+  SkinnyGroup qgemm_w4a16_skinny_group_*
 """
 from __future__ import annotations
 
@@ -29,12 +30,19 @@ EXPORTS = [
     "qg_moe_workspace_h_offset", "hadamard32_quant_i8", "gemm_w8a8_i32", "qg_set_pdl", "qg_device_error",
     "moe_mxfp4_expert_forward_noalloc", "qg_moe_noalloc_max_bytes",
     "qgemv_w4a16_group_create", "qgemv_w4a16_group_run", "qgemv_w4a16_group_destroy",
+    "qgemm_w4a16_skinny_group_create", "qgemm_w4a16_skinny_group_run", "qgemm_w4a16_skinny_group_destroy",
 ]
 
 
 class _GemvDesc(ctypes.Structure):
     _fields_ = [("wq", ctypes.c_void_p), ("scales_f16", ctypes.c_void_p), ("biases_f16", ctypes.c_void_p),
                 ("x_bf16", ctypes.c_void_p), ("y", ctypes.c_void_p), ("N", ctypes.c_int), ("K", ctypes.c_int)]
+
+
+class _GemmDesc(ctypes.Structure):
+    _fields_ = [("wq", ctypes.c_void_p), ("scales_f16", ctypes.c_void_p), ("biases_f16", ctypes.c_void_p),
+                ("x_bf16", ctypes.c_void_p), ("y", ctypes.c_void_p), ("M", ctypes.c_int), ("N", ctypes.c_int),
+                ("K", ctypes.c_int)]
 
 
 class QGError(RuntimeError):
@@ -90,6 +98,12 @@ def lib() -> ctypes.CDLL:
         L.qgemv_w4a16_group_run.argtypes = [P, P]
         L.qgemv_w4a16_group_destroy.restype = None
         L.qgemv_w4a16_group_destroy.argtypes = [P]
+        L.qgemm_w4a16_skinny_group_create.restype = I
+        L.qgemm_w4a16_skinny_group_create.argtypes = [ctypes.POINTER(_GemmDesc), I, I, ctypes.POINTER(P)]
+        L.qgemm_w4a16_skinny_group_run.restype = I
+        L.qgemm_w4a16_skinny_group_run.argtypes = [P, P]
+        L.qgemm_w4a16_skinny_group_destroy.restype = None
+        L.qgemm_w4a16_skinny_group_destroy.argtypes = [P]
         _lib = L
     return _lib
 
@@ -207,6 +221,43 @@ class GemvGroup:
     def close(self):
         if self._h:
             lib().qgemv_w4a16_group_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class SkinnyGroup:
+    """Many independent skinny projections (3 <= M <= 32) as one persistent
+    tensor-core launch.
+
+    `items` is a list of (wq, scales, biases, x, y) CUDA tensors with the
+    layouts of qgemm_w4a16_skinny (x bf16 [M][K], y preallocated fp32 [M][N]).
+    The tensors are held by the group: every run reads the x's and writes the
+    y's in place."""
+
+    def __init__(self, items):
+        descs = (_GemmDesc * len(items))()
+        for d, (wq, s, b, x, y) in zip(descs, items):
+            for t, nb, n in ((wq, 4, "wq"), (s, 2, "scales"), (b, 2, "biases"), (x, 2, "x"), (y, 4, "y")):
+                _need(t, nb, n)
+            d.wq, d.scales_f16, d.biases_f16 = wq.data_ptr(), s.data_ptr(), b.data_ptr()
+            d.x_bf16, d.y = x.data_ptr(), y.data_ptr()
+            d.M, d.N, d.K = x.shape[0], wq.shape[0], wq.shape[1] * 8
+        self._items = list(items)
+        self._h = ctypes.c_void_p()
+        _check(lib().qgemm_w4a16_skinny_group_create(descs, len(items), 64, ctypes.byref(self._h)),
+               "qgemm_w4a16_skinny_group_create")
+
+    def run(self, stream=None):
+        _check(lib().qgemm_w4a16_skinny_group_run(self._h, _stream(stream)), "qgemm_w4a16_skinny_group_run")
+
+    def close(self):
+        if self._h:
+            lib().qgemm_w4a16_skinny_group_destroy(self._h)
             self._h = ctypes.c_void_p()
 
     def __del__(self):

@@ -193,6 +193,44 @@ qg_status qgemm_w4a16_skinny(const uint32_t* wq, const uint16_t* scales_f16, con
   return run_w4(wq, scales_f16, biases_f16, x_bf16, y, M, N, K, workspace, ws_bytes, stream);
 }
 
+struct qg_w4_skinny_group {
+  qg::TcGroupPlan plan;
+};
+
+qg_status qgemm_w4a16_skinny_group_create(const qg_w4_gemm_desc* descs, int count, int group_size,
+                                          qg_w4_skinny_group** group) {
+  if (!descs || !group || count < 1) return QG_ERR_INVALID_ARG;
+  std::vector<qg::TcGroupItem> list(count);
+  for (int i = 0; i < count; ++i) {
+    const qg_w4_gemm_desc& d = descs[i];
+    qg_status st = check_w4(d.wq, d.scales_f16, d.biases_f16, d.x_bf16, d.y, d.M, d.N, d.K, group_size);
+    if (st != QG_OK) return st;
+    list[i] = qg::TcGroupItem{d.wq, d.scales_f16, d.biases_f16, d.x_bf16, d.y, d.M, d.N, d.K};
+  }
+  if (qg::tc_group_check(list.data(), count) != 0) return QG_ERR_UNSUPPORTED;
+  auto* out = new (std::nothrow) qg_w4_skinny_group();
+  if (!out) return QG_ERR_CUDA;
+  if (qg::tc_group_plan_build(list.data(), count, qg::device_sm_count(), &out->plan) != cudaSuccess) {
+    delete out;
+    return QG_ERR_CUDA;
+  }
+  *group = out;
+  return QG_OK;
+}
+
+qg_status qgemm_w4a16_skinny_group_run(const qg_w4_skinny_group* group, void* stream) {
+  if (!group) return QG_ERR_INVALID_ARG;
+  uint32_t* err = err_word();
+  if (!err) return QG_ERR_CUDA;
+  return from_cuda(qg::tc_group_launch(group->plan, err, static_cast<cudaStream_t>(stream), g_pdl));
+}
+
+void qgemm_w4a16_skinny_group_destroy(qg_w4_skinny_group* group) {
+  if (!group) return;
+  qg::tc_group_plan_free(&group->plan);
+  delete group;
+}
+
 size_t qg_moe_workspace_size(int T, int H, int I, int E, int top_k) {
   if (T < 1 || H < 1 || I < 1 || E < 1 || top_k < 1) return 0;
   return qg::moe_layout(T, H, I, E, top_k).total;

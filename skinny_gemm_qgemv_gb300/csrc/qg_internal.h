@@ -68,6 +68,29 @@ size_t tc_workspace_size(int M, int N, int K);
 cudaError_t launch_w4a16_tc(const uint32_t* wq, const uint16_t* sc, const uint16_t* bi, const uint16_t* x,
                             float* y, int M, int N, int K, void* ws, size_t ws_bytes, uint32_t* err,
                             cudaStream_t stream, bool pdl);
+// Grouped skinny GEMM on tcgen05 (w4a16_tc.cu): one persistent launch over a
+// list of independent projections Y_i = X_i W_i^T, all with 3 <= M <= 32 in one
+// width class (M <= 16, or 17..32); full-K row tiles, no workspace.
+struct TcGroupItem {
+  const uint32_t* wq;
+  const uint16_t* scales;
+  const uint16_t* biases;
+  const uint16_t* x;
+  float* y;
+  int M, N, K;
+};
+struct TcGroupPlan {
+  void* d_gemvs;  // device descriptors (tensor maps + shapes)
+  int* d_cta;     // [grid + 1] first unit of each CTA, then [grid] its projection
+  int ngemv, grid, NT, ST;
+  uint32_t stage_bytes;
+  size_t smem;
+};
+// 0: fine; 1: a shape outside the tcgen05 path; 2: mixed width classes
+int tc_group_check(const TcGroupItem* list, int n);
+cudaError_t tc_group_plan_build(const TcGroupItem* list, int n, int sms, TcGroupPlan* out);
+void tc_group_plan_free(TcGroupPlan* p);
+cudaError_t tc_group_launch(const TcGroupPlan& p, uint32_t* err, cudaStream_t stream, bool pdl);
 cudaError_t launch_w4a16_generic(const uint32_t* wq, const uint16_t* sc, const uint16_t* bi, const uint16_t* x,
                                  float* y, int M, int N, int K, cudaStream_t stream, bool pdl);
 

@@ -43,7 +43,9 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "qg_common.cuh"
 #include "qg_internal.h"
@@ -64,16 +66,79 @@ constexpr uint32_t kACol = 256;     // first TMEM column of the A buffers
 constexpr uint32_t kTmemCols = 512;
 constexpr int kThreads = 480;  // 1 producer + 2 MMA + 8 converter + 4 epilogue warps
 
+// One projection of a grouped launch, as the kernel reads it from global
+// memory; the tensor maps need 64-byte alignment (CUtensorMap is declared with 128).
+struct TcGemv {
+  CUtensorMap codes, scales, biases, x;
+  float* y;
+  int N, M, K;
+  int unit0, unit_end;  // its row tiles in the launch's unit numbering
+};
+static_assert(alignof(TcGemv) >= 64, "tensor maps need 64-byte alignment");
+
 struct TcArgs {
   int N, K, M;
   int ntiles, splits, kper, nunits;
   int ST;
   uint32_t stage_bytes;
   float* y;
-  const uint16_t* x;
   float* partial;
   uint32_t* counters;
   uint32_t* err;
+  // grouped launch (null for one matrix): per-projection descriptors, the
+  // first unit of every CTA's range ([grid + 1]) and the projection of that unit
+  const TcGemv* gemvs;
+  const int* cta_unit0;
+  const int* cta_gemv0;
+};
+
+// The units one CTA works on, in order: for one matrix a grid-stride walk over
+// its (128-row tile, K split) pairs; for a grouped launch a contiguous range of
+// full-K row tiles of the group's projections, the projections in group order.
+struct UnitWalk {
+  int u, end, stride, g;
+  int tile, n0, k0, kper, N, M;
+  float* y;
+  __device__ __forceinline__ explicit UnitWalk(const TcArgs& a) {
+    if (a.gemvs) {
+      u = a.cta_unit0[blockIdx.x];
+      end = a.cta_unit0[blockIdx.x + 1];
+      stride = 1;
+      g = a.cta_gemv0[blockIdx.x];
+    } else {
+      u = blockIdx.x;
+      end = a.nunits;
+      stride = gridDim.x;
+      g = 0;
+    }
+    load(a);
+  }
+  __device__ __forceinline__ bool valid() const { return u < end; }
+  __device__ __forceinline__ void next(const TcArgs& a) {
+    u += stride;
+    load(a);
+  }
+  __device__ __forceinline__ void load(const TcArgs& a) {
+    if (u >= end) return;
+    if (a.gemvs) {
+      while (u >= a.gemvs[g].unit_end) ++g;
+      const TcGemv& d = a.gemvs[g];
+      tile = u - d.unit0;
+      k0 = 0;
+      kper = d.K;
+      N = d.N;
+      M = d.M;
+      y = d.y;
+    } else {
+      tile = u / a.splits;
+      k0 = (u % a.splits) * a.kper;
+      kper = a.kper;
+      N = a.N;
+      M = a.M;
+      y = a.y;
+    }
+    n0 = tile * kRows;
+  }
 };
 
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
@@ -91,6 +156,11 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm,
           dst),
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
       : "memory");
+}
+
+__device__ __forceinline__ void tensormap_acquire(const CUtensorMap* tm) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(reinterpret_cast<uint64_t>(tm))
+               : "memory");
 }
 
 __device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
@@ -212,8 +282,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* const gbase = smem_raw + (base - raw);
   // shared layout: stages | sx [2][4 groups][NT] f32 (x sums of a chunk) | barriers
   const uint32_t s_stages = base;
-  const int nchunk = a.kper / kChunkK;
-  const int nstage = a.kper / kStageK;
   float* sx = reinterpret_cast<float*>(gbase + a.ST * a.stage_bytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(
       gbase + ((a.ST * a.stage_bytes + sizeof(float) * 2 * kChunkGroups * NT + 7) & ~(size_t)7));
@@ -261,24 +329,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
-      int issued = 0;
-      for (int ui = 0, u = blockIdx.x; u < a.nunits && !*abort_flag; ++ui, u += gridDim.x) {
-        const int tile = u / a.splits, split = u % a.splits;
-        const int n0 = tile * kRows, k0 = split * a.kper;
+      int issued = 0, fenced = -1;
+      for (UnitWalk w(a); w.valid() && !*abort_flag; w.next(a)) {
+        const int nstage = w.kper / kStageK;
+        if (a.gemvs && w.g != fenced) {
+          // the descriptors were written through the generic proxy (a host copy,
+          // possibly into memory that held other descriptors before): make the
+          // TMA unit see their current contents
+          const TcGemv* d = &a.gemvs[w.g];
+          tensormap_acquire(&d->codes);
+          tensormap_acquire(&d->scales);
+          tensormap_acquire(&d->biases);
+          tensormap_acquire(&d->x);
+          fenced = w.g;
+        }
+        const CUtensorMap* mc = a.gemvs ? &a.gemvs[w.g].codes : &tm_codes;
+        const CUtensorMap* ms = a.gemvs ? &a.gemvs[w.g].scales : &tm_scales;
+        const CUtensorMap* mb = a.gemvs ? &a.gemvs[w.g].biases : &tm_biases;
+        const CUtensorMap* mx = a.gemvs ? &a.gemvs[w.g].x : &tm_x;
         for (int s = 0; s < nstage; ++s) {
-          const int sg = ui * nstage + s, st = sg % a.ST;
+          const int sg = issued, st = sg % a.ST;
           if (sg >= a.ST &&
               !wait_or_abort<true>(&empty[st], ((sg / a.ST) & 1) ^ 1, abort_flag, a.err, kErrTcEmptyWait))
             break;
           const uint32_t sb = s_stages + st * a.stage_bytes;
           mbar_arrive_expect_tx(&full[st], a.stage_bytes);
-          const int kk = k0 + s * kStageK;
+          const int kk = w.k0 + s * kStageK;
           // X viewed as {64 k, rows, K/64}: one box = the stage's eight [NT][128 B] tiles;
           // codes viewed as {128 B, rows, K/256}: one box = two [128][128 B] tiles (one per chunk)
-          tma_load_3d(sb + x_off, &tm_x, 0, 0, kk / 64, &full[st]);
-          tma_load_3d(sb + c_off, &tm_codes, 0, n0, kk / 256, &full[st]);
-          tma_load_2d(sb + s_off, &tm_scales, kk / 64, n0, &full[st]);
-          tma_load_2d(sb + b_off, &tm_biases, kk / 64, n0, &full[st]);
+          tma_load_3d(sb + x_off, mx, 0, 0, kk / 64, &full[st]);
+          tma_load_3d(sb + c_off, mc, 0, w.n0, kk / 256, &full[st]);
+          tma_load_2d(sb + s_off, ms, kk / 64, w.n0, &full[st]);
+          tma_load_2d(sb + b_off, mb, kk / 64, w.n0, &full[st]);
           ++issued;
         }
       }
@@ -293,10 +375,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NT >> 3) << 17) |
                              ((uint32_t)(kRows >> 4) << 24);
       bool ok = true;
-      for (int ui = 0, u = blockIdx.x; u < a.nunits && ok; ++ui, u += gridDim.x) {
+      int gcb = 0, sgb = 0;  // chunks and stages of the CTA's earlier units
+      for (UnitWalk w(a); w.valid() && ok; w.next(a)) {
+        const int nchunk = w.kper / kChunkK;
         for (int c = 0; c < nchunk && ok; ++c) {
-          const int gc = ui * nchunk + c;
-          const int sg = ui * nstage + c / kChunksPerStage, st = sg % a.ST;
+          const int gc = gcb + c;
+          const int sg = sgb + c / kChunksPerStage, st = sg % a.ST;
           const int ab = gc % kNAB, nb = gc % NACC;
           if (c % kChunksPerStage == 0)
             ok = wait_or_abort<false>(&full[st], (sg / a.ST) & 1, abort_flag, a.err, kErrTcFullWait);
@@ -318,6 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mma_commit(&accfull[nb]);
         }
+        gcb += nchunk;
+        sgb += nchunk / kChunksPerStage;
       }
       mma_commit(&done[h]);
       mbar_wait(&done[h], 0, a.err, kErrTcDrain);
@@ -330,10 +416,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = (warp & 3) * 32 + lane;  // weight row of the tile, 0..127
     const uint32_t rsw = r & 7;
     const uint32_t tlane = tbase + ((uint32_t)((warp & 3) * 32) << 16) + kACol;
-    for (int ui = 0, u = blockIdx.x; u < a.nunits; ++ui, u += gridDim.x) {
+    int gcb = 0, sgb = 0;
+    for (UnitWalk w(a); w.valid(); w.next(a)) {
+      const int nchunk = w.kper / kChunkK;
       for (int c = 0; c < nchunk; ++c) {
-        const int gc = ui * nchunk + c;
-        const int sg = ui * nstage + c / kChunksPerStage, st = sg % a.ST;
+        const int gc = gcb + c;
+        const int sg = sgb + c / kChunksPerStage, st = sg % a.ST;
         const int ab = gc % kNAB;
         if (!*abort_flag && c % kChunksPerStage == 0)
           wait_or_abort<true>(&full[st], (sg / a.ST) & 1, abort_flag, a.err, kErrTcFullWait);
@@ -372,6 +460,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (c % kChunksPerStage == kChunksPerStage - 1) mbar_arrive(&empty[st]);
         }
       }
+      gcb += nchunk;
+      sgb += nchunk / kChunksPerStage;
     }
   } else {
     // ---------------------------------------------------------------- epilogue (warps 11..14)
@@ -379,15 +469,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = q * 32 + lane;
     const int et = threadIdx.x - 352;  // 0..127 (warps 11..14)
     const uint32_t tlane = tbase + ((uint32_t)(q * 32) << 16);
-    for (int ui = 0, u = blockIdx.x; u < a.nunits; ++ui, u += gridDim.x) {
-      const int tile = u / a.splits;
-      const int n0 = tile * kRows;
+    int gcb = 0, sgb = 0;
+    for (UnitWalk w(a); w.valid(); w.next(a)) {
+      const int nchunk = w.kper / kChunkK;
       uint64_t yacc2[NT / 2];  // activation rows (2p, 2p + 1)
 #pragma unroll
       for (int q2 = 0; q2 < NT / 2; ++q2) yacc2[q2] = 0ull;
       for (int c = 0; c < nchunk; ++c) {
-        const int gc = ui * nchunk + c;
-        const int sg = ui * nstage + c / kChunksPerStage, st = sg % a.ST;
+        const int gc = gcb + c;
+        const int sg = sgb + c / kChunksPerStage, st = sg % a.ST;
         const int nb = gc % NACC;
         // the epilogue releases accumulators on the MMA critical path: no backoff
         if (!*abort_flag && c % kChunksPerStage == 0)
@@ -456,15 +546,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       float yacc[NT];
 #pragma unroll
       for (int q2 = 0; q2 < NT / 2; ++q2) unpair2(yacc2[q2], yacc[2 * q2], yacc[2 * q2 + 1]);
-      const int n = n0 + row;
-      if (a.splits == 1) {
-        if (n < a.N) {
+      const int n = w.n0 + row;
+      if (a.gemvs || a.splits == 1) {
+        if (n < w.N) {
 #pragma unroll
           for (int m = 0; m < NT; ++m)
-            if (m < a.M) a.y[(size_t)m * a.N + n] = yacc[m];
+            if (m < w.M) w.y[(size_t)m * w.N + n] = yacc[m];
         }
       } else {
-        float* part = a.partial + (size_t)u * NT * kRows;
+        const int tile = w.tile;
+        float* part = a.partial + (size_t)w.u * NT * kRows;
 #pragma unroll
         for (int m = 0; m < NT; ++m) part[m * kRows + row] = yacc[m];
         __threadfence();
@@ -494,6 +585,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         epi_bar();
       }
+      gcb += nchunk;
+      sgb += nchunk / kChunksPerStage;
     }
   }
 
@@ -515,6 +608,30 @@ namespace {
 // split-K happens only while 2 x tiles <= SMs, so a few hundred counters cover it
 constexpr size_t kCounterBytes = 1024;
 
+// codes {128 B, N rows, K/256 chunks} in [128][128 B] boxes (two per stage),
+// scales and biases {K/64, N} in [128][8] boxes, X {64 k, M rows, K/64 groups}
+// in [8][NT][64] boxes (one per stage), the rows past M read as zeros
+bool tc_maps(CUtensorMap (&maps)[4], const uint32_t* wq, const uint16_t* sc, const uint16_t* bi, const uint16_t* x,
+             int M, int N, int K, int NT) {
+  return tmap_3d(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, 128, (uint64_t)N, (uint64_t)K / 256, (uint64_t)K / 2,
+                 128, 128, kRows, 2) &&
+         tmap_2d(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT16, sc, (uint64_t)K / 64, (uint64_t)N, (uint64_t)K / 32, 8,
+                 kRows, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+         tmap_2d(&maps[2], CU_TENSOR_MAP_DATA_TYPE_UINT16, bi, (uint64_t)K / 64, (uint64_t)N, (uint64_t)K / 32, 8,
+                 kRows, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+         tmap_3d(&maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, 64, (uint64_t)M, (uint64_t)K / 64, (uint64_t)K * 2,
+                 128, 64, (uint32_t)NT, kGroupsPerStage);
+}
+
+int stages_for(int NT, uint32_t stage_bytes, size_t* smem) {
+  const size_t fixed = 1024 + 256;  // alignment slack, barriers
+  const size_t budget = 224 * 1024;
+  const size_t sx_bytes = sizeof(float) * 2 * kChunkGroups * NT;
+  const int ST = (int)std::min<size_t>(4, (budget - fixed - sx_bytes) / stage_bytes);
+  *smem = fixed + sx_bytes + (size_t)ST * stage_bytes;
+  return ST;
+}
+
 struct TcPlan {
   int NT, ntiles, splits, kper, nunits, ST;
   uint32_t stage_bytes;
@@ -532,11 +649,7 @@ TcPlan tc_plan(int M, int N, int K, int sms) {
   p.kper = K / p.splits;
   p.nunits = p.ntiles * p.splits;
   p.stage_bytes = (uint32_t)(p.NT * 1024 + 36864);
-  const size_t fixed = 1024 + 256;  // alignment slack, barriers
-  const size_t budget = 224 * 1024;
-  const size_t sx_bytes = sizeof(float) * 2 * kChunkGroups * p.NT;
-  p.ST = (int)std::min<size_t>(4, (budget - fixed - sx_bytes) / p.stage_bytes);
-  p.smem = fixed + sx_bytes + (size_t)p.ST * p.stage_bytes;
+  p.ST = stages_for(p.NT, p.stage_bytes, &p.smem);
   p.ws_partial = p.splits > 1 ? sizeof(float) * (size_t)p.nunits * p.NT * kRows : 0;
   // the counters sit at a fixed place (the workspace's first bytes) for every
   // shape, so a later call never finds partial sums of another shape there
@@ -573,16 +686,7 @@ cudaError_t launch_w4a16_tc(const uint32_t* wq, const uint16_t* sc, const uint16
   const TcPlan p = tc_plan(M, N, K, sms);
   if (ws_bytes < tc_workspace_size(M, N, K)) return cudaErrorInvalidValue;
   CUtensorMap maps[4];
-  const bool ok =
-      tmap_3d(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, 128, (uint64_t)N, (uint64_t)K / 256, (uint64_t)K / 2,
-                128, 128, kRows, 2) &&
-      tmap_2d(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT16, sc, (uint64_t)K / 64, (uint64_t)N, (uint64_t)K / 32, 8,
-               kRows, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-      tmap_2d(&maps[2], CU_TENSOR_MAP_DATA_TYPE_UINT16, bi, (uint64_t)K / 64, (uint64_t)N, (uint64_t)K / 32, 8,
-               kRows, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-      tmap_3d(&maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, 64, (uint64_t)M, (uint64_t)K / 64, (uint64_t)K * 2,
-                128, 64, (uint32_t)p.NT, kGroupsPerStage);
-  if (!ok) return cudaErrorInvalidValue;
+  if (!tc_maps(maps, wq, sc, bi, x, M, N, K, p.NT)) return cudaErrorInvalidValue;
   TcArgs a;
   a.N = N;
   a.K = K;
@@ -594,15 +698,117 @@ cudaError_t launch_w4a16_tc(const uint32_t* wq, const uint16_t* sc, const uint16
   a.ST = p.ST;
   a.stage_bytes = p.stage_bytes;
   a.y = y;
-  a.x = x;
   a.counters = p.splits > 1 ? static_cast<uint32_t*>(ws) : nullptr;
   a.partial = p.splits > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kCounterBytes) : nullptr;
   a.err = err;
+  a.gemvs = nullptr;
+  a.cta_unit0 = nullptr;
+  a.cta_gemv0 = nullptr;
   // the counters start at zero (caller contract) and the last arriver of every
   // tile resets its counter, so no clearing launch is needed between calls
   const int grid = std::min(p.nunits, sms);
   if (p.NT == 16) return launch_tc_nt<16>(maps, a, p, grid, stream, pdl);
   return launch_tc_nt<32>(maps, a, p, grid, stream, pdl);
+}
+
+// ---------------------------------------------------------------------------
+// Grouped launch: the row tiles of every projection, full K each, in one
+// persistent grid; each CTA takes a contiguous range of equal cost.
+// ---------------------------------------------------------------------------
+int tc_group_check(const TcGroupItem* list, int n) {
+  for (int i = 0; i < n; ++i)
+    if (!tc_path_ok(list[i].M, list[i].N, list[i].K)) return 1;
+  for (int i = 1; i < n; ++i)
+    if ((list[i].M <= 16) != (list[0].M <= 16)) return 2;
+  return 0;
+}
+
+cudaError_t tc_group_plan_build(const TcGroupItem* list, int n, int sms, TcGroupPlan* out) {
+  if (n < 1 || tc_group_check(list, n) != 0) return cudaErrorInvalidValue;
+  TcGroupPlan p{};
+  p.NT = list[0].M <= 16 ? 16 : 32;
+  std::vector<TcGemv> g(n);
+  long long units = 0;
+  for (int i = 0; i < n; ++i) {
+    const TcGroupItem& it = list[i];
+    CUtensorMap maps[4];
+    if (!tc_maps(maps, it.wq, it.scales, it.biases, it.x, it.M, it.N, it.K, p.NT)) return cudaErrorInvalidValue;
+    TcGemv& d = g[i];
+    d.codes = maps[0];
+    d.scales = maps[1];
+    d.biases = maps[2];
+    d.x = maps[3];
+    d.y = it.y;
+    d.N = it.N;
+    d.M = it.M;
+    d.K = it.K;
+    d.unit0 = (int)units;
+    units += (it.N + kRows - 1) / kRows;
+    if (units >= (1LL << 30)) return cudaErrorInvalidValue;
+    d.unit_end = (int)units;
+  }
+  // a unit costs its stages plus about one stage of hand-over at its end
+  std::vector<long long> cum(units + 1, 0);
+  for (const TcGemv& d : g)
+    for (int u = d.unit0; u < d.unit_end; ++u) cum[u + 1] = cum[u] + d.K / kStageK + 1;
+  const int grid = (int)std::max<long long>(1, std::min<long long>(sms, units));
+  std::vector<int> cta(2 * grid + 1);
+  cta[0] = 0;
+  for (int c = 1; c < grid; ++c) {
+    const long long target = cum[units] * c / grid;
+    cta[c] = (int)(std::lower_bound(cum.begin(), cum.end(), target) - cum.begin());
+    cta[c] = std::max(cta[c], cta[c - 1]);
+  }
+  cta[grid] = (int)units;
+  for (int c = 0, gi = 0; c < grid; ++c) {
+    while (gi + 1 < n && cta[c] >= g[gi].unit_end) ++gi;
+    cta[grid + 1 + c] = gi;
+  }
+  p.ngemv = n;
+  p.grid = grid;
+  p.stage_bytes = (uint32_t)(p.NT * 1024 + 36864);
+  p.ST = stages_for(p.NT, p.stage_bytes, &p.smem);
+  cudaError_t e = cudaMalloc(&p.d_gemvs, sizeof(TcGemv) * n);
+  if (e != cudaSuccess) return e;
+  e = cudaMalloc(&p.d_cta, sizeof(int) * cta.size());
+  if (e != cudaSuccess) {
+    cudaFree(p.d_gemvs);
+    return e;
+  }
+  e = cudaMemcpy(p.d_gemvs, g.data(), sizeof(TcGemv) * n, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(p.d_cta, cta.data(), sizeof(int) * cta.size(), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    cudaFree(p.d_gemvs);
+    cudaFree(p.d_cta);
+    return e;
+  }
+  *out = p;
+  return cudaSuccess;
+}
+
+void tc_group_plan_free(TcGroupPlan* p) {
+  if (p->d_gemvs) cudaFree(p->d_gemvs);
+  if (p->d_cta) cudaFree(p->d_cta);
+  p->d_gemvs = nullptr;
+  p->d_cta = nullptr;
+}
+
+cudaError_t tc_group_launch(const TcGroupPlan& p, uint32_t* err, cudaStream_t stream, bool pdl) {
+  TcArgs a{};
+  a.splits = 1;
+  a.ST = p.ST;
+  a.stage_bytes = p.stage_bytes;
+  a.err = err;
+  a.gemvs = static_cast<const TcGemv*>(p.d_gemvs);
+  a.cta_unit0 = p.d_cta;
+  a.cta_gemv0 = p.d_cta + p.grid + 1;
+  // the kernel reads every projection's maps from its descriptor
+  CUtensorMap unused[4];
+  std::memset(unused, 0, sizeof(unused));
+  TcPlan tp{};
+  tp.smem = p.smem;
+  if (p.NT == 16) return launch_tc_nt<16>(unused, a, tp, p.grid, stream, pdl);
+  return launch_tc_nt<32>(unused, a, tp, p.grid, stream, pdl);
 }
 
 }  // namespace qg

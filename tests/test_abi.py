@@ -114,3 +114,30 @@ def test_gemv_group_validation(L):
     assert f(make((16, 4096), ptr=A + 4), 1, 64, ctypes.byref(out)) == 2   # misaligned
     assert L.qgemv_w4a16_group_run(None, None) == 1
     L.qgemv_w4a16_group_destroy(None)
+
+
+def test_skinny_group_validation(L):
+    Desc = q._GemmDesc
+    out = P()
+
+    def make(*shapes, ptr=A):
+        ds = (Desc * len(shapes))()
+        for d, (M, N, K) in zip(ds, shapes):
+            d.wq = d.scales_f16 = d.biases_f16 = d.x_bf16 = d.y = ptr
+            d.M, d.N, d.K = M, N, K
+        return ds
+
+    f = L.qgemm_w4a16_skinny_group_create
+    assert f(make((16, 128, 4096)), 0, 64, ctypes.byref(out)) == 1                   # empty group
+    assert f(None, 1, 64, ctypes.byref(out)) == 1
+    assert f(make((16, 128, 4096)), 1, 64, None) == 1
+    assert f(make((16, 128, 4096), (16, 0, 4096)), 2, 64, ctypes.byref(out)) == 1    # N < 1
+    assert f(make((33, 128, 4096)), 1, 64, ctypes.byref(out)) == 1                   # M > 32
+    assert f(make((2, 128, 4096)), 1, 64, ctypes.byref(out)) == 3                    # M < 3
+    assert f(make((16, 128, 4096), (16, 128, 448)), 2, 64, ctypes.byref(out)) == 3   # K % 512
+    assert f(make((16, 128, 65536)), 1, 64, ctypes.byref(out)) == 3                  # K > 32768
+    assert f(make((16, 128, 4096), (17, 128, 4096)), 2, 64, ctypes.byref(out)) == 3  # mixed classes
+    assert f(make((16, 128, 4096)), 1, 128, ctypes.byref(out)) == 3                  # group 128
+    assert f(make((16, 128, 4096), ptr=A + 4), 1, 64, ctypes.byref(out)) == 2       # misaligned
+    assert L.qgemm_w4a16_skinny_group_run(None, None) == 1
+    L.qgemm_w4a16_skinny_group_destroy(None)
