@@ -245,6 +245,24 @@ __device__ __forceinline__ void nib8_to_bf16x2_biased(uint32_t w, uint32_t (&o)[
   asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(o[3]) : "r"(s3), "r"(kMask), "r"(kMagic));
 }
 
+// Two fp32 lanes in one 64-bit register, for the paired fp32 FMA (fma.rn.f32x2).
+__device__ __forceinline__ uint64_t pair2(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpair2(uint64_t v, float& lo, float& hi) {
+  uint32_t a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(a), "=r"(b) : "l"(v));
+  lo = __uint_as_float(a);
+  hi = __uint_as_float(b);
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 // Pack two bf16 bit patterns (low, high) into one register.
 __device__ __forceinline__ uint32_t pack2(uint32_t lo16, uint32_t hi16) { return (lo16 & 0xFFFFu) | (hi16 << 16); }
 

@@ -18,7 +18,10 @@
 //  warps 1, 2   MMA issuers (groups 0-1 / 2-3 of every chunk): per group four
 //               tcgen05.mma.kind::f16 (M = 128 weight rows, N = 16 or 32
 //               activation rows, K = 16) with A read from TMEM, each group into
-//               its own accumulator; one commit per chunk.
+//               its own accumulator; one commit per chunk. They learn that A is
+//               converted and that an accumulator buffer was read from shared
+//               counters, and need no wait on the stage itself (the converters
+//               waited for it before converting).
 //  warps 3..10  converters, all on every chunk (warps 3..6 its groups 0-1,
 //               7..10 groups 2-3): decode each code word into eight bf16 values
 //               128 + q (exact) in natural k order and store them into TMEM as
@@ -33,6 +36,9 @@
 //               the same warps while the chunk's MMAs run.
 // TMEM: columns 0..255 hold the accumulators (chunk buffers of 4 x N columns),
 // 256..511 two A chunk buffers of 4 x 32 columns.
+// A grouped launch walks the full-K row tiles of many projections, one
+// contiguous equal-cost range per CTA, reading each projection's tensor maps
+// from a descriptor in device memory.
 // Short matrices are split along K while twice the units still fit the SMs
 // (each unit then pipelines several stages); the CTA finishing a row tile last
 // (atomic counter, no waiting) adds the partial tiles in split order
@@ -232,29 +238,31 @@ __device__ __forceinline__ void nib8_to_bf16x2_natural(uint32_t w, uint32_t (&o)
   o[3] = __byte_perm(t1, kMagic, 0x7352);
 }
 
-// two fp32 lanes in one 64-bit register, for the paired fp32 FMA (fma.rn.f32x2)
-__device__ __forceinline__ uint64_t pair2(uint32_t lo, uint32_t hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
-  return r;
-}
-__device__ __forceinline__ void unpair2(uint64_t v, float& lo, float& hi) {
-  uint32_t a, b;
-  asm("mov.b64 {%0, %1}, %2;" : "=r"(a), "=r"(b) : "l"(v));
-  lo = __uint_as_float(a);
-  hi = __uint_as_float(b);
-}
-__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 // Bounded wait that also honours the CTA-wide abort flag. Waiters off the
 // MMA-issue critical path back off with a short sleep so their polling does not
 // slow down the barrier operations of the issuing threads.
+__device__ __forceinline__ uint32_t ld_acquire_s32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_add_s32(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ bool wait_count(const uint32_t* p, uint32_t target, volatile uint32_t* abort_flag,
+                                           uint32_t* err, uint32_t code) {
+  for (uint32_t i = 0; i < (kMaxPolls << 6); ++i) {
+    if ((int32_t)(ld_acquire_s32(p) - target) >= 0) return true;
+    if ((i & 1023u) == 1023u && *abort_flag) return false;
+  }
+  report_error(err, code);
+  *abort_flag = 1u;
+  return false;
+}
+
 template <bool kBackoff>
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
                                               uint32_t* err, uint32_t code) {
@@ -287,13 +295,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       gbase + ((a.ST * a.stage_bytes + sizeof(float) * 2 * kChunkGroups * NT + 7) & ~(size_t)7));
   uint64_t* full = bars;
   uint64_t* empty = full + a.ST;
-  uint64_t* afull = empty + a.ST;      // [kNAB][2] half a chunk (two groups) of converted A is in TMEM
-  uint64_t* accfull = afull + 2 * kNAB;  // the MMAs of a chunk completed: accumulators ready, A buffer free
-  uint64_t* accempty = accfull + NACC; // the epilogue has read a chunk's accumulators
-  uint64_t* done = accempty + NACC;    // [2] all MMAs of an issuing warp completed
+  uint64_t* accfull = empty + a.ST;    // the MMAs of a chunk completed: accumulators ready, A buffer free
+  uint64_t* done = accfull + NACC;     // [2] all MMAs of an issuing warp completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 2);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   volatile uint32_t* is_last = tmem_slot + 2;
+  // Hand-offs to the MMA issuers are monotonic shared-memory counters (release
+  // add / acquire load): polling one costs a shared load, where an mbarrier
+  // try_wait costs a few hundred cycles while the converters keep the shared
+  // memory pipe busy, and the issuers wait on every chunk.
+  uint32_t* conv_cnt = tmem_slot + 4;       // [kNAB][2] converter warps done with half an A buffer
+  uint32_t* epi_cnt = conv_cnt + 2 * kNAB;  // [NACC] epilogue warps done reading an accumulator buffer
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // per stage: [0, NT*1024) X tiles; codes 32 KB; scales, biases 2 KB each
@@ -304,14 +316,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 12);  // 8 converter warps + 4 epilogue warps
     }
-    for (int i = 0; i < 2 * kNAB; ++i) mbar_init(&afull[i], 4);
     for (int i = 0; i < NACC; ++i) {
       mbar_init(&accfull[i], 2);  // one commit per MMA warp
-      mbar_init(&accempty[i], 4);
     }
     mbar_init(&done[0], 1);
     mbar_init(&done[1], 1);
     *abort_flag = 0u;
+    for (int i = 0; i < 2 * kNAB + NACC; ++i) conv_cnt[i] = 0u;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -382,11 +393,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int gc = gcb + c;
           const int sg = sgb + c / kChunksPerStage, st = sg % a.ST;
           const int ab = gc % kNAB, nb = gc % NACC;
-          if (c % kChunksPerStage == 0)
-            ok = wait_or_abort<false>(&full[st], (sg / a.ST) & 1, abort_flag, a.err, kErrTcFullWait);
-          ok = ok && wait_or_abort<false>(&afull[2 * ab + h], (gc / kNAB) & 1, abort_flag, a.err, kErrTcMmaWait);
+          ok = wait_count(&conv_cnt[2 * ab + h], 4u * (uint32_t)(gc / kNAB + 1), abort_flag, a.err, kErrTcMmaWait);
           if (ok && gc >= NACC)
-            ok = wait_or_abort<false>(&accempty[nb], ((gc / NACC) & 1) ^ 1, abort_flag, a.err, kErrTcAccWait);
+            ok = wait_count(&epi_cnt[nb], 4u * (uint32_t)(gc / NACC), abort_flag, a.err, kErrTcAccWait);
           if (!ok) break;
           tc_fence_after();
           const uint32_t xs = s_stages + st * a.stage_bytes + x_off;
@@ -456,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&afull[2 * ab + h]);
+          red_release_add_s32(&conv_cnt[2 * ab + h], 1u);
           if (c % kChunksPerStage == kChunksPerStage - 1) mbar_arrive(&empty[st]);
         }
       }
@@ -522,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j1 + G == kChunkGroups) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&accempty[nb]);
+            if (lane == 0) red_release_add_s32(&epi_cnt[nb], 1u);
           }
 #pragma unroll
           for (int jj = 0; jj < G; ++jj) {
@@ -624,7 +633,7 @@ bool tc_maps(CUtensorMap (&maps)[4], const uint32_t* wq, const uint16_t* sc, con
 }
 
 int stages_for(int NT, uint32_t stage_bytes, size_t* smem) {
-  const size_t fixed = 1024 + 256;  // alignment slack, barriers
+  const size_t fixed = 1024 + 512;  // alignment slack, barriers
   const size_t budget = 224 * 1024;
   const size_t sx_bytes = sizeof(float) * 2 * kChunkGroups * NT;
   const int ST = (int)std::min<size_t>(4, (budget - fixed - sx_bytes) / stage_bytes);
