@@ -263,6 +263,20 @@ __device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
   return d;
 }
 
+// Eight 4-bit codes (code i in bits 4i..4i+3) -> four f16x2 registers with one
+// shift and four lop3s: o[0] = (1024 + q0, 1024 + q4), o[1] = (1024 + 16 q1,
+// 1024 + 16 q5), o[2] = (1024 + q2, 1024 + q6), o[3] = (1024 + 16 q3,
+// 1024 + 16 q7). 0x6400 is fp16 1024 (ulp 1): a code in mantissa bits 0-3 adds
+// q, in bits 4-7 adds 16 q; all values are exact.
+__device__ __forceinline__ void nib8_to_f16x2_offset(uint32_t w, uint32_t (&o)[4]) {
+  constexpr uint32_t kLo = 0x000F000Fu, kHi = 0x00F000F0u, kMagic = 0x64006400u;
+  const uint32_t t = w >> 8;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(o[0]) : "r"(w), "r"(kLo), "r"(kMagic));
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(o[1]) : "r"(w), "r"(kHi), "r"(kMagic));
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(o[2]) : "r"(t), "r"(kLo), "r"(kMagic));
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(o[3]) : "r"(t), "r"(kHi), "r"(kMagic));
+}
+
 // Pack two bf16 bit patterns (low, high) into one register.
 __device__ __forceinline__ uint32_t pack2(uint32_t lo16, uint32_t hi16) { return (lo16 & 0xFFFFu) | (hi16 << 16); }
 

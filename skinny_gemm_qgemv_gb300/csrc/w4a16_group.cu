@@ -20,10 +20,19 @@
 //    (every tile then holds 96 K-rows' worth of codes, 55 KB).
 //    When the range crosses into the next projection the consumers reload
 //    their activations (x is small and stays in L2).
-//  * Dequant and fold as in the single GEMV: (word >> 4j) & 0x000F000F |
-//    0x43004300 gives two bf16 128 + q, fma.rn.f32.bf16 into fp32, and per
-//    64-group s * (sum (128+q) x - 128 sum x) + b * sum x.
+//  * Dequant and fold: a lane keeps its 64 activations in fp16, scaled by a
+//    power of two 2^-sigma that puts the lane's largest |x| just below 2^15
+//    (exact: bf16 has 8 significant bits, fp16 11). Each code word gives four
+//    fp16x2 registers with one shift and four lop3s: (w & 0x000F000F) |
+//    0x64006400 is (1024 + q) for the codes in bits 0-3 of each half and
+//    (w & 0x00F000F0) | 0x64006400 is (1024 + 16 q) for bits 4-7, the same on
+//    w >> 8 for the other two; fma.rn.f32.f16 multiplies them (exact products)
+//    into fp32 sums A (1024 + q terms) and B (1024 + 16 q terms), and per lane
+//    s * 2^sigma * ((A - 1024 X_A) + (B - 1024 X_B) / 16) + b * sum x folds the
+//    affine group, X_A, X_B being the sums of the scaled activations of each
+//    class.
 //  * Slices of one row are summed in slice order through shared memory.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -123,9 +132,10 @@ __global__ void __launch_bounds__(kGrpThreads, kGrpCtasPerSm) w4a16_group_kernel
   GroupGemv d;
   int s = 0, rg = 0, k0 = 0, g_lane = 0;
   bool busy = false, active = false;
-  uint32_t xr[kGrpWPL][4];
-  float sx = 0.f;
-  int it = 0;
+  uint32_t xr[kGrpWPL][4];  // fp16x2: (x0, x4), (x1, x5), (x2, x6), (x3, x7) of each word, scaled
+  float sx = 0.f, up = 1.f, acc0a = 0.f, acc0b = 0.f;
+  int it = 0, st = 0;
+  uint32_t par = 0;
   for (int tile = t0; tile < t1; ++tile, ++it) {
     if (g < 0 || tile >= d.tile_end) {
       // next projection of the range: its slice layout and activations
@@ -144,21 +154,46 @@ __global__ void __launch_bounds__(kGrpThreads, kGrpCtasPerSm) w4a16_group_kernel
       active = busy && k0 < d.K;
       g_lane = k0 / 64;
       sx = 0.f;
+      float amax = 0.f;
 #pragma unroll
       for (int i = 0; i < kGrpWPL; ++i) {
         uint4 v = make_uint4(0, 0, 0, 0);
         if (active) v = *reinterpret_cast<const uint4*>(d.x + k0 + 8 * i);
-        xr[i][0] = __byte_perm(v.x, v.z, 0x5410);
-        xr[i][1] = __byte_perm(v.x, v.z, 0x7632);
-        xr[i][2] = __byte_perm(v.y, v.w, 0x5410);
-        xr[i][3] = __byte_perm(v.y, v.w, 0x7632);
-        const uint32_t e[4] = {v.x, v.y, v.z, v.w};
+        xr[i][0] = v.x;
+        xr[i][1] = v.y;
+        xr[i][2] = v.z;
+        xr[i][3] = v.w;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) sx += bf16_bits_to_f32(e[j] & 0xFFFFu) + bf16_bits_to_f32(e[j] >> 16);
+        for (int j = 0; j < 4; ++j) {
+          const float lo = bf16_bits_to_f32(xr[i][j] & 0xFFFFu), hi = bf16_bits_to_f32(xr[i][j] >> 16);
+          sx += lo + hi;
+          amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
+        }
       }
+      const int sig = fp16_prescale_exp(amax);
+      const float down = ldexpf(1.f, -sig);
+      up = ldexpf(1.f, sig);
+      float sxa = 0.f, sxb = 0.f;
+#pragma unroll
+      for (int i = 0; i < kGrpWPL; ++i) {
+        float xv[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          xv[2 * j] = bf16_bits_to_f32(xr[i][j] & 0xFFFFu) * down;
+          xv[2 * j + 1] = bf16_bits_to_f32(xr[i][j] >> 16) * down;
+        }
+        // pair k and k + 4 of the word: the decode puts codes j and j + 4 in one register
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const __half2 h2 = __floats2half2_rn(xv[j], xv[j + 4]);
+          xr[i][j] = *reinterpret_cast<const uint32_t*>(&h2);
+          const float2 back = __half22float2(h2);
+          if (j % 2 == 0) sxa += back.x + back.y; else sxb += back.x + back.y;
+        }
+      }
+      acc0a = -1024.f * sxa;
+      acc0b = -1024.f * sxb;
     }
-    const int st = it % a.ST;
-    const uint32_t par = (it / a.ST) & 1;
     if (!mbar_wait(&full[st], par, a.err, kErrGemvFullWait)) break;
     const uint32_t rcb = d.K / 2, rsb = d.K / 32;
     const int r0 = (tile - d.tile0) * d.R;
@@ -183,16 +218,22 @@ __global__ void __launch_bounds__(kGrpThreads, kGrpCtasPerSm) w4a16_group_kernel
         }
         const float sc = f16_bits_to_f32(lds16(stg + d.R * rcb + r * rsb + 2 * g_lane));
         const float bi = f16_bits_to_f32(lds16(stg + d.R * (rcb + rsb) + r * rsb + 2 * g_lane));
-        float acc[4] = {-128.f * sx, 0.f, 0.f, 0.f};
+        float aa = acc0a, ab = 0.f, ba = acc0b, bb = 0.f;
 #pragma unroll
         for (int i2 = 0; i2 < kGrpWPL; ++i2) {
           uint32_t q[4];
-          nib8_to_bf16x2_biased(w[i2], q);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) acc[j] = fma_bf16x2_dot(q[j], xr[i2][j], acc[j]);
+          nib8_to_f16x2_offset(w[i2], q);
+          aa = fma_f16_lo_lo(q[0], xr[i2][0], aa);
+          ab = fma_f16_hi_hi(q[0], xr[i2][0], ab);
+          ba = fma_f16_lo_lo(q[1], xr[i2][1], ba);
+          bb = fma_f16_hi_hi(q[1], xr[i2][1], bb);
+          aa = fma_f16_lo_lo(q[2], xr[i2][2], aa);
+          ab = fma_f16_hi_hi(q[2], xr[i2][2], ab);
+          ba = fma_f16_lo_lo(q[3], xr[i2][3], ba);
+          bb = fma_f16_hi_hi(q[3], xr[i2][3], bb);
         }
-        const float t = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-        part[i] = fmaf(sc, t, bi * sx);
+        const float t = (aa + ab) + 0.0625f * (ba + bb);
+        part[i] = fmaf(sc * up, t, bi * sx);
       }
     }
     const float v = transposed_warp_sum<kGrpRPW>(part, lane);
@@ -213,6 +254,10 @@ __global__ void __launch_bounds__(kGrpThreads, kGrpCtasPerSm) w4a16_group_kernel
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st]);
+    if (++st == a.ST) {
+      st = 0;
+      par ^= 1u;
+    }
   }
 }
 
