@@ -20,6 +20,7 @@
 //    form of the affine dot product.
 //  * Lane partials are reduced with a transposed butterfly; slices of one row
 //    are summed in a fixed order through shared memory (deterministic).
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -112,33 +113,60 @@ __global__ void __launch_bounds__(288, MINB) w4a16_gemv_kernel(const GemvArgs a)
   const int k0 = s * 32 * KPL + lane * KPL;
   const bool active = k0 < K;
 
-  // activations: pairs (k+j, k+j+4) of every word as bf16x2, and sum x
+  // activations: fp16 pairs (k+j, k+j+4) of every word, scaled by 2^-sigma
+  // (the lane's largest |x| just below 2^15; exact), the sum of x, and the
+  // offset sums -1024 X_A, -1024 X_B of the scaled values of each code class
   pdl_wait();
   uint32_t xr[M][WPL][4];
-  float sx[M];
+  float sx[M], up[M], acc0a[M], acc0b[M];
 #pragma unroll
   for (int m = 0; m < M; ++m) {
     sx[m] = 0.f;
+    float amax = 0.f;
 #pragma unroll
     for (int i = 0; i < WPL; ++i) {
       uint4 v = make_uint4(0, 0, 0, 0);
       if (active) v = *reinterpret_cast<const uint4*>(a.x + (size_t)m * K + k0 + 8 * i);
-      xr[m][i][0] = __byte_perm(v.x, v.z, 0x5410);
-      xr[m][i][1] = __byte_perm(v.x, v.z, 0x7632);
-      xr[m][i][2] = __byte_perm(v.y, v.w, 0x5410);
-      xr[m][i][3] = __byte_perm(v.y, v.w, 0x7632);
-      const uint32_t e[4] = {v.x, v.y, v.z, v.w};
+      xr[m][i][0] = v.x;
+      xr[m][i][1] = v.y;
+      xr[m][i][2] = v.z;
+      xr[m][i][3] = v.w;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) sx[m] += bf16_bits_to_f32(e[j] & 0xFFFFu) + bf16_bits_to_f32(e[j] >> 16);
+      for (int j = 0; j < 4; ++j) {
+        const float lo = bf16_bits_to_f32(xr[m][i][j] & 0xFFFFu), hi = bf16_bits_to_f32(xr[m][i][j] >> 16);
+        sx[m] += lo + hi;
+        amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
+      }
     }
+    const int sig = fp16_prescale_exp(amax);
+    const float down = ldexpf(1.f, -sig);
+    up[m] = ldexpf(1.f, sig);
+    float sxa = 0.f, sxb = 0.f;
+#pragma unroll
+    for (int i = 0; i < WPL; ++i) {
+      float xv[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        xv[2 * j] = bf16_bits_to_f32(xr[m][i][j] & 0xFFFFu) * down;
+        xv[2 * j + 1] = bf16_bits_to_f32(xr[m][i][j] >> 16) * down;
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const __half2 h2 = __floats2half2_rn(xv[j], xv[j + 4]);
+        xr[m][i][j] = *reinterpret_cast<const uint32_t*>(&h2);
+        const float2 back = __half22float2(h2);
+        if (j % 2 == 0) sxa += back.x + back.y; else sxb += back.x + back.y;
+      }
+    }
+    acc0a[m] = -1024.f * sxa;
+    acc0b[m] = -1024.f * sxb;
   }
   const int g_lane = k0 / 64;  // this lane's group (KPL <= 64 never straddles)
 
   const uint32_t sbase = smem_u32(stages);
-  int it = 0;
-  for (int tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x, ++it) {
-    const int st = it % a.ST;
-    const uint32_t par = (it / a.ST) & 1;
+  int st = 0;
+  uint32_t par = 0;
+  for (int tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
     if (!mbar_wait(&full[st], par, a.err, kErrGemvFullWait)) break;
     const int r0 = tile * a.R;
     const int rows = min(a.R, N - r0);
@@ -164,29 +192,32 @@ __global__ void __launch_bounds__(288, MINB) w4a16_gemv_kernel(const GemvArgs a)
         const float sc = f16_bits_to_f32(lds16(stg + a.R * row_code_bytes + r * row_sb_bytes + 2 * g_lane));
         const float bi =
             f16_bits_to_f32(lds16(stg + a.R * (row_code_bytes + row_sb_bytes) + r * row_sb_bytes + 2 * g_lane));
+        // acc[m][0], [1]: the (1024 + q) class, [2], [3]: the (1024 + 16 q) class
         float acc[M][4];
 #pragma unroll
         for (int m = 0; m < M; ++m) {
-          acc[m][0] = -128.f * sx[m];
-          acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
+          acc[m][0] = acc0a[m];
+          acc[m][2] = acc0b[m];
+          acc[m][1] = acc[m][3] = 0.f;
         }
 #pragma unroll
         for (int i2 = 0; i2 < WPL; ++i2) {
           uint32_t q[4];
-          nib8_to_bf16x2_biased(w[i2], q);
+          nib8_to_f16x2_offset(w[i2], q);
 #pragma unroll
           for (int m = 0; m < M; ++m) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              acc[m][j] = fma_bf16_lo_lo(q[j], xr[m][i2][j], acc[m][j]);
-              acc[m][j] = fma_bf16_hi_hi(q[j], xr[m][i2][j], acc[m][j]);
+              const int c = (j & 1) * 2;
+              acc[m][c] = fma_f16_lo_lo(q[j], xr[m][i2][j], acc[m][c]);
+              acc[m][c + 1] = fma_f16_hi_hi(q[j], xr[m][i2][j], acc[m][c + 1]);
             }
           }
         }
 #pragma unroll
         for (int m = 0; m < M; ++m) {
-          const float t = (acc[m][0] + acc[m][1]) + (acc[m][2] + acc[m][3]);
-          part[i][m] = fmaf(sc, t, bi * sx[m]);
+          const float t = (acc[m][0] + acc[m][1]) + 0.0625f * (acc[m][2] + acc[m][3]);
+          part[i][m] = fmaf(sc * up[m], t, bi * sx[m]);
         }
       }
     }
@@ -233,6 +264,10 @@ __global__ void __launch_bounds__(288, MINB) w4a16_gemv_kernel(const GemvArgs a)
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
       }
+    }
+    if (++st == a.ST) {
+      st = 0;
+      par ^= 1u;
     }
   }
 }
