@@ -350,9 +350,9 @@ __global__ void __launch_bounds__(32 * (gu_warps(TC) + 1), 1) moe_mx_gateup_kern
   uint32_t xr[TC][16];
   int cur_v = -1, np = 0;
   int my_pair = -1, my_sig = 0;  // lane j < TC: pair j of the virtual expert and its prescale
-  int it = 0;
-  for (int tile = t0; tile < t1; ++tile, ++it) {
-    const int st = it % a.ST;
+  int st = 0;
+  uint32_t par = 0;
+  for (int tile = t0; tile < t1; ++tile) {
     const int v = tile / a.tpe, r0 = (tile % a.tpe) * a.R;
     if (v != cur_v) {
       cur_v = v;
@@ -366,7 +366,7 @@ __global__ void __launch_bounds__(32 * (gu_warps(TC) + 1), 1) moe_mx_gateup_kern
         if (on && pj >= 0) {
           // x * 2^-sigma rounded to fp16: the exact power-of-two prescale of the router
           const uint4* xp = reinterpret_cast<const uint4*>(a.x + (size_t)(pj / a.top_k) * H + 32 * kb);
-          const float sc = ldexpf(1.f, -sj);
+          const float sc = pow2f(-sj);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const uint4 w = __ldg(xp + c);
@@ -385,7 +385,7 @@ __global__ void __launch_bounds__(32 * (gu_warps(TC) + 1), 1) moe_mx_gateup_kern
     const int jl = lane % TC;
     const int pj_l = __shfl_sync(kFull, my_pair, jl);
     const int sj_l = __shfl_sync(kFull, my_sig, jl);
-    if (!mbar_wait(&full[st], (it / a.ST) & 1, a.err, kErrMoeWait)) break;
+    if (!mbar_wait(&full[st], par, a.err, kErrMoeWait)) break;
     const uint8_t* sbase = stages + (size_t)st * a.stage_bytes;
     float acc[V];
 #pragma unroll
@@ -417,10 +417,14 @@ __global__ void __launch_bounds__(32 * (gu_warps(TC) + 1), 1) moe_mx_gateup_kern
         if (busy) mbar_arrive(&redfull[st]);
         mbar_arrive(&empty[st]);
       }
+      if (++st == a.ST) {
+        st = 0;
+        par ^= 1u;
+      }
       continue;
     }
     if (busy) {
-      if (a.S > 1 && !mbar_wait(&redfull[st], (it / a.ST) & 1, a.err, kErrMoeWait)) break;
+      if (a.S > 1 && !mbar_wait(&redfull[st], par, a.err, kErrMoeWait)) break;
       for (int s2 = 1; s2 < a.S; ++s2) tot += red[((st * a.S + s2) * a.RG + rg) * 32 + lane];
     }
     __syncwarp();
@@ -432,14 +436,18 @@ __global__ void __launch_bounds__(32 * (gu_warps(TC) + 1), 1) moe_mx_gateup_kern
         const int rr = lane / TC, j = lane % TC;
         const int row = r0 + rg * RPW + rr;
         if (j < np && row < I) {
-          const float g = ldexpf(outv[rg * 32 + 2 * lane], sj_l);
-          const float u = ldexpf(outv[rg * 32 + 2 * lane + 1], sj_l);
+          const float g = outv[rg * 32 + 2 * lane] * pow2f(sj_l);
+          const float u = outv[rg * 32 + 2 * lane + 1] * pow2f(sj_l);
           const float hv = g / (1.f + expf(-g)) * u;
           a.h[(size_t)pj_l * I + row] = hv;
           atomicMax(&a.hmax[pj_l], __float_as_uint(fabsf(hv)));
         }
       }
       __syncwarp();
+    }
+    if (++st == a.ST) {
+      st = 0;
+      par ^= 1u;
     }
   }
 }
@@ -527,19 +535,24 @@ __global__ void __launch_bounds__(32 * (dn_warps(TC) + 1), 1)
   const bool busy = rg < a.RG;
   const int kb = s * 32 + lane;
   const bool on = busy && kb < I / 32;
-  int it = 0;
+  int st = 0;
+  uint32_t par = 0;
   bool ok = true;
   for (int ri = blockIdx.x; ri < a.nranges; ri += gridDim.x) {
     const int n0 = ri * a.R, rows = min(a.R, H - n0);
-    for (int i = 0; i < nv; ++i, ++it) {
-      const int v = (vstart + i) % nv;
-      const int st = it % a.ST;
+    for (int i = 0, v = vstart; i < nv; ++i, v = (v + 1 == nv ? 0 : v + 1)) {
+      const int cst = st;
+      const uint32_t cpar = par;
+      if (++st == a.ST) {
+        st = 0;
+        par ^= 1u;
+      }
       const int np = vtab[v * kMxVexpInts + 1];
       const int jl = lane % TC;
       const int pj_l = vtab[v * kMxVexpInts + 2 + jl];
       const int sj_l = pj_l >= 0 ? sigp[pj_l] : 0;
-      if (ok) ok = mbar_wait(&full[st], (it / a.ST) & 1, a.err, kErrMoeWait);
-      const uint8_t* sbase = stages + (size_t)st * a.stage_bytes;
+      if (ok) ok = mbar_wait(&full[cst], cpar, a.err, kErrMoeWait);
+      const uint8_t* sbase = stages + (size_t)cst * a.stage_bytes;
       float acc[V];
 #pragma unroll
       for (int q = 0; q < V; ++q) acc[q] = 0.f;
@@ -550,7 +563,7 @@ __global__ void __launch_bounds__(32 * (dn_warps(TC) + 1), 1)
         for (int j = 0; j < TC; ++j) {
           if (j < np) {
             const int sj = sigp[vtab[v * kMxVexpInts + 2 + j]];
-            const float sc = ldexpf(1.f, -sj);
+            const float sc = pow2f(-sj);
             const uint32_t hp = smem_u32(sbase + o_h + j * (I * 4) + kb * 128);
             const uint32_t sw = (uint32_t)kb & 7u;
 #pragma unroll
@@ -579,20 +592,20 @@ __global__ void __launch_bounds__(32 * (dn_warps(TC) + 1), 1)
       }
       float tot = transposed_warp_sum<V>(acc, lane);
       if (s > 0) {
-        if (busy) red[((st * a.S + s) * a.RG + rg) * 32 + lane] = tot;
+        if (busy) red[((cst * a.S + s) * a.RG + rg) * 32 + lane] = tot;
         __syncwarp();
         if (lane == 0) {
-          if (busy) mbar_arrive(&redfull[st]);
-          mbar_arrive(&empty[st]);
+          if (busy) mbar_arrive(&redfull[cst]);
+          mbar_arrive(&empty[cst]);
         }
         continue;
       }
       if (busy) {
-        if (a.S > 1 && ok) ok = mbar_wait(&redfull[st], (it / a.ST) & 1, a.err, kErrMoeWait);
-        for (int s2 = 1; s2 < a.S; ++s2) tot += red[((st * a.S + s2) * a.RG + rg) * 32 + lane];
+        if (a.S > 1 && ok) ok = mbar_wait(&redfull[cst], cpar, a.err, kErrMoeWait);
+        for (int s2 = 1; s2 < a.S; ++s2) tot += red[((cst * a.S + s2) * a.RG + rg) * 32 + lane];
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);
+      if (lane == 0) mbar_arrive(&empty[cst]);
       if (busy) {
         outv[rg * 32 + transposed_row<V>(lane)] = tot;
         __syncwarp();
@@ -600,7 +613,7 @@ __global__ void __launch_bounds__(32 * (dn_warps(TC) + 1), 1)
           const int rr = lane / TC, j = lane % TC;
           const int row = rg * RPW + rr;
           if (j < np && row < rows)
-            pbl[(size_t)pj_l * a.R + row] = a.wts[pj_l] * ldexpf(outv[rg * 32 + lane], sj_l);
+            pbl[(size_t)pj_l * a.R + row] = a.wts[pj_l] * (outv[rg * 32 + lane] * pow2f(sj_l));
         }
         __syncwarp();
       }

@@ -320,12 +320,16 @@ __device__ __forceinline__ int transposed_row(int lane) {
 
 // power-of-two exponent sigma such that max|v| * 2^-sigma lies in [2^14, 2^15):
 // activations scaled by 2^-sigma fit fp16's range with the largest exponent
+// (clamped at -126 so that 2^sigma and 2^-sigma are normal fp32 numbers)
 __device__ __forceinline__ int fp16_prescale_exp(float amax) {
   if (!(amax > 0.f)) return 0;
   int e;
   frexpf(amax, &e);  // amax = f * 2^e, f in [0.5, 1)
-  return e - 15;
+  return max(e - 15, -126);
 }
+
+// 2^e as an fp32 for -126 <= e <= 127 (exact, two integer instructions)
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

@@ -139,8 +139,8 @@ __global__ void __launch_bounds__(288, MINB) w4a16_gemv_kernel(const GemvArgs a)
       }
     }
     const int sig = fp16_prescale_exp(amax);
-    const float down = ldexpf(1.f, -sig);
-    up[m] = ldexpf(1.f, sig);
+    const float down = pow2f(-sig);
+    up[m] = pow2f(sig);
     float sxa = 0.f, sxb = 0.f;
 #pragma unroll
     for (int i = 0; i < WPL; ++i) {

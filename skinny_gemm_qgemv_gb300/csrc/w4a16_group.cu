@@ -171,8 +171,8 @@ __global__ void __launch_bounds__(kGrpThreads, kGrpCtasPerSm) w4a16_group_kernel
         }
       }
       const int sig = fp16_prescale_exp(amax);
-      const float down = ldexpf(1.f, -sig);
-      up = ldexpf(1.f, sig);
+      const float down = pow2f(-sig);
+      up = pow2f(sig);
       float sxa = 0.f, sxb = 0.f;
 #pragma unroll
       for (int i = 0; i < kGrpWPL; ++i) {
