@@ -456,7 +456,7 @@ __global__ void __launch_bounds__(32 * (gu_warps(TC) + 1), 1) moe_mx_gateup_kern
 // down + routing-weighted combine
 // ---------------------------------------------------------------------------
 template <int TC>
-__global__ void __launch_bounds__(32 * (dn_warps(TC) + 1), 1)
+__global__ void __launch_bounds__(32 * (dn_warps(TC) + 2), 1)
     moe_mx_down_kernel(const __grid_constant__ CUtensorMap tm_h, const MxDownArgs a) {
   constexpr int kDnWarps = dn_warps(TC);
   constexpr int RPW = dn_rpw(TC);
@@ -465,8 +465,11 @@ __global__ void __launch_bounds__(32 * (dn_warps(TC) + 1), 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = a.H, I = a.I, P = a.T * a.top_k;
   const uint32_t rcb = I / 2, rsb = I / 32;
-  // h rows land 128B-swizzled (16-byte unit u of block b at u ^ (b & 7)): 1024-byte aligned
-  const uint32_t o_s = a.R * rcb, o_h = (o_s + a.R * rsb + 1023u) & ~1023u;
+  // h rows land 128B-swizzled (16-byte unit u of block b at u ^ (b & 7)): 1024-byte aligned;
+  // the converter warp writes them as fp16 * 2^-sigma at o_hf: block b's four
+  // 16-byte units at b * 64 + ((c ^ ((b >> 1) & 3)) << 4), conflict-free for
+  // the consumers' 128-bit loads
+  const uint32_t o_s = a.R * rcb, o_h = (o_s + a.R * rsb + 1023u) & ~1023u, o_hf = o_h + TC * I * 4;
   pdl_wait();  // the routing table and h come from the previous kernels
   const int nv = *a.nvirt;
   // shared layout (from a 1024-byte aligned base): stages | red [ST][S][RG][32] |
@@ -481,12 +484,14 @@ __global__ void __launch_bounds__(32 * (dn_warps(TC) + 1), 1)
   uint64_t* full = bars;
   uint64_t* empty = bars + a.ST;
   uint64_t* redfull = bars + 2 * a.ST;
+  uint64_t* hready = bars + 3 * a.ST;  // the stage's h is in fp16
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.ST; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kDnWarps);
+      mbar_init(&empty[i], kDnWarps + 1);  // consumers + the h converter
       mbar_init(&redfull[i], a.S > 1 ? (a.S - 1) * a.RG : 1);
+      mbar_init(&hready[i], 1);
     }
     fence_mbar_init();
   }
@@ -530,6 +535,53 @@ __global__ void __launch_bounds__(32 * (dn_warps(TC) + 1), 1)
     return;
   }
 
+  if (warp == kDnWarps + 1) {
+    // ------------------------------------------------------- h converter
+    // once per stage for the whole CTA: fp32 h of the virtual expert's pairs
+    // -> fp16 * 2^-sigma (sigma from the pair's max |h|: in fp16's range)
+    int st = 0;
+    uint32_t par = 0;
+    bool ok = true;
+    for (int ri = blockIdx.x; ri < a.nranges && ok; ri += gridDim.x) {
+      for (int i = 0, v = vstart; i < nv; ++i, v = (v + 1 == nv ? 0 : v + 1)) {
+        const int np = vtab[v * kMxVexpInts + 1];
+        if (ok) ok = mbar_wait(&full[st], par, a.err, kErrMoeWait);
+        if (ok) {
+          uint8_t* sbase = stages + (size_t)st * a.stage_bytes;
+          for (int j = 0; j < np; ++j) {
+            const float sc = pow2f(-sigp[vtab[v * kMxVexpInts + 2 + j]]);
+            for (int b = lane; b < I / 32; b += 32) {
+              const uint32_t hp = smem_u32(sbase + o_h + j * (I * 4) + b * 128);
+              const uint32_t hq = smem_u32(sbase + o_hf + j * (I * 2) + b * 64);
+              const uint32_t sw = (uint32_t)b & 7u, sw2 = ((uint32_t)b >> 1) & 3u;
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                const uint4 w0 = lds128(hp + (((uint32_t)(2 * c) ^ sw) << 4));
+                const uint4 w1 = lds128(hp + (((uint32_t)(2 * c + 1) ^ sw) << 4));
+                uint4 o;
+                o.x = f32x2_to_f16x2(__uint_as_float(w0.x) * sc, __uint_as_float(w0.y) * sc);
+                o.y = f32x2_to_f16x2(__uint_as_float(w0.z) * sc, __uint_as_float(w0.w) * sc);
+                o.z = f32x2_to_f16x2(__uint_as_float(w1.x) * sc, __uint_as_float(w1.y) * sc);
+                o.w = f32x2_to_f16x2(__uint_as_float(w1.z) * sc, __uint_as_float(w1.w) * sc);
+                sts128(hq + (((uint32_t)c ^ sw2) << 4), o);
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&hready[st]);
+          mbar_arrive(&empty[st]);
+        }
+        if (++st == a.ST) {
+          st = 0;
+          par ^= 1u;
+        }
+      }
+    }
+    return;
+  }
+
   // -------------------------------------------------------------- consumers
   const int s = warp % a.S, rg = warp / a.S;
   const bool busy = rg < a.RG;
@@ -551,26 +603,26 @@ __global__ void __launch_bounds__(32 * (dn_warps(TC) + 1), 1)
       const int jl = lane % TC;
       const int pj_l = vtab[v * kMxVexpInts + 2 + jl];
       const int sj_l = pj_l >= 0 ? sigp[pj_l] : 0;
-      if (ok) ok = mbar_wait(&full[cst], cpar, a.err, kErrMoeWait);
+      if (ok) ok = mbar_wait(&hready[cst], cpar, a.err, kErrMoeWait);
       const uint8_t* sbase = stages + (size_t)cst * a.stage_bytes;
       float acc[V];
 #pragma unroll
       for (int q = 0; q < V; ++q) acc[q] = 0.f;
       if (on && ok) {
-        // this lane's 32 values of h per pair: fp32 in the stage -> fp16 * 2^-sigma
+        // this lane's 32 values of h per pair, fp16 * 2^-sigma from the converter warp
         uint32_t xr[TC][16];
 #pragma unroll
         for (int j = 0; j < TC; ++j) {
           if (j < np) {
-            const int sj = sigp[vtab[v * kMxVexpInts + 2 + j]];
-            const float sc = pow2f(-sj);
-            const uint32_t hp = smem_u32(sbase + o_h + j * (I * 4) + kb * 128);
-            const uint32_t sw = (uint32_t)kb & 7u;
+            const uint32_t hq = smem_u32(sbase + o_hf + j * (I * 2) + kb * 64);
+            const uint32_t sw2 = ((uint32_t)kb >> 1) & 3u;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const uint4 w = lds128(hp + (((uint32_t)c ^ sw) << 4));
-              xr[j][2 * c] = f32x2_to_f16x2(__uint_as_float(w.x) * sc, __uint_as_float(w.y) * sc);
-              xr[j][2 * c + 1] = f32x2_to_f16x2(__uint_as_float(w.z) * sc, __uint_as_float(w.w) * sc);
+            for (int c = 0; c < 4; ++c) {
+              const uint4 w = lds128(hq + (((uint32_t)c ^ sw2) << 4));
+              xr[j][4 * c] = w.x;
+              xr[j][4 * c + 1] = w.y;
+              xr[j][4 * c + 2] = w.z;
+              xr[j][4 * c + 3] = w.w;
             }
           } else {
 #pragma unroll
@@ -662,12 +714,12 @@ MxPlan plan_down(int T, int H, int I, int E, int top_k, int tc) {
   p.RG = dn_warps(tc) / p.S;
   p.R = p.RG * dn_rpw(tc);
   const uint32_t o_h = (uint32_t)((p.R * (I / 2 + I / 32) + 1023) & ~1023);
-  p.stage_bytes = (uint32_t)((o_h + tc * I * 4 + 1023) & ~1023);
+  p.stage_bytes = (uint32_t)((o_h + tc * I * 6 + 1023) & ~1023);  // + fp32 h and its fp16 copy
   const size_t P = (size_t)T * top_k;
   p.nvmax = moe_nvirt_max(T, E, top_k);
   const size_t fixed = sizeof(float) * (p.RG * 32 + P * p.R) +
                        sizeof(int32_t) * ((size_t)p.nvmax * kMxVexpInts + ((P + 1) & ~(size_t)1)) + 64 + 1024;
-  const size_t per_stage = p.stage_bytes + sizeof(float) * p.S * p.RG * 32 + 3 * 8;
+  const size_t per_stage = p.stage_bytes + sizeof(float) * p.S * p.RG * 32 + 4 * 8;
   p.ST = fixed < kSmemBudget ? (int)std::min<size_t>(4, (kSmemBudget - fixed) / per_stage) : 0;
   p.smem = fixed + (size_t)p.ST * per_stage;
   p.count = (H + p.R - 1) / p.R;
@@ -721,7 +773,7 @@ static cudaError_t launch_mx_tc(const uint8_t* gq, const uint8_t* gs, const uint
     return cudaErrorInvalidValue;
   e = allow_max_smem(moe_mx_down_kernel<TC>);
   if (e != cudaSuccess) return e;
-  return launch_kernel(moe_mx_down_kernel<TC>, dim3(std::min(sms, pd.count)), dim3(32 * (dn_warps(TC) + 1)), pd.smem,
+  return launch_kernel(moe_mx_down_kernel<TC>, dim3(std::min(sms, pd.count)), dim3(32 * (dn_warps(TC) + 2)), pd.smem,
                        stream, pdl, tm_h, da);
 }
 
