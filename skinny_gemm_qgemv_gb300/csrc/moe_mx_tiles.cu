@@ -45,9 +45,9 @@ constexpr size_t kSmemBudget = 224 * 1024;
 // Consumer warps and rows per warp. With one pair per virtual expert (T = 1)
 // the activations take 16 registers, so more warps fit the register file.
 constexpr int gu_warps(int tc) { return tc == 1 ? 21 : 14; }
-constexpr int dn_warps(int tc) { return tc == 1 ? 24 : 12; }
+constexpr int dn_warps(int tc) { return tc == 1 ? 12 : 12; }
 constexpr int gu_rpw(int) { return 4; }
-constexpr int dn_rpw(int) { return 4; }
+constexpr int dn_rpw(int tc) { return tc == 1 ? 8 : 4; }
 constexpr int kMaxSlices = 12;  // K / 1024 of either matrix (one 32-k block per lane)
 
 struct MxGateUpArgs {
