@@ -163,9 +163,10 @@ QG_API void qgemv_w4a16_group_destroy(qg_w4_group *group);
  *   M       1..32 (M = 1 is the same result as qgemv_w4a16).
  *   workspace / ws_bytes: at least qg_skinny_workspace_size(M, N, K,
  *           group_size) bytes of device memory, 16-byte aligned, zero-filled
- *           before its first use. Every completed call leaves it zero-filled
- *           again (it holds split-K partial sums and arrival counters), so one
- *           workspace serves any sequence of calls ordered on one stream;
+ *           before its first use. Its first 1024 bytes are arrival counters
+ *           that every completed call leaves at zero again; the rest is
+ *           scratch (the activations' MMA operands, split-K partial sums). So
+ *           one workspace serves any sequence of calls ordered on one stream;
  *           calls that may overlap need separate workspaces. After a call that
  *           reported a device error (qg_device_error) zero-fill it again.
  */
@@ -201,10 +202,12 @@ QG_API size_t qg_skinny_workspace_size(int M, int N, int K, int group_size);
  *                    copies). The descriptors' buffers are used by every later
  *                    run: they must stay allocated until the group is
  *                    destroyed. *group is set on QG_OK.
- *   qgemm_w4a16_skinny_group_run     one launch on stream computing every Y_i
- *                    from the current contents of X_i and W_i; no workspace,
- *                    stream-ordered, no allocation, capturable in a CUDA
- *                    graph. Run it on the device that was current at create.
+ *   qgemm_w4a16_skinny_group_run     computes every Y_i from the current
+ *                    contents of X_i and W_i: for M <= 16 two launches (the
+ *                    activations' MMA operands, then the grid over all row
+ *                    tiles), else one; no workspace, stream-ordered, no
+ *                    allocation, capturable in a CUDA graph. Run it on the
+ *                    device that was current at create.
  *   qgemm_w4a16_skinny_group_destroy frees the plan (NULL is ignored); no run
  *                    of the group may be pending.
  */

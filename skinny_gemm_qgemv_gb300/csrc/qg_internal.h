@@ -80,9 +80,10 @@ struct TcGroupItem {
   int M, N, K;
 };
 struct TcGroupPlan {
-  void* d_gemvs;  // device descriptors (tensor maps + shapes)
-  int* d_cta;     // [grid + 1] first unit of each CTA, then [grid] its projection
-  int ngemv, grid, NT, ST;
+  void* d_gemvs;    // device descriptors (tensor maps + shapes)
+  int* d_cta;       // [grid + 1] first unit of each CTA, then [grid] its projection
+  void* d_scratch;  // M <= 16: every projection's B fragments and group table
+  int ngemv, grid, NT, ST, mma, max_groups;
   uint32_t stage_bytes;
   size_t smem;
 };

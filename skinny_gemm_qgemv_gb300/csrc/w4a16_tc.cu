@@ -77,6 +77,9 @@ constexpr int kThreads = 480;  // 1 producer + 2 MMA + 8 converter + 4 epilogue 
 struct TcGemv {
   CUtensorMap codes, scales, biases, x;
   float* y;
+  const uint16_t* xraw;  // the activations (mma path: read by the B-fragment pass)
+  uint32_t* frag;        // mma path: B fragments of X, K * 32 bytes
+  float* tab;            // mma path: per 64-k group offsets, sums of x and 2^sigma
   int N, M, K;
   int unit0, unit_end;  // its row tiles in the launch's unit numbering
 };
@@ -91,6 +94,8 @@ struct TcArgs {
   float* partial;
   uint32_t* counters;
   uint32_t* err;
+  const uint32_t* frag;  // mma path, one matrix: B fragments and group table
+  const float* tab;
   // grouped launch (null for one matrix): per-projection descriptors, the
   // first unit of every CTA's range ([grid + 1]) and the projection of that unit
   const TcGemv* gemvs;
@@ -105,6 +110,8 @@ struct UnitWalk {
   int u, end, stride, g;
   int tile, n0, k0, kper, N, M;
   float* y;
+  const uint32_t* frag;
+  const float* tab;
   __device__ __forceinline__ explicit UnitWalk(const TcArgs& a) {
     if (a.gemvs) {
       u = a.cta_unit0[blockIdx.x];
@@ -135,6 +142,8 @@ struct UnitWalk {
       N = d.N;
       M = d.M;
       y = d.y;
+      frag = d.frag;
+      tab = d.tab;
     } else {
       tile = u / a.splits;
       k0 = (u % a.splits) * a.kper;
@@ -142,6 +151,8 @@ struct UnitWalk {
       N = a.N;
       M = a.M;
       y = a.y;
+      frag = a.frag;
+      tab = a.tab;
     }
     n0 = tile * kRows;
   }
@@ -610,6 +621,387 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Skinny GEMM with warp-level MMA, M <= 16 (w4a16_mma_kernel)
+//
+// At N = 16 activation rows one tcgen05.mma (M = 128, K = 16) costs its issuing
+// thread about 44 cycles whatever N is, and its A operand has to be handed from
+// converter warps to the issuer through TMEM; the resulting chain of hand-offs
+// sets the tcgen05 kernel's period. Here every consumer warp decodes its own
+// weights into registers and multiplies them with mma.sync.m16n8k16 (f16 in,
+// fp32 accumulate), so no role waits on another within a stage:
+//  * The same TMA stages as the tcgen05 kernel carry the codes (128 rows x
+//    512 k, 128B-swizzled), the fp16 scales and biases, and -- instead of the
+//    X tile -- the stage's B fragments, prepared once per call by
+//    w4a16_mma_prep_kernel (below) for the whole matrix.
+//  * Warp w of the 8 consumer warps owns 64-k group w of every stage and all
+//    128 rows (eight 16-row blocks): the B fragments of its group are loaded
+//    once per stage and reused by all row blocks.
+//  * A codes word gives four fp16x2 registers with one shift and four lop3:
+//    (1024 + q) for codes 0, 4 / 2, 6 and (1024 + 16 q) for codes 1, 5 / 3, 7
+//    (exact). Lane (g, c) takes words 2c, 2c + 1 of rows g and g + 8 of a row
+//    block; the k order inside a group is permuted the same way in A and B, and
+//    the B fragment of a (1024 + 16 q) slot holds x / 16, so one accumulator
+//    per output collects 1024 X_A + 64 X_B + sum q x': it starts at minus that
+//    offset (from the table), so the MMA result is sum q x' directly.
+//  * Per group: y += s * 2^sigma * acc + b * sum x, in paired fp32 FMAs; at the
+//    end of a 128-row tile the eight warps' partial sums are added in warp
+//    order through shared memory (deterministic).
+// ---------------------------------------------------------------------------
+constexpr int kMmaWarps = 8;                           // consumer warps = 64-k groups per stage
+constexpr int kMmaThreads = 32 * (kMmaWarps + 1);      // + 1 producer warp
+constexpr uint32_t kMmaFragStage = 8 * 2048;           // B fragments of one stage: 8 groups x 2 KB
+constexpr uint32_t kMmaStageBytes = 32768 + 4096 + kMmaFragStage;  // codes, scales + biases, fragments
+constexpr uint32_t kMmaRedBytes = kMmaWarps * 16 * 32 * 16;        // 64 KB: partial tiles of all warps
+constexpr int kMmaTab = 48;                            // floats per group: offset[16], sum x[16], 2^sigma
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t f16x2_of(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ void f16x2_to_f32(uint32_t v, float& lo, float& hi) {
+  asm("{.reg .f16 l, h; mov.b32 {l, h}, %2; cvt.f32.f16 %0, l; cvt.f32.f16 %1, h;}" : "=f"(lo), "=f"(hi) : "r"(v));
+}
+
+struct MmaPrepArgs {
+  const TcGemv* gemvs;  // grouped launch (null: one matrix)
+  int ngemv;
+  const uint16_t* x;    // one matrix
+  uint32_t* frag;
+  float* tab;
+  int M, K;
+};
+
+// B fragments of X for every 64-k group: one warp per group. Lane (g, c) covers
+// activation rows g and g + 8 at k = 16c .. 16c + 15 of the group (words 2c and
+// 2c + 1); step s = 0..3 of the group uses word 2c + (s >> 1) and codes
+// j = 2 (s & 1) (slots 2c, 2c + 1 <- codes j, j + 4) and j + 1 (slots 2c + 8,
+// 2c + 9 <- codes j + 1, j + 5, divided by 16). sigma is per group: the
+// group's largest |x| (over all rows) just below 2^15 after scaling.
+__global__ void __launch_bounds__(256) w4a16_mma_prep_kernel(const MmaPrepArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gi = blockIdx.x * 8 + warp;
+  const uint16_t* x = a.x;
+  uint32_t* frag = a.frag;
+  float* tab = a.tab;
+  int M = a.M, K = a.K;
+  if (a.gemvs) {
+    const TcGemv& d = a.gemvs[blockIdx.y];
+    x = d.xraw;
+    frag = d.frag;
+    tab = d.tab;
+    M = d.M;
+    K = d.K;
+  }
+  pdl_wait();  // x may come from the previous kernel
+  if (gi < K / 64) {
+    const int g = lane >> 2, c = lane & 3;
+    const int k0 = gi * 64 + 16 * c;
+    float v[2][16];
+    float amax = 0.f;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const int m = g + 8 * t;
+      uint4 u0 = make_uint4(0, 0, 0, 0), u1 = make_uint4(0, 0, 0, 0);
+      if (m < M) {
+        const uint4* p = reinterpret_cast<const uint4*>(x + (size_t)m * K + k0);
+        u0 = p[0];
+        u1 = p[1];
+      }
+      const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        v[t][2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
+        v[t][2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[t][i]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const int sig = fp16_prescale_exp(amax);
+    const float down = pow2f(-sig), down16 = pow2f(-sig - 4);
+    uint32_t b[16];
+    float off[2] = {0.f, 0.f}, sx[2] = {0.f, 0.f};
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        const int wb = 8 * (s >> 1), j = 2 * (s & 1);  // the word's first value in v, first code
+        const uint32_t b0 = f16x2_of(v[t][wb + j] * down, v[t][wb + j + 4] * down);
+        const uint32_t b1 = f16x2_of(v[t][wb + j + 1] * down16, v[t][wb + j + 5] * down16);
+        b[(s * 2 + t) * 2] = b0;
+        b[(s * 2 + t) * 2 + 1] = b1;
+        float l0, h0, l1, h1;
+        f16x2_to_f32(b0, l0, h0);
+        f16x2_to_f32(b1, l1, h1);
+        off[t] += (l0 + h0) + (l1 + h1);
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) sx[t] += v[t][i];
+    }
+    // fragments: [u][lane][4] of this group, 16-byte units contiguous over the lanes
+    uint4* fg = reinterpret_cast<uint4*>(frag + (size_t)gi * 512);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) fg[u * 32 + lane] = make_uint4(b[4 * u], b[4 * u + 1], b[4 * u + 2], b[4 * u + 3]);
+    // per row: 1024 x (the sum of its fragment values), the sum of x; lanes of one row add up
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      off[t] += __shfl_xor_sync(0xFFFFFFFFu, off[t], 1);
+      off[t] += __shfl_xor_sync(0xFFFFFFFFu, off[t], 2);
+      sx[t] += __shfl_xor_sync(0xFFFFFFFFu, sx[t], 1);
+      sx[t] += __shfl_xor_sync(0xFFFFFFFFu, sx[t], 2);
+    }
+    float* tg = tab + (size_t)gi * kMmaTab;
+    if (c == 0) {
+      tg[g] = 1024.f * off[0];
+      tg[g + 8] = 1024.f * off[1];
+      tg[16 + g] = sx[0];
+      tg[16 + g + 8] = sx[1];
+    }
+    if (lane == 0) tg[32] = pow2f(sig);
+  }
+  pdl_launch_dependents();
+}
+
+__global__ void __launch_bounds__(kMmaThreads, 1)
+    w4a16_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scales,
+                     const __grid_constant__ CUtensorMap tm_biases, const TcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const gbase = smem_raw + (base - raw);
+  // shared layout: stages | red (64 KB) | barriers
+  const uint32_t s_stages = base;
+  float* red = reinterpret_cast<float*>(gbase + a.ST * kMmaStageBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(gbase + a.ST * kMmaStageBytes + kMmaRedBytes);
+  uint64_t* empty = full + a.ST;
+  volatile uint32_t* is_last = reinterpret_cast<uint32_t*>(empty + a.ST);
+  // per stage: codes [2 chunks][128 rows][128 B] | scales [128][8] | biases [128][8] | fragments
+  constexpr uint32_t c_off = 0, s_off = 32768, b_off = s_off + 2048, f_off = b_off + 2048;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < a.ST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kMmaWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_wait();  // the fragments come from the preparation kernel
+
+  if (warp == kMmaWarps) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      int issued = 0, fenced = -1;
+      bool ok = true;
+      for (UnitWalk w(a); w.valid() && ok; w.next(a)) {
+        const int nstage = w.kper / kStageK;
+        if (a.gemvs && w.g != fenced) {
+          const TcGemv* d = &a.gemvs[w.g];
+          tensormap_acquire(&d->codes);
+          tensormap_acquire(&d->scales);
+          tensormap_acquire(&d->biases);
+          fenced = w.g;
+        }
+        const CUtensorMap* mc = a.gemvs ? &a.gemvs[w.g].codes : &tm_codes;
+        const CUtensorMap* ms = a.gemvs ? &a.gemvs[w.g].scales : &tm_scales;
+        const CUtensorMap* mb = a.gemvs ? &a.gemvs[w.g].biases : &tm_biases;
+        for (int s = 0; s < nstage; ++s) {
+          const int sg = issued, st = sg % a.ST;
+          if (sg >= a.ST) ok = mbar_wait(&empty[st], ((sg / a.ST) & 1) ^ 1, a.err, kErrTcEmptyWait);
+          if (!ok) break;
+          const uint32_t sb = s_stages + st * kMmaStageBytes;
+          mbar_arrive_expect_tx(&full[st], kMmaStageBytes);
+          const int kk = w.k0 + s * kStageK;
+          tma_load_3d(sb + c_off, mc, 0, w.n0, kk / 256, &full[st]);
+          tma_load_2d(sb + s_off, ms, kk / 64, w.n0, &full[st]);
+          tma_load_2d(sb + b_off, mb, kk / 64, w.n0, &full[st]);
+          bulk_g2s(gbase + (sb - s_stages) + f_off, w.frag + (size_t)(kk / 64) * 512, kMmaFragStage, &full[st]);
+          ++issued;
+        }
+      }
+      for (int j = max(0, issued - a.ST); j < issued; ++j)
+        mbar_wait(&full[j % a.ST], (j / a.ST) & 1, a.err, kErrTcDrain);
+    }
+  } else {
+    // ---------------------------------------------------------------- consumers
+    const int g = lane >> 2, c = lane & 3;
+    const int et = threadIdx.x;  // 0..255
+    int sgc = 0;                 // stages consumed
+    bool ok = true;
+    for (UnitWalk w(a); w.valid(); w.next(a)) {
+      const int nstage = w.kper / kStageK;
+      uint64_t y2[8][2][2];  // [row block][n tile][rows g, g + 8]: (col 2c, col 2c + 1)
+#pragma unroll
+      for (int rb = 0; rb < 8; ++rb)
+#pragma unroll
+        for (int t = 0; t < 2; ++t) y2[rb][t][0] = y2[rb][t][1] = 0ull;
+      for (int s = 0; s < nstage; ++s, ++sgc) {
+        const int st = sgc % a.ST;
+        // this warp's group: offsets and sums of x of its output columns, 2^sigma
+        const int gi = (w.k0 + s * kStageK) / 64 + warp;
+        const float* tg = w.tab + (size_t)gi * kMmaTab;
+        const float2 o0 = __ldg(reinterpret_cast<const float2*>(tg + 2 * c));
+        const float2 o1 = __ldg(reinterpret_cast<const float2*>(tg + 8 + 2 * c));
+        const float2 x0 = __ldg(reinterpret_cast<const float2*>(tg + 16 + 2 * c));
+        const float2 x1 = __ldg(reinterpret_cast<const float2*>(tg + 24 + 2 * c));
+        const float up = __ldg(tg + 32);
+        if (ok) ok = mbar_wait(&full[st], (sgc / a.ST) & 1, a.err, kErrTcFullWait);
+        const uint32_t sb = s_stages + st * kMmaStageBytes;
+        if (ok) {
+          uint32_t b[16];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint4 v = lds128(sb + f_off + warp * 2048 + (u * 32 + lane) * 16);
+            b[4 * u] = v.x;
+            b[4 * u + 1] = v.y;
+            b[4 * u + 2] = v.z;
+            b[4 * u + 3] = v.w;
+          }
+          const uint64_t sxp[2] = {pair2(__float_as_uint(x0.x), __float_as_uint(x0.y)),
+                                   pair2(__float_as_uint(x1.x), __float_as_uint(x1.y))};
+          // codes of group `warp`: chunk warp / 4, 32-byte segment warp % 4 of each 128-byte row;
+          // words 2c, 2c + 1 are 8 bytes of 16-byte unit 2 (warp % 4) + c / 2
+          const uint32_t cu = 2u * (uint32_t)(warp & 3) + ((uint32_t)c >> 1);
+          const uint32_t cbase = sb + c_off + (uint32_t)(warp >> 2) * 16384 + 8u * (uint32_t)(c & 1);
+#pragma unroll
+          for (int rb = 0; rb < 8; ++rb) {
+            const int r0 = 16 * rb + g;  // rows r0 and r0 + 8 share the swizzle (r & 7 = g)
+            const uint32_t sw = (cu ^ (uint32_t)g) << 4;
+            const uint2 w0 = lds64(cbase + r0 * 128 + sw);
+            const uint2 w1 = lds64(cbase + (r0 + 8) * 128 + sw);
+            uint32_t q00[4], q01[4], q10[4], q11[4];  // [row][word]
+            nib8_to_f16x2_offset(w0.x, q00);
+            nib8_to_f16x2_offset(w0.y, q01);
+            nib8_to_f16x2_offset(w1.x, q10);
+            nib8_to_f16x2_offset(w1.y, q11);
+            float acc[2][4];
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              const float2 o = t == 0 ? o0 : o1;
+              acc[t][0] = -o.x;
+              acc[t][1] = -o.y;
+              acc[t][2] = -o.x;
+              acc[t][3] = -o.y;
+            }
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4) {
+              const uint32_t* qa = (s4 >> 1) ? q01 : q00;
+              const uint32_t* qb = (s4 >> 1) ? q11 : q10;
+              const int p = 2 * (s4 & 1);
+#pragma unroll
+              for (int t = 0; t < 2; ++t)
+                mma_16816(acc[t], qa[p], qb[p], qa[p + 1], qb[p + 1], b[(s4 * 2 + t) * 2], b[(s4 * 2 + t) * 2 + 1]);
+            }
+            const float s0 = f16_bits_to_f32(lds16(sb + s_off + r0 * 16 + 2 * warp));
+            const float s1 = f16_bits_to_f32(lds16(sb + s_off + (r0 + 8) * 16 + 2 * warp));
+            const float bb0 = f16_bits_to_f32(lds16(sb + b_off + r0 * 16 + 2 * warp));
+            const float bb1 = f16_bits_to_f32(lds16(sb + b_off + (r0 + 8) * 16 + 2 * warp));
+            const float cf0 = s0 * up, cf1 = s1 * up;
+            const uint64_t c0 = pair2(__float_as_uint(cf0), __float_as_uint(cf0));
+            const uint64_t c1 = pair2(__float_as_uint(cf1), __float_as_uint(cf1));
+            const uint64_t d0 = pair2(__float_as_uint(bb0), __float_as_uint(bb0));
+            const uint64_t d1 = pair2(__float_as_uint(bb1), __float_as_uint(bb1));
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              y2[rb][t][0] = ffma2(c0, pair2(__float_as_uint(acc[t][0]), __float_as_uint(acc[t][1])),
+                                   ffma2(d0, sxp[t], y2[rb][t][0]));
+              y2[rb][t][1] = ffma2(c1, pair2(__float_as_uint(acc[t][2]), __float_as_uint(acc[t][3])),
+                                   ffma2(d1, sxp[t], y2[rb][t][1]));
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+      }
+      // the 8 warps' partial tiles -> one tile, summed in warp order
+      {
+        uint4* rv = reinterpret_cast<uint4*>(red);
+#pragma unroll
+        for (int rb = 0; rb < 8; ++rb)
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            float e0, e1, e2, e3;
+            unpair2(y2[rb][t][0], e0, e1);
+            unpair2(y2[rb][t][1], e2, e3);
+            rv[(warp * 16 + rb * 2 + t) * 32 + lane] =
+                make_uint4(__float_as_uint(e0), __float_as_uint(e1), __float_as_uint(e2), __float_as_uint(e3));
+          }
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      {
+        // thread et: lane et % 32 of units 2 (et / 32), 2 (et / 32) + 1 (row block, n tile)
+        const int ln = et & 31, u0 = 2 * (et >> 5);
+        const int gg = ln >> 2, cc = ln & 3;
+        const uint4* rv = reinterpret_cast<const uint4*>(red);
+        float tot[2][4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) tot[h][e] = 0.f;
+#pragma unroll
+        for (int w2 = 0; w2 < kMmaWarps; ++w2)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint4 v = rv[(w2 * 16 + u0 + h) * 32 + ln];
+            tot[h][0] += __uint_as_float(v.x);
+            tot[h][1] += __uint_as_float(v.y);
+            tot[h][2] += __uint_as_float(v.z);
+            tot[h][3] += __uint_as_float(v.w);
+          }
+        const bool whole = a.gemvs || a.splits == 1;
+        float* part = whole ? nullptr : a.partial + (size_t)w.u * 16 * kRows;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int uu = u0 + h, rb = uu >> 1, t = uu & 1;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int row = 16 * rb + gg + 8 * (e >> 1);
+            const int m = 8 * t + 2 * cc + (e & 1);
+            if (whole) {
+              if (m < w.M && w.n0 + row < w.N) w.y[(size_t)m * w.N + w.n0 + row] = tot[h][e];
+            } else {
+              part[m * kRows + row] = tot[h][e];
+            }
+          }
+        }
+        if (!whole) {
+          // split K: the CTA that finishes a row tile last adds the partial tiles in split order
+          __threadfence();
+          asm volatile("bar.sync 1, 256;" ::: "memory");
+          if (et == 0) *is_last = (atomicAdd(&a.counters[w.tile], 1u) == (uint32_t)(a.splits - 1)) ? 1u : 0u;
+          asm volatile("bar.sync 1, 256;" ::: "memory");
+          if (*is_last) {
+            __threadfence();
+            for (int q = et; q < 16 * kRows; q += 256) {
+              const int m = q / kRows, row = q % kRows;
+              float acc = 0.f;
+              for (int s2 = 0; s2 < a.splits; ++s2)
+                acc += __ldcg(a.partial + (size_t)(w.tile * a.splits + s2) * 16 * kRows + q);
+              if (m < w.M && w.n0 + row < w.N) w.y[(size_t)m * w.N + w.n0 + row] = acc;
+            }
+            if (et == 0) a.counters[w.tile] = 0u;
+          }
+        }
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+    }
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+}
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 namespace {
@@ -643,13 +1035,25 @@ int stages_for(int NT, uint32_t stage_bytes, size_t* smem) {
 
 struct TcPlan {
   int NT, ntiles, splits, kper, nunits, ST;
+  bool mma;  // M <= 16: the warp-level MMA kernel
   uint32_t stage_bytes;
-  size_t smem, ws_partial, ws_counters;
+  size_t smem, ws_partial, ws_counters, ws_frag, ws_tab;
 };
+
+// shared memory of the mma kernel with ST stages: alignment slack, stages, the
+// 64 KB reduction buffer, barriers
+size_t mma_smem(int ST) { return 1024 + (size_t)ST * kMmaStageBytes + kMmaRedBytes + 16 * (size_t)ST + 64; }
+
+int mma_stages() {
+  int ST = 4;
+  while (ST > 2 && mma_smem(ST) > (size_t)device_max_smem_optin()) --ST;
+  return ST;
+}
 
 TcPlan tc_plan(int M, int N, int K, int sms) {
   TcPlan p;
   p.NT = M <= 16 ? 16 : 32;
+  p.mma = M <= 16;
   p.ntiles = (N + kRows - 1) / kRows;
   const int kstages = K / kStageK;
   // split K until every SM has a unit, keeping each split a whole number of stages
@@ -659,10 +1063,18 @@ TcPlan tc_plan(int M, int N, int K, int sms) {
   p.nunits = p.ntiles * p.splits;
   p.stage_bytes = (uint32_t)(p.NT * 1024 + 36864);
   p.ST = stages_for(p.NT, p.stage_bytes, &p.smem);
+  p.ws_frag = p.ws_tab = 0;
+  if (p.mma) {
+    p.stage_bytes = kMmaStageBytes;
+    p.ST = mma_stages();
+    p.smem = mma_smem(p.ST);
+    p.ws_frag = (size_t)K * 32;                       // B fragments: 2 KB per 64-k group
+    p.ws_tab = (size_t)(K / 64) * kMmaTab * 4;        // offsets, sums of x, 2^sigma per group
+  }
   p.ws_partial = p.splits > 1 ? sizeof(float) * (size_t)p.nunits * p.NT * kRows : 0;
   // the counters sit at a fixed place (the workspace's first bytes) for every
   // shape, so a later call never finds partial sums of another shape there
-  p.ws_counters = p.splits > 1 ? kCounterBytes : 0;
+  p.ws_counters = (p.splits > 1 || p.mma) ? kCounterBytes : 0;
   return p;
 }
 
@@ -675,7 +1087,7 @@ bool tc_path_ok(int M, int N, int K) {
 size_t tc_workspace_size(int M, int N, int K) {
   if (!tc_path_ok(M, N, K)) return 0;
   const TcPlan p = tc_plan(M, N, K, device_sm_count());
-  return p.ws_counters + p.ws_partial;
+  return p.ws_counters + p.ws_frag + p.ws_tab + p.ws_partial;
 }
 
 template <int NT>
@@ -696,7 +1108,7 @@ cudaError_t launch_w4a16_tc(const uint32_t* wq, const uint16_t* sc, const uint16
   if (ws_bytes < tc_workspace_size(M, N, K)) return cudaErrorInvalidValue;
   CUtensorMap maps[4];
   if (!tc_maps(maps, wq, sc, bi, x, M, N, K, p.NT)) return cudaErrorInvalidValue;
-  TcArgs a;
+  TcArgs a{};
   a.N = N;
   a.K = K;
   a.M = M;
@@ -707,8 +1119,13 @@ cudaError_t launch_w4a16_tc(const uint32_t* wq, const uint16_t* sc, const uint16
   a.ST = p.ST;
   a.stage_bytes = p.stage_bytes;
   a.y = y;
-  a.counters = p.splits > 1 ? static_cast<uint32_t*>(ws) : nullptr;
-  a.partial = p.splits > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kCounterBytes) : nullptr;
+  // workspace: counters | B fragments | group table | partial tiles
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  a.counters = p.splits > 1 ? reinterpret_cast<uint32_t*>(wsb) : nullptr;
+  uint8_t* after = wsb + p.ws_counters;
+  a.frag = p.mma ? reinterpret_cast<uint32_t*>(after) : nullptr;
+  a.tab = p.mma ? reinterpret_cast<float*>(after + p.ws_frag) : nullptr;
+  a.partial = p.splits > 1 ? reinterpret_cast<float*>(after + p.ws_frag + p.ws_tab) : nullptr;
   a.err = err;
   a.gemvs = nullptr;
   a.cta_unit0 = nullptr;
@@ -716,6 +1133,20 @@ cudaError_t launch_w4a16_tc(const uint32_t* wq, const uint16_t* sc, const uint16
   // the counters start at zero (caller contract) and the last arriver of every
   // tile resets its counter, so no clearing launch is needed between calls
   const int grid = std::min(p.nunits, sms);
+  if (p.mma) {
+    MmaPrepArgs pa{};
+    pa.x = x;
+    pa.frag = const_cast<uint32_t*>(a.frag);
+    pa.tab = const_cast<float*>(a.tab);
+    pa.M = M;
+    pa.K = K;
+    cudaError_t e = launch_kernel(w4a16_mma_prep_kernel, dim3((K / 64 + 7) / 8), dim3(256), 0, stream, pdl, pa);
+    if (e != cudaSuccess) return e;
+    e = allow_max_smem(w4a16_mma_kernel);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(w4a16_mma_kernel, dim3(grid), dim3(kMmaThreads), p.smem, stream, pdl, maps[0], maps[1],
+                         maps[2], a);
+  }
   if (p.NT == 16) return launch_tc_nt<16>(maps, a, p, grid, stream, pdl);
   return launch_tc_nt<32>(maps, a, p, grid, stream, pdl);
 }
@@ -736,8 +1167,11 @@ cudaError_t tc_group_plan_build(const TcGroupItem* list, int n, int sms, TcGroup
   if (n < 1 || tc_group_check(list, n) != 0) return cudaErrorInvalidValue;
   TcGroupPlan p{};
   p.NT = list[0].M <= 16 ? 16 : 32;
+  p.mma = list[0].M <= 16 ? 1 : 0;
   std::vector<TcGemv> g(n);
   long long units = 0;
+  size_t scratch = 0;  // mma path: every projection's B fragments and group table
+  for (int i = 0; i < n; ++i) scratch += (size_t)list[i].K * 32 + (size_t)(list[i].K / 64) * kMmaTab * 4;
   for (int i = 0; i < n; ++i) {
     const TcGroupItem& it = list[i];
     CUtensorMap maps[4];
@@ -748,9 +1182,13 @@ cudaError_t tc_group_plan_build(const TcGroupItem* list, int n, int sms, TcGroup
     d.biases = maps[2];
     d.x = maps[3];
     d.y = it.y;
+    d.xraw = it.x;
+    d.frag = nullptr;
+    d.tab = nullptr;
     d.N = it.N;
     d.M = it.M;
     d.K = it.K;
+    p.max_groups = std::max(p.max_groups, it.K / 64);
     d.unit0 = (int)units;
     units += (it.N + kRows - 1) / kRows;
     if (units >= (1LL << 30)) return cudaErrorInvalidValue;
@@ -777,11 +1215,30 @@ cudaError_t tc_group_plan_build(const TcGroupItem* list, int n, int sms, TcGroup
   p.grid = grid;
   p.stage_bytes = (uint32_t)(p.NT * 1024 + 36864);
   p.ST = stages_for(p.NT, p.stage_bytes, &p.smem);
-  cudaError_t e = cudaMalloc(&p.d_gemvs, sizeof(TcGemv) * n);
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
+  if (p.mma) {
+    p.stage_bytes = kMmaStageBytes;
+    p.ST = mma_stages();
+    p.smem = mma_smem(p.ST);
+    e = cudaMalloc(&p.d_scratch, scratch);
+    if (e != cudaSuccess) return e;
+    uint8_t* q = static_cast<uint8_t*>(p.d_scratch);
+    for (TcGemv& d : g) {
+      d.frag = reinterpret_cast<uint32_t*>(q);
+      q += (size_t)d.K * 32;
+      d.tab = reinterpret_cast<float*>(q);
+      q += (size_t)(d.K / 64) * kMmaTab * 4;
+    }
+  }
+  e = cudaMalloc(&p.d_gemvs, sizeof(TcGemv) * n);
+  if (e != cudaSuccess) {
+    if (p.d_scratch) cudaFree(p.d_scratch);
+    return e;
+  }
   e = cudaMalloc(&p.d_cta, sizeof(int) * cta.size());
   if (e != cudaSuccess) {
     cudaFree(p.d_gemvs);
+    if (p.d_scratch) cudaFree(p.d_scratch);
     return e;
   }
   e = cudaMemcpy(p.d_gemvs, g.data(), sizeof(TcGemv) * n, cudaMemcpyHostToDevice);
@@ -789,6 +1246,7 @@ cudaError_t tc_group_plan_build(const TcGroupItem* list, int n, int sms, TcGroup
   if (e != cudaSuccess) {
     cudaFree(p.d_gemvs);
     cudaFree(p.d_cta);
+    if (p.d_scratch) cudaFree(p.d_scratch);
     return e;
   }
   *out = p;
@@ -798,8 +1256,10 @@ cudaError_t tc_group_plan_build(const TcGroupItem* list, int n, int sms, TcGroup
 void tc_group_plan_free(TcGroupPlan* p) {
   if (p->d_gemvs) cudaFree(p->d_gemvs);
   if (p->d_cta) cudaFree(p->d_cta);
+  if (p->d_scratch) cudaFree(p->d_scratch);
   p->d_gemvs = nullptr;
   p->d_cta = nullptr;
+  p->d_scratch = nullptr;
 }
 
 cudaError_t tc_group_launch(const TcGroupPlan& p, uint32_t* err, cudaStream_t stream, bool pdl) {
@@ -816,6 +1276,19 @@ cudaError_t tc_group_launch(const TcGroupPlan& p, uint32_t* err, cudaStream_t st
   std::memset(unused, 0, sizeof(unused));
   TcPlan tp{};
   tp.smem = p.smem;
+  if (p.mma) {
+    // B fragments of every projection's X, then the grid over all row tiles
+    MmaPrepArgs pa{};
+    pa.gemvs = a.gemvs;
+    pa.ngemv = p.ngemv;
+    cudaError_t e = launch_kernel(w4a16_mma_prep_kernel, dim3((p.max_groups + 7) / 8, p.ngemv), dim3(256), 0,
+                                  stream, pdl, pa);
+    if (e != cudaSuccess) return e;
+    e = allow_max_smem(w4a16_mma_kernel);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(w4a16_mma_kernel, dim3(p.grid), dim3(kMmaThreads), p.smem, stream, pdl, unused[0],
+                         unused[1], unused[2], a);
+  }
   if (p.NT == 16) return launch_tc_nt<16>(unused, a, tp, p.grid, stream, pdl);
   return launch_tc_nt<32>(unused, a, tp, p.grid, stream, pdl);
 }
