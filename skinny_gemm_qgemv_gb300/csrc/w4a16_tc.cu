@@ -846,16 +846,24 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       for (int rb = 0; rb < 8; ++rb)
 #pragma unroll
         for (int t = 0; t < 2; ++t) y2[rb][t][0] = y2[rb][t][1] = 0ull;
+      // this warp's group in a stage: offsets and sums of x of its output
+      // columns and 2^sigma, loaded one stage ahead (the table is in L2)
+      float2 no0, no1, nx0, nx1;
+      float nup;
+      auto load_tab = [&](int s) {
+        const float* tg = w.tab + (size_t)((w.k0 + s * kStageK) / 64 + warp) * kMmaTab;
+        no0 = __ldg(reinterpret_cast<const float2*>(tg + 2 * c));
+        no1 = __ldg(reinterpret_cast<const float2*>(tg + 8 + 2 * c));
+        nx0 = __ldg(reinterpret_cast<const float2*>(tg + 16 + 2 * c));
+        nx1 = __ldg(reinterpret_cast<const float2*>(tg + 24 + 2 * c));
+        nup = __ldg(tg + 32);
+      };
+      load_tab(0);
       for (int s = 0; s < nstage; ++s, ++sgc) {
         const int st = sgc % a.ST;
-        // this warp's group: offsets and sums of x of its output columns, 2^sigma
-        const int gi = (w.k0 + s * kStageK) / 64 + warp;
-        const float* tg = w.tab + (size_t)gi * kMmaTab;
-        const float2 o0 = __ldg(reinterpret_cast<const float2*>(tg + 2 * c));
-        const float2 o1 = __ldg(reinterpret_cast<const float2*>(tg + 8 + 2 * c));
-        const float2 x0 = __ldg(reinterpret_cast<const float2*>(tg + 16 + 2 * c));
-        const float2 x1 = __ldg(reinterpret_cast<const float2*>(tg + 24 + 2 * c));
-        const float up = __ldg(tg + 32);
+        const float2 o0 = no0, o1 = no1, x0 = nx0, x1 = nx1;
+        const float up = nup;
+        if (s + 1 < nstage) load_tab(s + 1);
         if (ok) ok = mbar_wait(&full[st], (sgc / a.ST) & 1, a.err, kErrTcFullWait);
         const uint32_t sb = s_stages + st * kMmaStageBytes;
         if (ok) {
