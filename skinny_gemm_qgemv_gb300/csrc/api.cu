@@ -280,7 +280,7 @@ qg_status gemm_w8a8_i32(const int8_t* a, const int8_t* w, int32_t* c, int M, int
   if (M < 1 || M > 32 || N < 1 || K < 64 || K % 64 != 0) return QG_ERR_INVALID_ARG;
   if ((long long)K * 127 * 128 >= (1LL << 31)) return QG_ERR_INVALID_ARG;
   if (!aligned16(a) || !aligned16(w) || !aligned16(c)) return QG_ERR_MISALIGNED;
-  return from_cuda(qg::launch_w8a8_i32(a, w, c, M, N, K, static_cast<cudaStream_t>(stream), g_pdl));
+  return from_cuda(qg::launch_w8a8_i32(a, w, c, M, N, K, err_word(), static_cast<cudaStream_t>(stream), g_pdl));
 }
 
 qg_status qg_device_error(uint32_t* code, int clear) {

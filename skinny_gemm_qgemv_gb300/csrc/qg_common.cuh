@@ -290,8 +290,8 @@ __device__ __forceinline__ uint32_t pack2(uint32_t lo16, uint32_t hi16) { return
 // and adds its partner's copy of that half, so R values cost about
 // R - 1 + log2(32 / R) shuffles instead of 5 R. Afterwards lane L holds the
 // total of value transposed_row<R>(L).
-template <int R>
-__device__ __forceinline__ float transposed_warp_sum(float (&v)[R], int lane) {
+template <int R, typename T>
+__device__ __forceinline__ T transposed_warp_sum(T (&v)[R], int lane) {
   int cnt = R;
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) {
@@ -301,8 +301,8 @@ __device__ __forceinline__ float transposed_warp_sum(float (&v)[R], int lane) {
 #pragma unroll
       for (int i = 0; i < R / 2; ++i) {
         if (i < half) {
-          const float keep = upper ? v[i + half] : v[i];
-          const float send = upper ? v[i] : v[i + half];
+          const T keep = upper ? v[i + half] : v[i];
+          const T send = upper ? v[i] : v[i + half];
           v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
         }
       }

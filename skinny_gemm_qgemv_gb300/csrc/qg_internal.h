@@ -100,7 +100,7 @@ cudaError_t launch_hadamard32_quant_i8(const uint16_t* x, const uint32_t* sign_b
                                        int M, int K, cudaStream_t stream, bool pdl);
 
 // W8A8 (w8a8_i32.cu)
-cudaError_t launch_w8a8_i32(const int8_t* a, const int8_t* w, int32_t* c, int M, int N, int K,
+cudaError_t launch_w8a8_i32(const int8_t* a, const int8_t* w, int32_t* c, int M, int N, int K, uint32_t* err,
                             cudaStream_t stream, bool pdl);
 
 // Grouped M = 1 W4A16 GEMV (w4a16_group.cu): one persistent launch over a list

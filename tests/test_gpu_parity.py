@@ -168,7 +168,7 @@ def test_hadamard_zero_row_and_plain_normals(q):
 # ---------------------------------------------------------------- W8A8
 
 @pytest.mark.parametrize("M,N,K", [(16, 4096, 4096), (16, 12288, 4096), (1, 64, 64), (5, 100, 320),
-                                   (32, 256, 1024)])
+                                   (32, 256, 1024), (5, 2000, 1088), (32, 1300, 2048), (16, 1217, 64)])
 def test_w8a8_exact(q, M, N, K):
     x = synth.outlier_activations(M, K, seed=4, slot=0)
     sb = synth.sign_bits(K, seed=4, slot=5)
