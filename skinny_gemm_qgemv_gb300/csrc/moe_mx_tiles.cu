@@ -200,15 +200,27 @@ __global__ void __launch_bounds__(1024) moe_mx_route_kernel(const float* __restr
     for (int w = 0; w < WG; ++w) sum += red[grp * WG + w];
     __syncthreads();
     if (act) {
-      for (int e = g; e < E; e += G) {
-        const float v = lg[e];
+      // TPE adjacent threads per expert (a power of two, TPE * E <= G) each
+      // count the experts ahead of it in a strided share of the logits; their
+      // counts add up over the TPE lanes (the whole warp runs every round)
+      int tpe = 1;
+      while (tpe < 32 && tpe * 2 * E <= G) tpe *= 2;
+      const int per_round = G / tpe, rounds = (E + per_round - 1) / per_round;
+      const int part = g % tpe;
+      for (int r = 0; r < rounds; ++r) {
+        const int e = r * per_round + g / tpe;
+        const bool valid = e < E;
+        const float v = valid ? lg[e] : 0.f;
         int rank = 0;
-#pragma unroll 16
-        for (int f = 0; f < E; ++f) {
-          const float vf = lg[f];
-          rank += (vf > v) || (vf == v && f < e);
+        if (valid) {
+#pragma unroll 8
+          for (int f = part; f < E; f += tpe) {
+            const float vf = lg[f];
+            rank += (vf > v) || (vf == v && f < e);
+          }
         }
-        if (rank < top_k) {
+        for (int o = 1; o < tpe; o <<= 1) rank += __shfl_xor_sync(kFull, rank, o);
+        if (valid && part == 0 && rank < top_k) {
           idx[(size_t)t * top_k + rank] = e;
           wts[(size_t)t * top_k + rank] = expf(v - mx) / sum;
           sidx[t * top_k + rank] = e;
