@@ -238,7 +238,9 @@ static cudaError_t launch_w8a8_tile(const int8_t* a, const int8_t* w, int32_t* c
 
 cudaError_t launch_w8a8_i32(const int8_t* a, const int8_t* w, int32_t* c, int M, int N, int K, uint32_t* err,
                             cudaStream_t stream, bool pdl) {
-  // wide matrices: the tiled kernel (NC x MMAX = 64 sums per lane); else one warp per column
+  // M <= 16 with K a multiple of 512: the tensor cores through exact fp16 operands
+  if (err && w8a8_mma_ok(M, N, K)) return launch_w8a8_mma(a, w, c, M, N, K, err, stream, pdl);
+  // other wide matrices: the tiled kernel (NC x MMAX = 64 sums per lane); else one warp per column
   if (err && N >= 4 * kW8Warps * device_sm_count() / 4) {
     if (M <= 8) return launch_w8a8_tile<8, 8>(a, w, c, M, N, K, err, stream, pdl);
     if (M <= 16) return launch_w8a8_tile<16, 4>(a, w, c, M, N, K, err, stream, pdl);

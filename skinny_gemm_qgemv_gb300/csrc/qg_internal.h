@@ -102,6 +102,11 @@ cudaError_t launch_hadamard32_quant_i8(const uint16_t* x, const uint32_t* sign_b
 // W8A8 (w8a8_i32.cu)
 cudaError_t launch_w8a8_i32(const int8_t* a, const int8_t* w, int32_t* c, int M, int N, int K, uint32_t* err,
                             cudaStream_t stream, bool pdl);
+// W8A8 through exact fp16 operands on the tensor cores (w8a8_mma.cu): M <= 16,
+// K a multiple of 512, N >= 128; clears C itself (split K adds into it)
+bool w8a8_mma_ok(int M, int N, int K);
+cudaError_t launch_w8a8_mma(const int8_t* a, const int8_t* w, int32_t* c, int M, int N, int K, uint32_t* err,
+                            cudaStream_t stream, bool pdl);
 
 // Grouped M = 1 W4A16 GEMV (w4a16_group.cu): one persistent launch over a list
 // of independent projections. The caller fills wq, scales, biases, x, y, N, K;

@@ -1,0 +1,301 @@
+// W8A8 int32 GEMM on the tensor cores through exact fp16 operands, M <= 16.
+//
+// C[m][n] = sum_k a[m][k] w[n][k] with int8 a, w ("How Uzu optimizes bytes and
+// tokens per pass": 8-bit activations on the int8 matrix path, 16 verify rows).
+// The int8 mma.sync path of GB300 measured 252 MAC/clk/SM, so the products run
+// on the f16 path instead, exactly:
+//  * A weight byte b becomes the fp16 1024 + (b + 128) with one xor and one
+//    byte permute per two bytes (fp16 has an ulp of 1 in [1024, 2048)); an
+//    activation becomes its own value in fp16 (|a| <= 128, exact).
+//  * mma.sync.m16n8k16 (f16 in, fp32 accumulate) sums (1152 + b) a over a 64-k
+//    group starting from -1152 sum a, so it ends at sum b a; every partial
+//    sum is an integer below 2^24 in magnitude (1152 * 64 * 128 + 64 * 128^2),
+//    hence exact in fp32, and is moved into an int32 accumulator per group.
+//  * Layout as in the skinny W4A16 MMA kernel: one persistent CTA per SM, a
+//    producer warp loads per 512-k stage the codes of 128 weight rows and the
+//    stage's activations (128B-swizzled TMA tiles); warp w of 8 consumer warps
+//    owns 64-k group w of every stage and all 128 rows (eight 16-row blocks)
+//    and builds the group's B fragments from the landed activations once per
+//    stage. The warps' partial tiles are added through shared memory and the
+//    row tile's int32 results added into C with integer atomics (exact in any
+//    order), so K may be split over CTAs; C is cleared before the launch.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "qg_common.cuh"
+#include "qg_internal.h"
+
+namespace qg {
+
+namespace {
+
+constexpr int kW8Rows = 128;                          // weight rows (output columns) per tile
+constexpr int kW8StageK = 512;                        // k per stage
+constexpr int kW8Warps = 8;                           // consumer warps = 64-k groups per stage
+constexpr int kW8Threads = 32 * (kW8Warps + 1);       // + the producer warp
+constexpr uint32_t kW8Codes = kW8Rows * kW8StageK;    // 64 KB: [4 chunks][128 rows][128 B]
+constexpr uint32_t kW8Acts = 16 * kW8StageK;          // 8 KB: [4 chunks][16 rows][128 B]
+constexpr uint32_t kW8Stage = kW8Codes + kW8Acts;
+constexpr uint32_t kW8Red = kW8Warps * 16 * 32 * 16;  // 64 KB: int32 partial tiles of all warps
+
+struct W8MmaArgs {
+  int32_t* c;
+  int M, N, K;
+  int ntiles, splits, kper, nunits, ST;
+  uint32_t* err;
+};
+
+__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* tm, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// d = A B + C with C = (c0, c1) for both row halves (first k-step of a group)
+__device__ __forceinline__ void mma16816_from(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1, float c0, float c1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%10, %11, %10, %11};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void mma16816_acc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// four int8 weights (byte j = weight j) -> fp16 pairs (1152 + w0, 1152 + w1), (1152 + w2, 1152 + w3)
+__device__ __forceinline__ void w8_to_f16x2_offset(uint32_t word, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = word ^ 0x80808080u;  // signed byte b -> b + 128 in 0..255
+  lo = __byte_perm(u, 0x64646464u, 0x4140);  // bytes u0, 0x64, u1, 0x64: fp16 1024 + u
+  hi = __byte_perm(u, 0x64646464u, 0x4342);
+}
+
+// four int8 activations -> exact fp16 pairs (a0, a1), (a2, a3): the offset form
+// above minus 1152 (exact: integers below 2048 in magnitude)
+__device__ __forceinline__ void a8_to_f16x2(uint32_t word, uint32_t& lo, uint32_t& hi) {
+  uint32_t l, h;
+  w8_to_f16x2_offset(word, l, h);
+  constexpr uint32_t k1152 = 0x64806480u;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(l), "r"(k1152));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(h), "r"(k1152));
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kW8Threads, 1)
+    w8a8_mma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_a,
+                    const W8MmaArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const gbase = smem_raw + (base - raw);
+  // shared layout: stages | red (64 KB) | barriers
+  int32_t* red = reinterpret_cast<int32_t*>(gbase + a.ST * kW8Stage);
+  uint64_t* full = reinterpret_cast<uint64_t*>(gbase + a.ST * kW8Stage + kW8Red);
+  uint64_t* empty = full + a.ST;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < a.ST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kW8Warps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_wait();  // C is cleared and a written before this kernel
+  const int nstage = a.kper / kW8StageK;
+
+  if (warp == kW8Warps) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      int issued = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < a.nunits && ok; u += gridDim.x) {
+        const int n0 = (u / a.splits) * kW8Rows, k0 = (u % a.splits) * a.kper;
+        for (int s = 0; s < nstage; ++s) {
+          const int st = issued % a.ST;
+          if (issued >= a.ST) ok = mbar_wait(&empty[st], ((issued / a.ST) & 1) ^ 1, a.err, kErrGemvEmptyWait);
+          if (!ok) break;
+          const uint32_t sb = base + st * kW8Stage;
+          mbar_arrive_expect_tx(&full[st], kW8Stage);
+          const int kc = (k0 + s * kW8StageK) / 128;  // first 128-byte chunk of the stage
+          tma_3d(sb, &tm_w, 0, n0, kc, &full[st]);
+          tma_3d(sb + kW8Codes, &tm_a, 0, 0, kc, &full[st]);
+          ++issued;
+        }
+      }
+      for (int j = max(0, issued - a.ST); j < issued; ++j)
+        mbar_wait(&full[j % a.ST], (j / a.ST) & 1, a.err, kErrGemvDrain);
+    }
+  } else {
+    // ---------------------------------------------------------------- consumers
+    const int g = lane >> 2, c = lane & 3;
+    // the 16 bytes of group `warp` this lane reads in every 128-byte row: unit 4 (warp % 2) + c
+    const uint32_t unit = 4u * (uint32_t)(warp & 1) + (uint32_t)c;
+    const uint32_t chunk = (uint32_t)(warp >> 1);
+    int sgc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < a.nunits; u += gridDim.x) {
+      const int n0 = (u / a.splits) * kW8Rows;
+      int yi[8][2][4];
+#pragma unroll
+      for (int rb = 0; rb < 8; ++rb)
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) yi[rb][t][e] = 0;
+      for (int s = 0; s < nstage; ++s, ++sgc) {
+        const int st = sgc % a.ST;
+        if (ok) ok = mbar_wait(&full[st], (sgc / a.ST) & 1, a.err, kErrGemvFullWait);
+        const uint32_t sb = base + st * kW8Stage;
+        if (ok) {
+          // B fragments of this group: activation rows g (tile 0) and g + 8 (tile 1),
+          // k = 16c .. 16c + 15 of the group; step s4 uses k 16c + 4 s4 .. + 3
+          uint32_t b[16];
+          int asum[2];
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int n = g + 8 * t;
+            const uint4 v = lds128(sb + kW8Codes + chunk * 2048 + n * 128 + ((unit ^ (uint32_t)(n & 7)) << 4));
+            const uint32_t wds[4] = {v.x, v.y, v.z, v.w};
+            int sa = 0;
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4) {
+              a8_to_f16x2(wds[s4], b[(s4 * 2 + t) * 2], b[(s4 * 2 + t) * 2 + 1]);
+              sa = __dp4a((int)wds[s4], 0x01010101, sa);
+            }
+            sa += __shfl_xor_sync(0xFFFFFFFFu, sa, 1);
+            sa += __shfl_xor_sync(0xFFFFFFFFu, sa, 2);
+            asum[t] = sa;  // sum of a over the group for activation row n
+          }
+          // accumulator start per output column (activation row 8t + 2c, + 1): -1152 sum a
+          float c0[2], c1[2];
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            c0[t] = -1152.f * (float)__shfl_sync(0xFFFFFFFFu, asum[t], 8 * c);
+            c1[t] = -1152.f * (float)__shfl_sync(0xFFFFFFFFu, asum[t], 8 * c + 4);
+          }
+          const uint32_t cbase = sb + chunk * 16384;
+#pragma unroll
+          for (int rb = 0; rb < 8; ++rb) {
+            const int r0 = 16 * rb + g;  // rows r0 and r0 + 8 share the swizzle (r & 7 = g)
+            const uint32_t sw = (unit ^ (uint32_t)g) << 4;
+            const uint4 w0 = lds128(cbase + r0 * 128 + sw);
+            const uint4 w1 = lds128(cbase + (r0 + 8) * 128 + sw);
+            const uint32_t x0[4] = {w0.x, w0.y, w0.z, w0.w}, x1[4] = {w1.x, w1.y, w1.z, w1.w};
+            float acc[2][4];
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4) {
+              uint32_t a0l, a0h, a1l, a1h;
+              w8_to_f16x2_offset(x0[s4], a0l, a0h);
+              w8_to_f16x2_offset(x1[s4], a1l, a1h);
+#pragma unroll
+              for (int t = 0; t < 2; ++t) {
+                if (s4 == 0)
+                  mma16816_from(acc[t], a0l, a1l, a0h, a1h, b[t * 2], b[t * 2 + 1], c0[t], c1[t]);
+                else
+                  mma16816_acc(acc[t], a0l, a1l, a0h, a1h, b[(s4 * 2 + t) * 2], b[(s4 * 2 + t) * 2 + 1]);
+              }
+            }
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) yi[rb][t][e] += __float2int_rn(acc[t][e]);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+      }
+      // the 8 warps' partial tiles -> one tile (integers: any order is exact), added into C
+      {
+        int4* rv = reinterpret_cast<int4*>(red);
+#pragma unroll
+        for (int rb = 0; rb < 8; ++rb)
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+            rv[(warp * 16 + rb * 2 + t) * 32 + lane] = make_int4(yi[rb][t][0], yi[rb][t][1], yi[rb][t][2], yi[rb][t][3]);
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      {
+        const int et = threadIdx.x;  // 0..255: lane et % 32 of units 2 (et / 32), + 1
+        const int ln = et & 31, u0 = 2 * (et >> 5);
+        const int gg = ln >> 2, cc = ln & 3;
+        const int4* rv = reinterpret_cast<const int4*>(red);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          int tot[4] = {0, 0, 0, 0};
+#pragma unroll
+          for (int w2 = 0; w2 < kW8Warps; ++w2) {
+            const int4 v = rv[(w2 * 16 + u0 + h) * 32 + ln];
+            tot[0] += v.x;
+            tot[1] += v.y;
+            tot[2] += v.z;
+            tot[3] += v.w;
+          }
+          const int uu = u0 + h, rb = uu >> 1, t = uu & 1;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int n = n0 + 16 * rb + gg + 8 * (e >> 1);
+            const int m = 8 * t + 2 * cc + (e & 1);
+            if (m < a.M && n < a.N) atomicAdd(&a.c[(size_t)m * a.N + n], tot[e]);
+          }
+        }
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+    }
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+bool w8a8_mma_ok(int M, int N, int K) {
+  return M >= 1 && M <= 16 && N >= kW8Rows && K >= kW8StageK && K % kW8StageK == 0;
+}
+
+cudaError_t launch_w8a8_mma(const int8_t* a8, const int8_t* w8, int32_t* c, int M, int N, int K, uint32_t* err,
+                            cudaStream_t stream, bool pdl) {
+  const int sms = device_sm_count();
+  W8MmaArgs a{};
+  a.c = c;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.err = err;
+  a.ntiles = (N + kW8Rows - 1) / kW8Rows;
+  const int kstages = K / kW8StageK;
+  // split K while twice the units still fit the SMs (integer atomics add the splits)
+  a.splits = 1;
+  while (a.ntiles * a.splits * 2 <= sms && kstages % (a.splits * 2) == 0) a.splits *= 2;
+  a.kper = K / a.splits;
+  a.nunits = a.ntiles * a.splits;
+  a.ST = 2;
+  const size_t smem = 1024 + (size_t)a.ST * kW8Stage + kW8Red + 16 * (size_t)a.ST;
+  CUtensorMap tm_w, tm_a;
+  // weights {128 B, N rows, K / 128 chunks} in [4][128][128 B] boxes; activations
+  // {128 B, M rows, K / 128 chunks} in [4][16][128 B] boxes (rows past M read as zeros)
+  if (!tmap_3d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w8, 128, (uint64_t)N, (uint64_t)K / 128, (uint64_t)K, 128, 128,
+               kW8Rows, 4) ||
+      !tmap_3d(&tm_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, a8, 128, (uint64_t)M, (uint64_t)K / 128, (uint64_t)K, 128, 128,
+               16, 4))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaMemsetAsync(c, 0, sizeof(int32_t) * (size_t)M * N, stream);
+  if (e != cudaSuccess) return e;
+  e = allow_max_smem(w8a8_mma_kernel);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(w8a8_mma_kernel, dim3(std::min(a.nunits, sms)), dim3(kW8Threads), smem, stream, pdl, tm_w,
+                       tm_a, a);
+}
+
+}  // namespace qg

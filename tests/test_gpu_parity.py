@@ -168,7 +168,8 @@ def test_hadamard_zero_row_and_plain_normals(q):
 # ---------------------------------------------------------------- W8A8
 
 @pytest.mark.parametrize("M,N,K", [(16, 4096, 4096), (16, 12288, 4096), (1, 64, 64), (5, 100, 320),
-                                   (32, 256, 1024), (5, 2000, 1088), (32, 1300, 2048), (16, 1217, 64)])
+                                   (32, 256, 1024), (5, 2000, 1088), (32, 1300, 2048), (16, 1217, 64),
+                                   (7, 1000, 1024), (16, 130, 3072)])
 def test_w8a8_exact(q, M, N, K):
     x = synth.outlier_activations(M, K, seed=4, slot=0)
     sb = synth.sign_bits(K, seed=4, slot=5)
@@ -178,12 +179,15 @@ def test_w8a8_exact(q, M, N, K):
     assert np.array_equal(c.cpu().numpy(), oracle.w8a8(qa, w))
 
 
-def test_w8a8_extremes(q):
+@pytest.mark.parametrize("N", [64, 384])
+def test_w8a8_extremes(q, N):
     K = 4096
     a = torch.full((16, K), 127, dtype=torch.int8)
     a[1::2] = -127
-    w = torch.full((64, K), -127, dtype=torch.int8)
+    a[3::8, ::2] = -128
+    w = torch.full((N, K), -127, dtype=torch.int8)
     w[:, ::3] = 127
+    w[1::5, 1::7] = -128  # the full int8 range on the weight side
     c = q.gemm_w8a8_i32(a.to(DEV), w.to(DEV))
     assert np.array_equal(c.cpu().numpy(), oracle.w8a8(a, w))
 
