@@ -1,0 +1,870 @@
+// MXFP4 routed-expert MoE layer on the tensor cores (warp-level MMA): the main path.
+//
+// "Running Kimi K3 (2.8T) on one Apple Silicon Mac" (Deltafin), section "How it
+// works": the router picks 16 experts per token and only the selected experts'
+// weights are read; section "Technical approach / compute": the expert GEMV
+// decodes the E2M1 codes and applies the E8M0 block scale in the same pass as
+// the multiply. The layer is g = Wg[e] x, u = Wu[e] x, h = silu(g) u,
+// y = sum_j p_j (Wd[e_j] h_j).
+//
+// Three launches:
+//  * route (one CTA): per token one warp finds the exact top-k by a radix
+//    select on order-preserving 32-bit keys of the logits (ties to the lower
+//    expert index) while the other warps take the activations' max |x|; then
+//    x * 2^-sigma in fp16 (sigma per token, an exact power of two that puts
+//    max |x| in [2^14, 2^15)), the per-expert grouping and the "virtual
+//    experts": runs of at most kMxTC = 8 pairs (token, slot) of one expert,
+//    the N = 8 columns of one MMA.
+//  * gate/up: persistent; a tile is (virtual expert, 32 rows of I) with both
+//    matrices. A producer warp moves 512-k stages with TMA: the E2M1 codes of
+//    the 32 gate and 32 up rows (128B-swizzled), their E8M0 scales and the fp16
+//    x rows of the tile's pairs. Eight consumer warps own two 32-k blocks of
+//    every stage each; one mma.sync.m16n8k16 row block holds 8 gate rows (MMA
+//    rows 0..7) and the same 8 up rows (rows 8..15), so g and u of a row meet
+//    in one accumulator fragment. Per block: 2 MMAs from zero, then
+//    acc += result * 2^(scale - 127) per row (the block scale is a row factor
+//    of the MMA result). At the end of a tile the warps' partial sums are added
+//    in warp order through shared memory and h = silu(g) u is written in fp32
+//    with the pair's max |h|.
+//  * down: one CTA per range of R = 16 * MT rows of H, over every virtual
+//    expert; the MMA columns are the batch's tokens, so one accumulator per
+//    (row, token) collects all of a token's experts. B is p * h * 2^-sigma_t in
+//    fp16 (sigma_t per token from max_j p_j max|h_j|), converted from the
+//    staged fp32 h by the warp that owns the block. One cross-warp sum at the
+//    end, then y = acc * 2^sigma_t.
+// E2M1 codes go through the hardware cvt.rn.f16x2.e2m1x2 (exact); products are
+// f16 x f16 with fp32 accumulation. Lane (g, c) of an MMA takes the 4 code
+// bytes 4c..4c+3 of a block (codes 8c..8c+7): bytes 0, 1 are the k slots
+// (2c, 2c+1) and (2c+8, 2c+9) of the first MMA, bytes 2, 3 those of the
+// second; B is loaded in the same order (8 consecutive fp16 values), so the k
+// permutation is the same on both sides and the dot product is unchanged.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "qg_common.cuh"
+#include "qg_internal.h"
+
+namespace qg {
+
+namespace {
+
+constexpr unsigned kFull = 0xFFFFFFFFu;
+constexpr int kMxWarps = 16;                       // BPW 32-k blocks of every stage each
+constexpr int kMxThreads = 32 * kMxWarps;
+constexpr size_t kMxSmem = 227 * 1024;
+// gate/up stage (up to 1024 k): codes [4 chunks][32 rows][128 B] per matrix, scales [32][32] per matrix
+constexpr uint32_t kGuCodes = 4 * 32 * 128;
+constexpr uint32_t kGuScales = 32 * 32;
+constexpr uint32_t kGuStage = 2 * kGuCodes + 2 * kGuScales;
+constexpr uint32_t kGuRed = 2u * kMxWarps * 4 * 32 * 16;  // two buffers of the warps' partial tiles
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// d = A B (zero accumulator)
+__device__ __forceinline__ void mma_f16_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%10, %10, %10, %10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+// E8M0 byte -> 2^(e - 127) by an integer multiply (the exponent field); e = 0
+// (2^-127, below the normal range) gives 0
+__device__ __forceinline__ float e8m0_mul(uint32_t e) { return __uint_as_float(e * 8388608u); }
+
+__device__ __forceinline__ uint32_t f16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// 32-bit key with the order of the logits: larger logit, larger key; -0 = +0
+__device__ __forceinline__ uint32_t logit_key(float v) {
+  uint32_t b = __float_as_uint(v);
+  if (b == 0x80000000u) b = 0u;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_logit(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+__device__ __forceinline__ void bar_consumers() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kMxWarps) : "memory"); }
+
+// Stage release: every warp adds one to the slot's counter after its last read
+// of the slot (acquire-release, so the last adder sees all the other warps'
+// reads done); the last one re-arms the slot and issues the copies of the
+// stage ST ahead into it. No warp is set aside for the copies.
+__device__ __forceinline__ bool release_is_last(uint32_t* cnt, uint32_t warps) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;" : "=r"(old) : "r"(smem_u32(cnt)) : "memory");
+  if (old + 1u != warps) return false;
+  *cnt = 0u;  // nobody touches the counter again before the new copies land
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic reads before the async-proxy writes
+  return true;
+}
+// TMA 3D load with an L2 eviction-priority hint (streamed weights: evict first)
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void* tm, int x, int y, int z, uint64_t* bar,
+                                                 uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+      "%3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// route: top-k, softmax weights, fp16 activations, grouping (one CTA, 1024 threads)
+// ---------------------------------------------------------------------------
+constexpr int kRouteThreads = 1024;
+
+namespace {
+
+// exclusive prefix sum of one value per thread of the CTA; every thread calls it
+__device__ __forceinline__ int cta_exclusive_scan(int v, int* wsum, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = wsum[lane];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(kFull, wi, o);
+      if (lane >= o) wi += t;
+    }
+    wsum[lane] = wi - w;
+    if (lane == 31) wsum[32] = wi;
+  }
+  __syncthreads();
+  const int r = wsum[warp] + incl - v;
+  total = wsum[32];
+  __syncthreads();
+  return r;
+}
+
+// One token's router on one warp. Lane l holds the keys of experts l + 32 i.
+// The top_k-th largest key is found bit by bit from the top (a radix select
+// that stops as soon as the keys matching the prefix are exactly the ones
+// still needed); equal keys at the threshold are taken in expert order. The
+// selected experts are ranked among themselves (larger logit first, ties to
+// the lower index) and written with their softmax probabilities. PER: logits
+// per lane (E <= 32 PER).
+template <int PER>
+__device__ __forceinline__ void route_token(const float* __restrict__ lg, int E, int top_k, int lane,
+                                            uint32_t* sel_k, int* sel_e, int32_t* __restrict__ idx,
+                                            float* __restrict__ wts, int* pe) {
+  const int ne = (E + 31) >> 5;
+  uint32_t key[PER];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    key[i] = 0u;
+    const int e = 32 * i + lane;
+    if (i < ne && e < E) {
+      const float v = __ldg(lg + e);
+      key[i] = logit_key(v);
+      mx = fmaxf(mx, v);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+  float sm = 0.f;
+#pragma unroll
+  for (int i = 0; i < PER; ++i)
+    if (i < ne && 32 * i + lane < E) sm += expf(key_logit(key[i]) - mx);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(kFull, sm, o);
+
+  uint32_t prefix = 0u, mask = 0u;
+  int need = top_k, match = E;  // keys still needed among those matching the prefix; how many match
+  for (int b = 31; b >= 0 && match != need; --b) {
+    const uint32_t bit = 1u << b, m2 = mask | bit, want = prefix | bit;
+    int cnt = 0;
+#pragma unroll
+    for (int i = 0; i < PER; ++i)
+      if (i < ne && 32 * i + lane < E) cnt += (key[i] & m2) == want;
+    cnt = (int)__reduce_add_sync(kFull, (unsigned)cnt);
+    if (cnt >= need) {
+      prefix = want;
+      match = cnt;
+    } else {
+      need -= cnt;
+      match -= cnt;
+    }
+    mask = m2;
+  }
+  // every key above the prefix range, and `need` of the keys in it in expert order
+  const unsigned below = (1u << lane) - 1u;
+  int base = 0, eq_seen = 0;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    if (i < ne) {
+      const bool valid = 32 * i + lane < E;
+      const uint32_t km = key[i] & mask;
+      const bool eq = valid && km == prefix;
+      const unsigned eqb = __ballot_sync(kFull, eq);
+      const bool take = (valid && km > prefix) || (eq && eq_seen + __popc(eqb & below) < need);
+      eq_seen += __popc(eqb);
+      const unsigned tb = __ballot_sync(kFull, take);
+      const int pos = base + __popc(tb & below);
+      if (take && pos < 32) {
+        sel_k[pos] = key[i];
+        sel_e[pos] = 32 * i + lane;
+      }
+      base += __popc(tb);
+    }
+  }
+  __syncwarp();
+  if (lane < top_k) {
+    const uint32_t kj = sel_k[lane];
+    const int ej = sel_e[lane];
+    int rank = 0;
+    for (int l = 0; l < top_k; ++l) {
+      const uint32_t kl = sel_k[l];
+      rank += (kl > kj) || (kl == kj && sel_e[l] < ej);
+    }
+    idx[rank] = ej;
+    wts[rank] = expf(key_logit(kj) - mx) / sm;
+    pe[rank] = ej;
+  }
+  __syncwarp();
+}
+
+}  // namespace
+
+template <int PER>
+__global__ void __launch_bounds__(kRouteThreads) moe_mx_route_mma_kernel(
+    const float* __restrict__ logits, const uint16_t* __restrict__ x, int T, int H, int E, int top_k,
+    int32_t* __restrict__ idx, float* __restrict__ wts, int32_t* __restrict__ xexp, uint16_t* __restrict__ xh,
+    int32_t* __restrict__ vexp, int32_t* __restrict__ nvirt, uint32_t* __restrict__ hmax) {
+  __shared__ uint32_t sel_k[32][32];
+  __shared__ int sel_e[32][32];
+  __shared__ int pe[kRouteThreads];      // expert of pair p = t * top_k + slot
+  __shared__ int cnt[kRouteThreads];     // pairs per expert, then the experts' offsets
+  __shared__ int sorder[kRouteThreads];  // pairs sorted by expert (stable)
+  __shared__ uint32_t amax[kRouteThreads];
+  __shared__ int wsum[33];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int P = T * top_k;
+  const int cpt = H >> 3;  // 16-byte chunks of x per token (a multiple of 32)
+  amax[tid] = 0u;
+  cnt[tid] = 0;
+  __syncthreads();
+  pdl_wait();  // the logits and x may come from the previous kernel
+  for (int t = warp; t < T; t += 32)
+    route_token<PER>(logits + (size_t)t * E, E, top_k, lane, sel_k[warp], sel_e[warp], idx + (size_t)t * top_k,
+                wts + (size_t)t * top_k, pe + t * top_k);
+  // max |x| per token; the 32 chunks of a warp belong to one token
+  const uint4* x4 = reinterpret_cast<const uint4*>(x);
+  for (int q0 = warp * 32; q0 < T * cpt; q0 += kRouteThreads) {
+    const uint4 w = __ldg(x4 + q0 + lane);
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+    float m = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      m = fmaxf(m, fmaxf(fabsf(bf16_bits_to_f32(ww[j] & 0xFFFFu)), fabsf(bf16_bits_to_f32(ww[j] >> 16))));
+    const unsigned mb = __reduce_max_sync(kFull, __float_as_uint(m));  // non-negative: uint order
+    if (lane == 0) atomicMax(&amax[q0 / cpt], mb);
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+  // x * 2^-sigma in fp16 (exact scaling; sigma puts max |x| in [2^14, 2^15))
+  if (tid < T) xexp[tid] = fp16_prescale_exp(__uint_as_float(amax[tid]));
+  for (int q = tid; q < T * cpt; q += kRouteThreads) {
+    const float sc = pow2f(-fp16_prescale_exp(__uint_as_float(amax[q / cpt])));
+    const uint4 w = __ldg(x4 + q);
+    uint4 o;
+    o.x = f16x2_rn(bf16_bits_to_f32(w.x & 0xFFFFu) * sc, bf16_bits_to_f32(w.x >> 16) * sc);
+    o.y = f16x2_rn(bf16_bits_to_f32(w.y & 0xFFFFu) * sc, bf16_bits_to_f32(w.y >> 16) * sc);
+    o.z = f16x2_rn(bf16_bits_to_f32(w.z & 0xFFFFu) * sc, bf16_bits_to_f32(w.z >> 16) * sc);
+    o.w = f16x2_rn(bf16_bits_to_f32(w.w & 0xFFFFu) * sc, bf16_bits_to_f32(w.w >> 16) * sc);
+    reinterpret_cast<uint4*>(xh)[q] = o;
+  }
+  // grouping: pairs per expert, stable order by expert, virtual experts of <= kMxTC pairs
+  for (int p = tid; p < P; p += kRouteThreads) {
+    atomicAdd(&cnt[pe[p]], 1);
+    hmax[p] = 0u;
+  }
+  __syncthreads();
+  const int n_e = tid < E ? cnt[tid] : 0;
+  int total_pairs, total_v;
+  const int off = cta_exclusive_scan(n_e, wsum, total_pairs);
+  const int nv_e = (n_e + kMxTC - 1) / kMxTC;
+  const int voff = cta_exclusive_scan(nv_e, wsum, total_v);
+  if (tid < E) cnt[tid] = off;
+  __syncthreads();
+  for (int p = tid; p < P; p += kRouteThreads) {
+    const int e = pe[p];
+    int r = 0;
+    for (int q = 0; q < p; ++q) r += pe[q] == e;
+    sorder[cnt[e] + r] = p;
+  }
+  __syncthreads();
+  if (tid < E) {
+    for (int c = 0; c < nv_e; ++c) {
+      int32_t* ent = vexp + (size_t)(voff + c) * kMxVexpInts;
+      const int n = min(kMxTC, n_e - c * kMxTC);
+      ent[0] = tid;
+      ent[1] = n;
+#pragma unroll
+      for (int j = 0; j < kMxTC; ++j) ent[2 + j] = j < n ? sorder[off + c * kMxTC + j] : -1;
+    }
+  }
+  if (tid == 0) nvirt[0] = total_v;
+  (void)total_pairs;
+}
+
+
+// ---------------------------------------------------------------------------
+// gate/up + SwiGLU
+// ---------------------------------------------------------------------------
+struct MxGuArgs {
+  const uint16_t* xh;    // [T][H] fp16 x * 2^-sigma_t
+  const int32_t* xexp;   // [T] sigma_t
+  const int32_t* vexp;   // [nv][kMxVexpInts]: expert, pair count, kMxTC pairs (-1 padded)
+  const int32_t* nvirt;
+  float* h;              // [P][I]
+  uint32_t* hmax;        // [P] bits of max |h|
+  int H, I, top_k, ST, BPW;  // BPW: 32-k blocks per warp and stage (stage = 512 BPW k)
+  uint32_t* err;
+};
+
+// x row of pair g of the tile's virtual expert (null: no such pair)
+__device__ __forceinline__ const uint16_t* gu_xrow(const MxGuArgs& a, int tile, int tpv, int g) {
+  const int32_t* ent = a.vexp + (size_t)(tile / tpv) * kMxVexpInts;
+  return g < __ldg(ent + 1) ? a.xh + (size_t)(__ldg(ent + 2 + g) / a.top_k) * a.H : nullptr;
+}
+
+// BPW: 32-k blocks per warp and stage (a stage is 512 BPW k of the tile's rows)
+template <int BPW>
+__global__ void __launch_bounds__(kMxThreads, 1)
+    moe_mx_gu_mma_kernel(const __grid_constant__ CUtensorMap tm_gq, const __grid_constant__ CUtensorMap tm_uq,
+                         const __grid_constant__ CUtensorMap tm_gs, const __grid_constant__ CUtensorMap tm_us,
+                         const MxGuArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const gbase = smem_raw + (base - raw);
+  // shared layout: stages | red (two buffers) | full barriers | release counters
+  float4* red = reinterpret_cast<float4*>(gbase + (size_t)a.ST * kGuStage);
+  uint64_t* full = reinterpret_cast<uint64_t*>(gbase + (size_t)a.ST * kGuStage + kGuRed);
+  uint32_t* rel = reinterpret_cast<uint32_t*>(full + a.ST);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < a.ST; ++i) {
+      mbar_init(&full[i], 1);
+      rel[i] = 0u;
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_wait();  // the routing table and x come from the route kernel
+  pdl_launch_dependents();
+  const int H = a.H, I = a.I;
+  constexpr int KS = 512 * BPW;
+  constexpr uint32_t kSRow = 16u * BPW;    // scale bytes of one row in a stage
+  const int nks = H / KS;                   // stages per tile
+  const int tpv = I / 32;                   // tiles per virtual expert
+  const int total = *a.nvirt * tpv;
+  const int per = (total + (int)gridDim.x - 1) / (int)gridDim.x;
+  const int t0 = min(total, (int)blockIdx.x * per), t1 = min(total, t0 + per);
+  const int nstages = (t1 - t0) * nks;
+  const uint64_t pol = policy_evict_first();
+  // stage q of this CTA into its slot: codes and scales of 32 gate and 32 up rows, 512 BPW k
+  auto issue = [&](int q) {
+    const int tile = t0 + q / nks, ks = q - (q / nks) * nks;
+    const int v = tile / tpv, r0 = (tile - v * tpv) * 32;
+    const int row = __ldg(a.vexp + (size_t)v * kMxVexpInts) * I + r0;
+    const int st = q % a.ST;
+    const uint32_t sb = base + st * kGuStage;
+    mbar_arrive_expect_tx(&full[st], (2 * 4096u + 512u) * 2u * BPW);
+    tma_load_3d_hint(sb, &tm_gq, 0, row, 2 * BPW * ks, &full[st], pol);
+    tma_load_3d_hint(sb + kGuCodes, &tm_uq, 0, row, 2 * BPW * ks, &full[st], pol);
+    tma_load_2d(sb + 2 * kGuCodes, &tm_gs, 16 * BPW * ks, row, &full[st]);
+    tma_load_2d(sb + 2 * kGuCodes + kGuScales, &tm_us, 16 * BPW * ks, row, &full[st]);
+  };
+  if (threadIdx.x == 0)
+    for (int q = 0; q < min(a.ST, nstages); ++q) issue(q);
+
+  // lane (g, c): MMA rows g (gate) and g + 8 (up) of each 8-row block, pair g,
+  // codes / x at k = 8c .. 8c + 7 of blocks BPW w + j of every stage
+  const int g = lane >> 2, c = lane & 3;
+  const int et = threadIdx.x;
+  // byte offsets in a stage of this lane's code word of row g, block BPW w + j (128B swizzle:
+  // 16-byte unit u of row r at u ^ (r & 7)), and of its E8M0 scale; + 1024 mt / + 8 kSRow mt for
+  // the rows of 8-row block mt
+  uint32_t coff[BPW], soff[BPW];
+#pragma unroll
+  for (int j = 0; j < BPW; ++j) {
+    const uint32_t blk = BPW * warp + j;
+    coff[j] = (blk >> 3) * 4096u + g * 128u + (((blk & 7u) ^ (uint32_t)g) << 4) + 4u * c;
+    soff[j] = 2 * kGuCodes + g * kSRow + blk;
+  }
+  int st = 0, q = 0, buf = 0;
+  uint32_t par = 0;
+  bool ok = true;
+  // x of the next stage, loaded one stage ahead (L2-resident)
+  uint4 xn[BPW];
+  const uint16_t* xrow = t0 < t1 ? gu_xrow(a, t0, tpv, g) : nullptr;
+  auto load_x = [&](const uint16_t* row, int ks) {
+#pragma unroll
+    for (int j = 0; j < BPW; ++j)
+      xn[j] = row ? __ldg(reinterpret_cast<const uint4*>(row + ks * KS + 32 * (BPW * warp + j) + 8 * c))
+                  : make_uint4(0u, 0u, 0u, 0u);
+  };
+  load_x(xrow, 0);
+  for (int tile = t0; tile < t1; ++tile) {
+    const int v = tile / tpv, r0 = (tile - v * tpv) * 32;
+    const int32_t* ent = a.vexp + (size_t)v * kMxVexpInts;
+    const int np = __ldg(ent + 1);
+    const uint16_t* xnext = tile + 1 < t1 ? gu_xrow(a, tile + 1, tpv, g) : nullptr;
+    float acc[4][4];
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[mt][i] = 0.f;
+    for (int ks = 0; ks < nks; ++ks, ++q) {
+      uint4 xb[BPW];
+#pragma unroll
+      for (int j = 0; j < BPW; ++j) xb[j] = xn[j];
+      if (ks + 1 < nks)
+        load_x(xrow, ks + 1);
+      else if (tile + 1 < t1)
+        load_x(xnext, 0);
+      if (ok) ok = mbar_wait(&full[st], par, a.err, kErrMoeWait);
+      if (ok) {
+        const uint8_t* sp = gbase + (size_t)st * kGuStage;
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+          for (int j = 0; j < BPW; ++j) {
+            const uint32_t wg = *reinterpret_cast<const uint32_t*>(sp + coff[j] + 1024u * mt);
+            const uint32_t wu = *reinterpret_cast<const uint32_t*>(sp + kGuCodes + coff[j] + 1024u * mt);
+            const float fg = e8m0_mul(sp[soff[j] + 8u * kSRow * mt]);
+            const float fu = e8m0_mul(sp[kGuScales + soff[j] + 8u * kSRow * mt]);
+            float t[4];
+            mma_f16_z(t, e2m1x2_to_f16x2<0>(wg), e2m1x2_to_f16x2<0>(wu), e2m1x2_to_f16x2<1>(wg),
+                      e2m1x2_to_f16x2<1>(wu), xb[j].x, xb[j].y);
+            mma_f16(t, e2m1x2_to_f16x2<2>(wg), e2m1x2_to_f16x2<2>(wu), e2m1x2_to_f16x2<3>(wg),
+                    e2m1x2_to_f16x2<3>(wu), xb[j].z, xb[j].w);
+            acc[mt][0] = fmaf(t[0], fg, acc[mt][0]);
+            acc[mt][1] = fmaf(t[1], fg, acc[mt][1]);
+            acc[mt][2] = fmaf(t[2], fu, acc[mt][2]);
+            acc[mt][3] = fmaf(t[3], fu, acc[mt][3]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0 && release_is_last(&rel[st], kMxWarps) && q + a.ST < nstages) issue(q + a.ST);
+      if (++st == a.ST) {
+        st = 0;
+        par ^= 1u;
+      }
+    }
+    xrow = xnext;
+    // the warps' partial tiles, summed in warp order; h = silu(g) u. Two
+    // buffers: a warp writes buffer b of the next tile only after every warp
+    // passed this tile's barrier, i.e. finished reading buffer b of the last one
+    float4* rb = red + buf * (kMxWarps * 4 * 32);
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt)
+      rb[(warp * 4 + mt) * 32 + lane] = make_float4(acc[mt][0], acc[mt][1], acc[mt][2], acc[mt][3]);
+    bar_consumers();
+    if (et < 256) {
+      const int mt = et >> 6, hs = (et >> 5) & 1, l = et & 31;
+      const int col = 2 * (l & 3) + hs;  // the pair
+      if (col < np) {
+        float gs = 0.f, us = 0.f;
+#pragma unroll
+        for (int w2 = 0; w2 < kMxWarps; ++w2) {
+          const float4 r4 = rb[(w2 * 4 + mt) * 32 + l];
+          gs += hs ? r4.y : r4.x;
+          us += hs ? r4.w : r4.z;
+        }
+        const int pair = __ldg(ent + 2 + col);
+        const float sc = pow2f(__ldg(a.xexp + pair / a.top_k));
+        const float gv = gs * sc, uv = us * sc;
+        const float hv = gv / (1.f + expf(-gv)) * uv;
+        const int row = r0 + 8 * mt + (l >> 2);
+        a.h[(size_t)pair * I + row] = hv;
+        atomicMax(&a.hmax[pair], __float_as_uint(fabsf(hv)));
+      }
+    }
+    buf ^= 1;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// down + routing-weighted combine
+// ---------------------------------------------------------------------------
+struct MxDnArgs {
+  const float* h;         // [P][I] fp32
+  const uint32_t* hmax;   // [P]
+  const float* wts;       // [P] routing weights
+  const int32_t* vexp;
+  const int32_t* nvirt;
+  float* y;               // [T][H]
+  int T, H, I, top_k, R, ST, BPW;
+  uint32_t stage_bytes, o_s;  // stage size; offset of the scales in a stage
+  uint32_t* err;
+};
+
+// a lane's tokens 8 nt + g in one virtual expert: the h row of the token's
+// pair (null if the token is not in it) and p * 2^-sigma_t
+template <int NT>
+struct DnLane {
+  const float* hp[NT];
+  float f[NT];
+};
+
+template <int NT>
+__device__ __forceinline__ void dn_lane(const MxDnArgs& a, int v, int g, const int* sig, DnLane<NT>& L) {
+  const int32_t* ent = a.vexp + (size_t)v * kMxVexpInts;
+  const int np = __ldg(ent + 1);
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    L.hp[nt] = nullptr;
+    L.f[nt] = 0.f;
+  }
+  for (int q = 0; q < np; ++q) {
+    const int pair = __ldg(ent + 2 + q);
+    const int t = pair / a.top_k;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+      if (t == 8 * nt + g) {
+        L.hp[nt] = a.h + (size_t)pair * a.I;
+        L.f[nt] = __ldg(a.wts + pair) * pow2f(-sig[t]);
+      }
+  }
+}
+
+// NT: n tiles of 8 tokens (T <= 8 NT); MT: 16-row blocks per CTA (R = 16 MT);
+// BPW: 32-k blocks per warp and stage (a stage is 512 BPW k)
+template <int NT, int MT, int BPW>
+__global__ void __launch_bounds__(kMxThreads, 1)
+    moe_mx_dn_mma_kernel(const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_ds,
+                         const MxDnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const gbase = smem_raw + (base - raw);
+  constexpr int R = 16 * MT;
+  constexpr int KS = 512 * BPW;
+  constexpr uint32_t kOS = 256u * R * BPW;                          // scales after the codes
+  constexpr uint32_t kStage = (272u * R * BPW + 1023u) & ~1023u;
+  constexpr uint32_t kSRow = 16u * BPW;
+  // shared layout: stages (the cross-warp sums reuse them at the end) | sigma per token |
+  //                full barriers | release counters
+  int* sig = reinterpret_cast<int*>(gbase + (size_t)a.ST * kStage);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sig + 8 * NT);
+  uint32_t* rel = reinterpret_cast<uint32_t*>(full + a.ST);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < a.ST; ++i) {
+      mbar_init(&full[i], 1);
+      rel[i] = 0u;
+    }
+    fence_mbar_init();
+  }
+  pdl_wait();  // h and its maxima come from gate/up, the table from the route kernel
+  // sigma_t: max over the token's pairs of p |h| lands in [2^14, 2^15) after scaling
+  if (threadIdx.x < 8 * NT) {
+    const int t = threadIdx.x;
+    float m = 0.f;
+    if (t < a.T)
+      for (int j = 0; j < a.top_k; ++j) {
+        const int p = t * a.top_k + j;
+        m = fmaxf(m, a.wts[p] * __uint_as_float(a.hmax[p]));
+      }
+    sig[t] = fp16_prescale_exp(m);
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+  const int H = a.H, I = a.I;
+  const int nks = I / KS;
+  const int nv = *a.nvirt;
+  const int n0 = blockIdx.x * R;
+  // CTAs walk the virtual experts from different starting points (no L2 hot spot on one h row)
+  const int vstart = nv > 0 ? (int)(((long long)blockIdx.x * nv) / gridDim.x) : 0;
+  const int nstages = nv * nks;
+  const uint64_t pol = policy_evict_first();
+  // stage q of this CTA into its slot: codes and scales of its R rows of one virtual expert, KS k
+  auto issue = [&](int q) {
+    const int i = q / nks, ks = q - i * nks;
+    int v = vstart + i;
+    if (v >= nv) v -= nv;
+    const int row = __ldg(a.vexp + (size_t)v * kMxVexpInts) * H + n0;
+    const int st = q % a.ST;
+    const uint32_t sb = base + st * kStage;
+    mbar_arrive_expect_tx(&full[st], 272u * R * BPW);
+    tma_load_3d_hint(sb, &tm_dq, 0, row, 2 * BPW * ks, &full[st], pol);
+    tma_load_2d(sb + kOS, &tm_ds, 16 * BPW * ks, row, &full[st]);
+  };
+  if (threadIdx.x == 0)
+    for (int q = 0; q < min(a.ST, nstages); ++q) issue(q);
+
+  // lane (g, c): rows g, g + 8 of each 16-row block, tokens 8 nt + g, k = 8c .. 8c + 7
+  // of blocks BPW w + j of every stage
+  const int g = lane >> 2, c = lane & 3;
+  const int et = threadIdx.x;
+  uint32_t coff[BPW], soff[BPW];
+#pragma unroll
+  for (int j = 0; j < BPW; ++j) {
+    const uint32_t blk = BPW * warp + j;
+    coff[j] = (blk >> 3) * (128u * R) + g * 128u + (((blk & 7u) ^ (uint32_t)g) << 4) + 4u * c;
+    soff[j] = kOS + g * kSRow + blk;
+  }
+  float acc[MT][NT][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[mt][nt][i] = 0.f;
+  // fp32 h of the next stage, loaded one stage ahead (L2-resident): [nt][block][half]
+  uint4 hn[NT][BPW][2];
+  auto load_h = [&](const DnLane<NT>& L, int ks) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int j = 0; j < BPW; ++j)
+        if (L.hp[nt]) {
+          const uint4* p = reinterpret_cast<const uint4*>(L.hp[nt] + ks * KS + 32 * (BPW * warp + j) + 8 * c);
+          hn[nt][j][0] = __ldcg(p);
+          hn[nt][j][1] = __ldcg(p + 1);
+        }
+  };
+  DnLane<NT> cur, nxt;
+  int st = 0, v = vstart, ks = 0, i = 0;
+  uint32_t par = 0;
+  bool ok = true;
+  if (nv > 0) {
+    dn_lane<NT>(a, v, g, sig, cur);
+    load_h(cur, 0);
+  }
+  for (int q = 0; q < nstages; ++q) {
+    // this stage's B: p h 2^-sigma_t in fp16
+    uint32_t b[NT][BPW][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int j = 0; j < BPW; ++j) {
+        if (cur.hp[nt]) {
+          const float f = cur.f[nt];
+          const uint4 lo = hn[nt][j][0], hi = hn[nt][j][1];
+          b[nt][j][0] = f16x2_rn(__uint_as_float(lo.x) * f, __uint_as_float(lo.y) * f);
+          b[nt][j][1] = f16x2_rn(__uint_as_float(lo.z) * f, __uint_as_float(lo.w) * f);
+          b[nt][j][2] = f16x2_rn(__uint_as_float(hi.x) * f, __uint_as_float(hi.y) * f);
+          b[nt][j][3] = f16x2_rn(__uint_as_float(hi.z) * f, __uint_as_float(hi.w) * f);
+        } else {
+          b[nt][j][0] = b[nt][j][1] = b[nt][j][2] = b[nt][j][3] = 0u;
+        }
+      }
+    // the next stage's h
+    bool newv = false;
+    if (ks + 1 < nks) {
+      load_h(cur, ks + 1);
+    } else if (i + 1 < nv) {
+      dn_lane<NT>(a, v + 1 == nv ? 0 : v + 1, g, sig, nxt);
+      load_h(nxt, 0);
+      newv = true;
+    }
+    if (ok) ok = mbar_wait(&full[st], par, a.err, kErrMoeWait);
+    if (ok) {
+      const uint8_t* sp = gbase + (size_t)st * kStage;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+        for (int j = 0; j < BPW; ++j) {
+          // rows 16 mt + g and 16 mt + g + 8 (both with row & 7 = g)
+          const uint32_t w0 = *reinterpret_cast<const uint32_t*>(sp + coff[j] + 2048u * mt);
+          const uint32_t w1 = *reinterpret_cast<const uint32_t*>(sp + coff[j] + 2048u * mt + 1024u);
+          const float f0 = e8m0_mul(sp[soff[j] + 16u * kSRow * mt]);
+          const float f1 = e8m0_mul(sp[soff[j] + 16u * kSRow * mt + 8u * kSRow]);
+          const uint32_t a0 = e2m1x2_to_f16x2<0>(w0), a1 = e2m1x2_to_f16x2<0>(w1);
+          const uint32_t a2 = e2m1x2_to_f16x2<1>(w0), a3 = e2m1x2_to_f16x2<1>(w1);
+          const uint32_t a4 = e2m1x2_to_f16x2<2>(w0), a5 = e2m1x2_to_f16x2<2>(w1);
+          const uint32_t a6 = e2m1x2_to_f16x2<3>(w0), a7 = e2m1x2_to_f16x2<3>(w1);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            float t[4];
+            mma_f16_z(t, a0, a1, a2, a3, b[nt][j][0], b[nt][j][1]);
+            mma_f16(t, a4, a5, a6, a7, b[nt][j][2], b[nt][j][3]);
+            acc[mt][nt][0] = fmaf(t[0], f0, acc[mt][nt][0]);
+            acc[mt][nt][1] = fmaf(t[1], f0, acc[mt][nt][1]);
+            acc[mt][nt][2] = fmaf(t[2], f1, acc[mt][nt][2]);
+            acc[mt][nt][3] = fmaf(t[3], f1, acc[mt][nt][3]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && release_is_last(&rel[st], kMxWarps) && q + a.ST < nstages) issue(q + a.ST);
+    if (++st == a.ST) {
+      st = 0;
+      par ^= 1u;
+    }
+    if (++ks == nks) {
+      ks = 0;
+      ++i;
+      v = v + 1 == nv ? 0 : v + 1;
+    }
+    if (newv) cur = nxt;
+  }
+  // every stage is consumed (and every copy landed): the ring holds the warps' partial tiles
+  bar_consumers();
+  float4* red = reinterpret_cast<float4*>(gbase);
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+      red[((warp * MT + mt) * NT + nt) * 32 + lane] =
+          make_float4(acc[mt][nt][0], acc[mt][nt][1], acc[mt][nt][2], acc[mt][nt][3]);
+  bar_consumers();
+  const float* redf = reinterpret_cast<const float*>(gbase);
+  for (int q = et; q < R * a.T; q += 32 * kMxWarps) {
+    const int row = q / a.T, t = q - row * a.T;
+    if (n0 + row >= H) continue;
+    const int mt = row >> 4, rr = row & 15, nt = t >> 3, tc = t & 7;
+    const int l = (rr & 7) * 4 + (tc >> 1), comp = (rr >> 3) * 2 + (tc & 1);
+    float sum = 0.f;
+#pragma unroll 4
+    for (int w2 = 0; w2 < kMxWarps; ++w2) sum += redf[(((w2 * MT + mt) * NT + nt) * 32 + l) * 4 + comp];
+    a.y[(size_t)t * H + n0 + row] = sum * pow2f(sig[t]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+namespace {
+
+struct MxDnPlan {
+  int R, MT, NT, ST, BPW, grid;
+  uint32_t stage_bytes, o_s;
+  size_t smem;
+};
+
+MxDnPlan plan_down(int T, int H, int I, int sms) {
+  MxDnPlan p{};
+  // rows per CTA: a multiple of 16 that gives about one range per SM
+  p.MT = std::min(4, std::max(1, (H + 16 * sms - 1) / (16 * sms)));
+  p.R = 16 * p.MT;
+  p.grid = (H + p.R - 1) / p.R;
+  p.NT = T <= 8 ? 1 : 2;
+  p.BPW = I % 1024 == 0 ? 2 : 1;
+  p.o_s = 256u * p.R * p.BPW;  // codes: [2 BPW chunks][R rows][128 B], then scales [R][16 BPW]
+  p.stage_bytes = (272u * p.R * p.BPW + 1023u) & ~1023u;
+  const size_t fixed = 1024 + 4 * 8 * p.NT + 64;
+  p.ST = (int)std::min<size_t>(8, (kMxSmem - fixed) / (p.stage_bytes + 16));
+  p.smem = fixed + (size_t)p.ST * (p.stage_bytes + 16);
+  return p;
+}
+
+int plan_gateup_stages() { return (int)std::min<size_t>(8, (kMxSmem - 1024 - kGuRed - 64) / (kGuStage + 16)); }
+
+size_t gateup_smem(int ST) { return 1024 + (size_t)ST * (kGuStage + 16) + kGuRed + 64; }
+
+template <int NT, int MT, int BPW>
+cudaError_t launch_down(const CUtensorMap& tm_dq, const CUtensorMap& tm_ds, const MxDnArgs& da, const MxDnPlan& pd,
+                        cudaStream_t stream, bool pdl) {
+  cudaError_t e = allow_max_smem(moe_mx_dn_mma_kernel<NT, MT, BPW>);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(moe_mx_dn_mma_kernel<NT, MT, BPW>, dim3(pd.grid), dim3(kMxThreads), pd.smem, stream, pdl,
+                       tm_dq, tm_ds, da);
+}
+
+template <int NT, int BPW>
+cudaError_t launch_down_mt(const CUtensorMap& tm_dq, const CUtensorMap& tm_ds, const MxDnArgs& da,
+                           const MxDnPlan& pd, cudaStream_t stream, bool pdl) {
+  switch (pd.MT) {
+    case 1: return launch_down<NT, 1, BPW>(tm_dq, tm_ds, da, pd, stream, pdl);
+    case 2: return launch_down<NT, 2, BPW>(tm_dq, tm_ds, da, pd, stream, pdl);
+    case 3: return launch_down<NT, 3, BPW>(tm_dq, tm_ds, da, pd, stream, pdl);
+    default: return launch_down<NT, 4, BPW>(tm_dq, tm_ds, da, pd, stream, pdl);
+  }
+}
+
+template <int BPW>
+cudaError_t launch_gateup(const CUtensorMap* tm, const MxGuArgs& ga, int grid, size_t smem, cudaStream_t stream,
+                          bool pdl) {
+  cudaError_t e = allow_max_smem(moe_mx_gu_mma_kernel<BPW>);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(moe_mx_gu_mma_kernel<BPW>, dim3(grid), dim3(kMxThreads), smem, stream, pdl, tm[0], tm[1],
+                       tm[2], tm[3], ga);
+}
+
+}  // namespace
+
+bool moe_mx_mma_ok(int T, int H, int I, int E, int top_k) {
+  if (T < 1 || T > 16 || E < 1 || E > 1024 || top_k < 1 || top_k > 32 || top_k > E) return false;
+  if (H < 512 || I < 512 || H % 512 || I % 512) return false;
+  const MxDnPlan pd = plan_down(T, H, I, device_sm_count());
+  if (pd.ST < 2 || (size_t)kMxWarps * pd.MT * pd.NT * 512 > (size_t)pd.ST * pd.stage_bytes) return false;
+  return plan_gateup_stages() >= 2;
+}
+
+cudaError_t launch_moe_mx_mma(const uint16_t* x, const float* logits, const uint8_t* gq, const uint8_t* gs,
+                              const uint8_t* uq, const uint8_t* us, const uint8_t* dq, const uint8_t* ds, int T,
+                              int H, int I, int E, int top_k, float* y, int32_t* idx, float* wts, int32_t* xexp,
+                              uint16_t* xh, int32_t* vexp, int32_t* nvirt, uint32_t* hmax, float* h, uint32_t* err,
+                              cudaStream_t stream, bool pdl) {
+  const int sms = device_sm_count();
+  cudaError_t e;
+  if (E <= 128)
+    e = launch_kernel(moe_mx_route_mma_kernel<4>, dim3(1), dim3(kRouteThreads), 0, stream, pdl, logits, x, T, H, E,
+                      top_k, idx, wts, xexp, xh, vexp, nvirt, hmax);
+  else if (E <= 512)
+    e = launch_kernel(moe_mx_route_mma_kernel<16>, dim3(1), dim3(kRouteThreads), 0, stream, pdl, logits, x, T, H, E,
+                      top_k, idx, wts, xexp, xh, vexp, nvirt, hmax);
+  else
+    e = launch_kernel(moe_mx_route_mma_kernel<32>, dim3(1), dim3(kRouteThreads), 0, stream, pdl, logits, x, T, H, E,
+                      top_k, idx, wts, xexp, xh, vexp, nvirt, hmax);
+  if (e != cudaSuccess) return e;
+  // E2M1 codes as [rows][128-byte chunks] with 128B swizzle; E8M0 scales as 16 BPW-byte boxes
+  const int gbpw = H % 1024 == 0 ? 2 : 1;
+  const MxDnPlan pd = plan_down(T, H, I, sms);
+  CUtensorMap tm_gq, tm_uq, tm_gs, tm_us, tm_dq, tm_ds;
+  const uint64_t rows_gu = (uint64_t)E * I, rows_d = (uint64_t)E * H;
+  const uint32_t gb = 2 * gbpw, db = 2 * pd.BPW;
+  if (!tmap_3d(&tm_gq, CU_TENSOR_MAP_DATA_TYPE_UINT8, gq, 128, rows_gu, H / 256, H / 2, 128, 128, 32, gb) ||
+      !tmap_3d(&tm_uq, CU_TENSOR_MAP_DATA_TYPE_UINT8, uq, 128, rows_gu, H / 256, H / 2, 128, 128, 32, gb) ||
+      !tmap_2d(&tm_gs, CU_TENSOR_MAP_DATA_TYPE_UINT8, gs, H / 32, rows_gu, H / 32, 8 * gb, 32,
+               CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !tmap_2d(&tm_us, CU_TENSOR_MAP_DATA_TYPE_UINT8, us, H / 32, rows_gu, H / 32, 8 * gb, 32,
+               CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !tmap_3d(&tm_dq, CU_TENSOR_MAP_DATA_TYPE_UINT8, dq, 128, rows_d, I / 256, I / 2, 128, 128, pd.R, db) ||
+      !tmap_2d(&tm_ds, CU_TENSOR_MAP_DATA_TYPE_UINT8, ds, I / 32, rows_d, I / 32, 8 * db, pd.R,
+               CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  const int gst = plan_gateup_stages();
+  const MxGuArgs ga{xh, xexp, vexp, nvirt, h, hmax, H, I, top_k, gst, gbpw, err};
+  const int gu_grid = std::min(sms, moe_nvirt_max(T, E, top_k) * (I / 32));
+  const CUtensorMap gmaps[4] = {tm_gq, tm_uq, tm_gs, tm_us};
+  e = gbpw == 2 ? launch_gateup<2>(gmaps, ga, gu_grid, gateup_smem(gst), stream, pdl)
+                : launch_gateup<1>(gmaps, ga, gu_grid, gateup_smem(gst), stream, pdl);
+  if (e != cudaSuccess) return e;
+  const MxDnArgs da{h, hmax, wts, vexp, nvirt, y, T, H, I, top_k, pd.R, pd.ST, pd.BPW, pd.stage_bytes, pd.o_s, err};
+  if (pd.NT == 1)
+    return pd.BPW == 2 ? launch_down_mt<1, 2>(tm_dq, tm_ds, da, pd, stream, pdl)
+                       : launch_down_mt<1, 1>(tm_dq, tm_ds, da, pd, stream, pdl);
+  return pd.BPW == 2 ? launch_down_mt<2, 2>(tm_dq, tm_ds, da, pd, stream, pdl)
+                     : launch_down_mt<2, 1>(tm_dq, tm_ds, da, pd, stream, pdl);
+}
+
+}  // namespace qg

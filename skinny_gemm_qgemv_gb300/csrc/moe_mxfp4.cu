@@ -387,15 +387,14 @@ cudaError_t launch_moe_mxfp4(const uint16_t* x, const float* logits, const uint8
   cudaError_t e;
   const bool aligned = ((reinterpret_cast<uintptr_t>(gq) | reinterpret_cast<uintptr_t>(gs) |
                          reinterpret_cast<uintptr_t>(uq) | reinterpret_cast<uintptr_t>(us) |
-                         reinterpret_cast<uintptr_t>(dq) | reinterpret_cast<uintptr_t>(ds)) & 15u) == 0;
-  if (aligned && P <= 1024 && moe_mx_tiles_ok(T, H, I, E, top_k)) {
-    // main path: routing + grouping in one CTA, then the two streamed expert GEMVs
-    e = launch_moe_mx_route(logits, x, T, H, E, top_k, idx, wts, I32(L.xexp), I32(L.order), I32(L.vexp),
-                            I32(L.nvirt), reinterpret_cast<uint32_t*>(base + L.hmax), stream, pdl);
-    if (e != cudaSuccess) return e;
-    return launch_moe_mx_tiles(gq, gs, uq, us, dq, ds, x, I32(L.xexp), I32(L.vexp), I32(L.nvirt), wts,
-                               reinterpret_cast<float*>(base + L.h), reinterpret_cast<uint32_t*>(base + L.hmax), y, T,
-                               H, I, E, top_k, err, stream, pdl);
+                         reinterpret_cast<uintptr_t>(dq) | reinterpret_cast<uintptr_t>(ds) |
+                         reinterpret_cast<uintptr_t>(x)) & 15u) == 0;
+  if (aligned && moe_mx_mma_ok(T, H, I, E, top_k)) {
+    // main path: routing + grouping in one CTA, then gate/up and down on warp-level MMA
+    return launch_moe_mx_mma(x, logits, gq, gs, uq, us, dq, ds, T, H, I, E, top_k, y, idx, wts, I32(L.xexp),
+                             reinterpret_cast<uint16_t*>(base + L.xh), I32(L.vexp), I32(L.nvirt),
+                             reinterpret_cast<uint32_t*>(base + L.hmax), reinterpret_cast<float*>(base + L.h), err,
+                             stream, pdl);
   }
   // shapes outside the main path's tiling: one warp per row
   e = launch_kernel(moe_router_kernel, dim3(T), dim3(256), 0, stream, pdl, logits, x, H, E, top_k, idx, wts,

@@ -142,8 +142,8 @@ bool tmap_3d(CUtensorMap* tm, CUtensorMapDataType dt, const void* ptr, uint64_t 
              uint64_t chunks, uint64_t row_bytes, uint64_t chunk_bytes, uint32_t box_inner, uint32_t box_rows,
              uint32_t box_chunks);
 
-// MXFP4 MoE (moe_mxfp4.cu, moe_mx_tiles.cu)
-constexpr int kMxTC = 2;                // pairs of one virtual expert (held in registers)
+// MXFP4 MoE (moe_mxfp4.cu, moe_mx_mma.cu)
+constexpr int kMxTC = 8;                // pairs of one virtual expert: the N = 8 columns of one MMA
 constexpr int kMxVexpInts = 2 + kMxTC;  // virtual-expert table entry: expert, pair count, pairs
 // upper bound of the virtual experts of a batch: every active expert once, plus
 // one more for every further kMxTC pairs
@@ -157,15 +157,12 @@ struct MoeLayout {
   size_t total;
 };
 MoeLayout moe_layout(int T, int H, int I, int E, int top_k);
-bool moe_mx_tiles_ok(int T, int H, int I, int E, int top_k);
-cudaError_t launch_moe_mx_route(const float* logits, const uint16_t* x, int T, int H, int E, int top_k, int32_t* idx,
-                                float* wts, int32_t* xexp, int32_t* order, int32_t* vexp, int32_t* nvirt,
-                                uint32_t* hmax, cudaStream_t stream, bool pdl);
-cudaError_t launch_moe_mx_tiles(const uint8_t* gq, const uint8_t* gs, const uint8_t* uq, const uint8_t* us,
-                                const uint8_t* dq, const uint8_t* ds, const uint16_t* x, const int32_t* xexp,
-                                const int32_t* vexp, const int32_t* nvirt, const float* wts, float* h,
-                                uint32_t* hmax, float* y, int T, int H, int I, int E, int top_k, uint32_t* err,
-                                cudaStream_t stream, bool pdl);
+bool moe_mx_mma_ok(int T, int H, int I, int E, int top_k);
+cudaError_t launch_moe_mx_mma(const uint16_t* x, const float* logits, const uint8_t* gq, const uint8_t* gs,
+                              const uint8_t* uq, const uint8_t* us, const uint8_t* dq, const uint8_t* ds, int T,
+                              int H, int I, int E, int top_k, float* y, int32_t* idx, float* wts, int32_t* xexp,
+                              uint16_t* xh, int32_t* vexp, int32_t* nvirt, uint32_t* hmax, float* h, uint32_t* err,
+                              cudaStream_t stream, bool pdl);
 cudaError_t launch_moe_mxfp4(const uint16_t* x, const float* logits, const uint8_t* gq, const uint8_t* gs,
                              const uint8_t* uq, const uint8_t* us, const uint8_t* dq, const uint8_t* ds, int T,
                              int H, int I, int E, int top_k, float* y, int32_t* idx, float* wts, void* ws,

@@ -236,7 +236,8 @@ def check_moe(q, x, lg, w, top_k, tokens=None):
 
 
 @pytest.mark.parametrize("E,H,I,T,k", [(8, 256, 128, 3, 2), (16, 512, 256, 5, 4), (4, 64, 64, 1, 4),
-                                       (32, 1024, 512, 16, 8)])
+                                       (32, 1024, 512, 16, 8), (24, 1536, 1024, 7, 6), (8, 512, 512, 32, 4),
+                                       (40, 2048, 512, 12, 8), (300, 7168, 512, 2, 16)])
 def test_moe_small(q, E, H, I, T, k):
     x, lg, w = moe_inputs(E, H, I, T, seed=30 + E)
     check_moe(q, x, lg, w, k)
@@ -250,6 +251,16 @@ def test_moe_tied_logits_pick_lower_index(q):
     y, idx = check_moe(q, x, lg, w, k)
     assert idx[0].tolist() == [0, 1, 2, 3, 4]
     assert idx[1].tolist() == [3, 9, 12, 0, 1]
+
+
+def test_moe_shared_experts_split_into_virtual_experts(q):
+    # every token picks experts 0..k-1 (zero logits, ties to the lower index):
+    # 20 pairs per expert, more than one MMA's 8 columns
+    E, H, I, T, k = 12, 1024, 512, 20, 3
+    x, lg, w = moe_inputs(E, H, I, T, seed=47)
+    lg = torch.zeros_like(lg)
+    y, idx = check_moe(q, x, lg, w, k)
+    assert (idx == torch.tensor([0, 1, 2], dtype=idx.dtype, device=idx.device)).all()
 
 
 @pytest.mark.parametrize("T", [1, 16])
