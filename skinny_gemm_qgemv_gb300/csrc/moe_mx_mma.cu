@@ -57,6 +57,7 @@ constexpr uint32_t kGuCodes = 4 * 32 * 128;
 constexpr uint32_t kGuScales = 32 * 32;
 constexpr uint32_t kGuStage = 2 * kGuCodes + 2 * kGuScales;
 constexpr uint32_t kGuRed = 2u * kMxWarps * 4 * 32 * 16;  // two buffers of the warps' partial tiles
+constexpr int kGuTileRows = 512;  // tiles of a CTA whose first weight row is kept in shared memory
 
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {
@@ -96,6 +97,15 @@ __device__ __forceinline__ float key_logit(uint32_t k) {
 }
 
 __device__ __forceinline__ void bar_consumers() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kMxWarps) : "memory"); }
+
+// split barrier over all warps of the CTA: the epilogue warps wait, the others
+// only arrive (ids 2, 3)
+__device__ __forceinline__ void bar_arrive_all(int id) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "n"(32 * kMxWarps) : "memory");
+}
+__device__ __forceinline__ void bar_sync_all(int id) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(32 * kMxWarps) : "memory");
+}
 
 // Stage release: every warp adds one to the slot's counter after its last read
 // of the slot (acquire-release, so the last adder sees all the other warps'
@@ -360,10 +370,12 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const gbase = smem_raw + (base - raw);
-  // shared layout: stages | red (two buffers) | full barriers | release counters
+  // shared layout: stages | red (two buffers) | full barriers | release counters | first weight
+  //                row of each of this CTA's tiles
   float4* red = reinterpret_cast<float4*>(gbase + (size_t)a.ST * kGuStage);
   uint64_t* full = reinterpret_cast<uint64_t*>(gbase + (size_t)a.ST * kGuStage + kGuRed);
   uint32_t* rel = reinterpret_cast<uint32_t*>(full + a.ST);
+  int* trow = reinterpret_cast<int*>(rel + a.ST);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.ST; ++i) {
@@ -385,11 +397,21 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   const int t0 = min(total, (int)blockIdx.x * per), t1 = min(total, t0 + per);
   const int nstages = (t1 - t0) * nks;
   const uint64_t pol = policy_evict_first();
+  for (int t = threadIdx.x; t < t1 - t0 && t < kGuTileRows; t += blockDim.x) {
+    const int v = (t0 + t) / tpv;
+    trow[t] = __ldg(a.vexp + (size_t)v * kMxVexpInts) * I + (t0 + t - v * tpv) * 32;
+  }
+  __syncthreads();
   // stage q of this CTA into its slot: codes and scales of 32 gate and 32 up rows, 512 BPW k
   auto issue = [&](int q) {
-    const int tile = t0 + q / nks, ks = q - (q / nks) * nks;
-    const int v = tile / tpv, r0 = (tile - v * tpv) * 32;
-    const int row = __ldg(a.vexp + (size_t)v * kMxVexpInts) * I + r0;
+    const int tl = q / nks, ks = q - tl * nks;
+    int row;
+    if (tl < kGuTileRows) {
+      row = trow[tl];
+    } else {
+      const int v = (t0 + tl) / tpv;
+      row = __ldg(a.vexp + (size_t)v * kMxVexpInts) * I + (t0 + tl - v * tpv) * 32;
+    }
     const int st = q % a.ST;
     const uint32_t sb = base + st * kGuStage;
     mbar_arrive_expect_tx(&full[st], (2 * 4096u + 512u) * 2u * BPW);
@@ -477,16 +499,21 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       }
     }
     xrow = xnext;
-    // the warps' partial tiles, summed in warp order; h = silu(g) u. Two
-    // buffers: a warp writes buffer b of the next tile only after every warp
-    // passed this tile's barrier, i.e. finished reading buffer b of the last one
+    // the warps' partial tiles, summed in warp order; h = silu(g) u. Buffer and
+    // barrier b alternate per tile, and so does the half of the warps that sums
+    // (the other half only arrives and goes on). A warp writes buffer b again
+    // two tiles later, after it waited at the other barrier for every warp,
+    // which each arrive there only after they finished reading buffer b.
     float4* rb = red + buf * (kMxWarps * 4 * 32);
 #pragma unroll
     for (int mt = 0; mt < 4; ++mt)
       rb[(warp * 4 + mt) * 32 + lane] = make_float4(acc[mt][0], acc[mt][1], acc[mt][2], acc[mt][3]);
-    bar_consumers();
-    if (et < 256) {
-      const int mt = et >> 6, hs = (et >> 5) & 1, l = et & 31;
+    if ((warp >> 3) != buf) {
+      bar_arrive_all(2 + buf);
+    } else {
+      bar_sync_all(2 + buf);
+      const int e2 = et & 255;
+      const int mt = e2 >> 6, hs = (e2 >> 5) & 1, l = e2 & 31;
       const int col = 2 * (l & 3) + hs;  // the pair
       if (col < np) {
         float gs = 0.f, us = 0.f;
@@ -543,13 +570,14 @@ __device__ __forceinline__ void dn_lane(const MxDnArgs& a, int v, int g, const i
   }
   for (int q = 0; q < np; ++q) {
     const int pair = __ldg(ent + 2 + q);
-    const int t = pair / a.top_k;
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-      if (t == 8 * nt + g) {
+    for (int nt = 0; nt < NT; ++nt) {
+      const int p0 = (8 * nt + g) * a.top_k;  // the pairs of token 8 nt + g
+      if (pair >= p0 && pair < p0 + a.top_k) {
         L.hp[nt] = a.h + (size_t)pair * a.I;
-        L.f[nt] = __ldg(a.wts + pair) * pow2f(-sig[t]);
+        L.f[nt] = __ldg(a.wts + pair) * pow2f(-sig[8 * nt + g]);
       }
+    }
   }
 }
 
@@ -573,6 +601,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   int* sig = reinterpret_cast<int*>(gbase + (size_t)a.ST * kStage);
   uint64_t* full = reinterpret_cast<uint64_t*>(sig + 8 * NT);
   uint32_t* rel = reinterpret_cast<uint32_t*>(full + a.ST);
+  int* vrow = reinterpret_cast<int*>(rel + a.ST);  // first weight row of each virtual expert's range
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.ST; ++i) {
@@ -603,12 +632,14 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   const int vstart = nv > 0 ? (int)(((long long)blockIdx.x * nv) / gridDim.x) : 0;
   const int nstages = nv * nks;
   const uint64_t pol = policy_evict_first();
+  for (int v2 = threadIdx.x; v2 < nv; v2 += blockDim.x) vrow[v2] = __ldg(a.vexp + (size_t)v2 * kMxVexpInts) * H + n0;
+  __syncthreads();
   // stage q of this CTA into its slot: codes and scales of its R rows of one virtual expert, KS k
   auto issue = [&](int q) {
     const int i = q / nks, ks = q - i * nks;
     int v = vstart + i;
     if (v >= nv) v -= nv;
-    const int row = __ldg(a.vexp + (size_t)v * kMxVexpInts) * H + n0;
+    const int row = vrow[v];
     const int st = q % a.ST;
     const uint32_t sb = base + st * kStage;
     mbar_arrive_expect_tx(&full[st], 272u * R * BPW);
@@ -760,25 +791,27 @@ struct MxDnPlan {
   size_t smem;
 };
 
-MxDnPlan plan_down(int T, int H, int I, int sms) {
+MxDnPlan plan_down(int T, int H, int I, int nvmax, int sms) {
   MxDnPlan p{};
   // rows per CTA: a multiple of 16 that gives about one range per SM
   p.MT = std::min(4, std::max(1, (H + 16 * sms - 1) / (16 * sms)));
   p.R = 16 * p.MT;
   p.grid = (H + p.R - 1) / p.R;
   p.NT = T <= 8 ? 1 : 2;
-  p.BPW = I % 1024 == 0 ? 2 : 1;
+  p.BPW = (p.NT == 1 && I % 2048 == 0) ? 4 : (I % 1024 == 0 ? 2 : 1);
   p.o_s = 256u * p.R * p.BPW;  // codes: [2 BPW chunks][R rows][128 B], then scales [R][16 BPW]
   p.stage_bytes = (272u * p.R * p.BPW + 1023u) & ~1023u;
-  const size_t fixed = 1024 + 4 * 8 * p.NT + 64;
+  const size_t fixed = 1024 + 4 * 8 * p.NT + 4 * (size_t)nvmax + 64;
   p.ST = (int)std::min<size_t>(8, (kMxSmem - fixed) / (p.stage_bytes + 16));
   p.smem = fixed + (size_t)p.ST * (p.stage_bytes + 16);
   return p;
 }
 
-int plan_gateup_stages() { return (int)std::min<size_t>(8, (kMxSmem - 1024 - kGuRed - 64) / (kGuStage + 16)); }
+int plan_gateup_stages() {
+  return (int)std::min<size_t>(8, (kMxSmem - 1024 - kGuRed - 4 * kGuTileRows - 64) / (kGuStage + 16));
+}
 
-size_t gateup_smem(int ST) { return 1024 + (size_t)ST * (kGuStage + 16) + kGuRed + 64; }
+size_t gateup_smem(int ST) { return 1024 + (size_t)ST * (kGuStage + 16) + kGuRed + 4 * kGuTileRows + 64; }
 
 template <int NT, int MT, int BPW>
 cudaError_t launch_down(const CUtensorMap& tm_dq, const CUtensorMap& tm_ds, const MxDnArgs& da, const MxDnPlan& pd,
@@ -814,7 +847,7 @@ cudaError_t launch_gateup(const CUtensorMap* tm, const MxGuArgs& ga, int grid, s
 bool moe_mx_mma_ok(int T, int H, int I, int E, int top_k) {
   if (T < 1 || T > 16 || E < 1 || E > 1024 || top_k < 1 || top_k > 32 || top_k > E) return false;
   if (H < 512 || I < 512 || H % 512 || I % 512) return false;
-  const MxDnPlan pd = plan_down(T, H, I, device_sm_count());
+  const MxDnPlan pd = plan_down(T, H, I, moe_nvirt_max(T, E, top_k), device_sm_count());
   if (pd.ST < 2 || (size_t)kMxWarps * pd.MT * pd.NT * 512 > (size_t)pd.ST * pd.stage_bytes) return false;
   return plan_gateup_stages() >= 2;
 }
@@ -838,7 +871,7 @@ cudaError_t launch_moe_mx_mma(const uint16_t* x, const float* logits, const uint
   if (e != cudaSuccess) return e;
   // E2M1 codes as [rows][128-byte chunks] with 128B swizzle; E8M0 scales as 16 BPW-byte boxes
   const int gbpw = H % 1024 == 0 ? 2 : 1;
-  const MxDnPlan pd = plan_down(T, H, I, sms);
+  const MxDnPlan pd = plan_down(T, H, I, moe_nvirt_max(T, E, top_k), sms);
   CUtensorMap tm_gq, tm_uq, tm_gs, tm_us, tm_dq, tm_ds;
   const uint64_t rows_gu = (uint64_t)E * I, rows_d = (uint64_t)E * H;
   const uint32_t gb = 2 * gbpw, db = 2 * pd.BPW;
@@ -861,8 +894,9 @@ cudaError_t launch_moe_mx_mma(const uint16_t* x, const float* logits, const uint
   if (e != cudaSuccess) return e;
   const MxDnArgs da{h, hmax, wts, vexp, nvirt, y, T, H, I, top_k, pd.R, pd.ST, pd.BPW, pd.stage_bytes, pd.o_s, err};
   if (pd.NT == 1)
-    return pd.BPW == 2 ? launch_down_mt<1, 2>(tm_dq, tm_ds, da, pd, stream, pdl)
-                       : launch_down_mt<1, 1>(tm_dq, tm_ds, da, pd, stream, pdl);
+    return pd.BPW == 4   ? launch_down_mt<1, 4>(tm_dq, tm_ds, da, pd, stream, pdl)
+           : pd.BPW == 2 ? launch_down_mt<1, 2>(tm_dq, tm_ds, da, pd, stream, pdl)
+                         : launch_down_mt<1, 1>(tm_dq, tm_ds, da, pd, stream, pdl);
   return pd.BPW == 2 ? launch_down_mt<2, 2>(tm_dq, tm_ds, da, pd, stream, pdl)
                      : launch_down_mt<2, 1>(tm_dq, tm_ds, da, pd, stream, pdl);
 }
