@@ -354,10 +354,12 @@ struct MxGuArgs {
   uint32_t* err;
 };
 
-// x row of pair g of the tile's virtual expert (null: no such pair)
+// x row of pair g of the tile's virtual expert; columns past the pair count
+// take pair 0's row (their MMA results are never read)
 __device__ __forceinline__ const uint16_t* gu_xrow(const MxGuArgs& a, int tile, int tpv, int g) {
   const int32_t* ent = a.vexp + (size_t)(tile / tpv) * kMxVexpInts;
-  return g < __ldg(ent + 1) ? a.xh + (size_t)(__ldg(ent + 2 + g) / a.top_k) * a.H : nullptr;
+  const int j = min(g, __ldg(ent + 1) - 1);
+  return a.xh + (size_t)(__ldg(ent + 2 + j) / a.top_k) * a.H;
 }
 
 // BPW: 32-k blocks per warp and stage (a stage is 512 BPW k of the tile's rows)
@@ -442,19 +444,22 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   bool ok = true;
   // x of the next stage, loaded one stage ahead (L2-resident)
   uint4 xn[BPW];
-  const uint16_t* xrow = t0 < t1 ? gu_xrow(a, t0, tpv, g) : nullptr;
+  const uint16_t* xrow = t0 < t1 ? gu_xrow(a, t0, tpv, g) : a.xh;
   auto load_x = [&](const uint16_t* row, int ks) {
 #pragma unroll
     for (int j = 0; j < BPW; ++j)
-      xn[j] = row ? __ldg(reinterpret_cast<const uint4*>(row + ks * KS + 32 * (BPW * warp + j) + 8 * c))
-                  : make_uint4(0u, 0u, 0u, 0u);
+      xn[j] = __ldg(reinterpret_cast<const uint4*>(row + ks * KS + 32 * (BPW * warp + j) + 8 * c));
   };
-  load_x(xrow, 0);
+  if (t0 < t1) load_x(xrow, 0);
   for (int tile = t0; tile < t1; ++tile) {
     const int v = tile / tpv, r0 = (tile - v * tpv) * 32;
     const int32_t* ent = a.vexp + (size_t)v * kMxVexpInts;
     const int np = __ldg(ent + 1);
-    const uint16_t* xnext = tile + 1 < t1 ? gu_xrow(a, tile + 1, tpv, g) : nullptr;
+    const uint16_t* xnext = tile + 1 < t1 ? gu_xrow(a, tile + 1, tpv, g) : xrow;
+    // this thread's epilogue column (pair) and its 2^sigma, fetched early
+    const int ecol = 2 * (et & 3) + ((et >> 5) & 1);
+    const int epair = ecol < np ? __ldg(ent + 2 + ecol) : 0;
+    const float esc = pow2f(__ldg(a.xexp + epair / a.top_k));
     float acc[4][4];
 #pragma unroll
     for (int mt = 0; mt < 4; ++mt)
@@ -523,9 +528,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           gs += hs ? r4.y : r4.x;
           us += hs ? r4.w : r4.z;
         }
-        const int pair = __ldg(ent + 2 + col);
-        const float sc = pow2f(__ldg(a.xexp + pair / a.top_k));
-        const float gv = gs * sc, uv = us * sc;
+        const int pair = epair;
+        const float gv = gs * esc, uv = us * esc;
         const float hv = gv / (1.f + expf(-gv)) * uv;
         const int row = r0 + 8 * mt + (l >> 2);
         a.h[(size_t)pair * I + row] = hv;
