@@ -550,38 +550,32 @@ struct MxDnArgs {
   const int32_t* vexp;
   const int32_t* nvirt;
   float* y;               // [T][H]
-  int T, H, I, top_k, R, ST, BPW;
+  int T, H, I, top_k, R, ST, BPW, nvmax;
   uint32_t stage_bytes, o_s;  // stage size; offset of the scales in a stage
   uint32_t* err;
 };
 
 // a lane's tokens 8 nt + g in one virtual expert: the h row of the token's
-// pair (null if the token is not in it) and p * 2^-sigma_t
+// pair and p * 2^-sigma_t (a token not in it: pair 0's row and factor 0, so its
+// column of B is 0); act: n tiles with at least one of their tokens in it
 template <int NT>
 struct DnLane {
   const float* hp[NT];
   float f[NT];
+  uint32_t act;
 };
 
+// from the shared tables: pair of (virtual expert, token) or -1, and p * 2^-sigma_t per pair
 template <int NT>
-__device__ __forceinline__ void dn_lane(const MxDnArgs& a, int v, int g, const int* sig, DnLane<NT>& L) {
-  const int32_t* ent = a.vexp + (size_t)v * kMxVexpInts;
-  const int np = __ldg(ent + 1);
+__device__ __forceinline__ void dn_lane(const MxDnArgs& a, int v, int g, const int16_t* tab, const float* fp,
+                                        DnLane<NT>& L) {
+  L.act = 0u;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    L.hp[nt] = nullptr;
-    L.f[nt] = 0.f;
-  }
-  for (int q = 0; q < np; ++q) {
-    const int pair = __ldg(ent + 2 + q);
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int p0 = (8 * nt + g) * a.top_k;  // the pairs of token 8 nt + g
-      if (pair >= p0 && pair < p0 + a.top_k) {
-        L.hp[nt] = a.h + (size_t)pair * a.I;
-        L.f[nt] = __ldg(a.wts + pair) * pow2f(-sig[8 * nt + g]);
-      }
-    }
+    const int pair = tab[v * 8 * NT + 8 * nt + g];
+    L.hp[nt] = a.h + (size_t)max(pair, 0) * a.I;
+    L.f[nt] = pair >= 0 ? fp[pair] : 0.f;
+    if (__any_sync(kFull, pair >= 0)) L.act |= 1u << nt;
   }
 }
 
@@ -606,6 +600,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(sig + 8 * NT);
   uint32_t* rel = reinterpret_cast<uint32_t*>(full + a.ST);
   int* vrow = reinterpret_cast<int*>(rel + a.ST);  // first weight row of each virtual expert's range
+  float* fp = reinterpret_cast<float*>(vrow + a.nvmax);                   // [P] p * 2^-sigma_t
+  int16_t* tab = reinterpret_cast<int16_t*>(fp + a.T * a.top_k);          // [nvmax][8 NT] pair or -1
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.ST; ++i) {
@@ -637,6 +633,16 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   const int nstages = nv * nks;
   const uint64_t pol = policy_evict_first();
   for (int v2 = threadIdx.x; v2 < nv; v2 += blockDim.x) vrow[v2] = __ldg(a.vexp + (size_t)v2 * kMxVexpInts) * H + n0;
+  for (int p = threadIdx.x; p < a.T * a.top_k; p += blockDim.x) fp[p] = a.wts[p] * pow2f(-sig[p / a.top_k]);
+  for (int q = threadIdx.x; q < nv * 8 * NT; q += blockDim.x) tab[q] = -1;
+  __syncthreads();
+  for (int q = threadIdx.x; q < nv * kMxTC; q += blockDim.x) {
+    const int v2 = q / kMxTC, j = q - v2 * kMxTC;
+    if (j < __ldg(a.vexp + (size_t)v2 * kMxVexpInts + 1)) {
+      const int pair = __ldg(a.vexp + (size_t)v2 * kMxVexpInts + 2 + j);
+      tab[v2 * 8 * NT + pair / a.top_k] = (int16_t)pair;
+    }
+  }
   __syncthreads();
   // stage q of this CTA into its slot: codes and scales of its R rows of one virtual expert, KS k
   auto issue = [&](int q) {
@@ -676,9 +682,9 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   auto load_h = [&](const DnLane<NT>& L, int ks) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
+      if ((L.act >> nt) & 1u)
 #pragma unroll
-      for (int j = 0; j < BPW; ++j)
-        if (L.hp[nt]) {
+        for (int j = 0; j < BPW; ++j) {
           const uint4* p = reinterpret_cast<const uint4*>(L.hp[nt] + ks * KS + 32 * (BPW * warp + j) + 8 * c);
           hn[nt][j][0] = __ldcg(p);
           hn[nt][j][1] = __ldcg(p + 1);
@@ -689,7 +695,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   uint32_t par = 0;
   bool ok = true;
   if (nv > 0) {
-    dn_lane<NT>(a, v, g, sig, cur);
+    dn_lane<NT>(a, v, g, tab, fp, cur);
     load_h(cur, 0);
   }
   for (int q = 0; q < nstages; ++q) {
@@ -697,25 +703,22 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     uint32_t b[NT][BPW][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
+      if ((cur.act >> nt) & 1u)
 #pragma unroll
-      for (int j = 0; j < BPW; ++j) {
-        if (cur.hp[nt]) {
+        for (int j = 0; j < BPW; ++j) {
           const float f = cur.f[nt];
           const uint4 lo = hn[nt][j][0], hi = hn[nt][j][1];
           b[nt][j][0] = f16x2_rn(__uint_as_float(lo.x) * f, __uint_as_float(lo.y) * f);
           b[nt][j][1] = f16x2_rn(__uint_as_float(lo.z) * f, __uint_as_float(lo.w) * f);
           b[nt][j][2] = f16x2_rn(__uint_as_float(hi.x) * f, __uint_as_float(hi.y) * f);
           b[nt][j][3] = f16x2_rn(__uint_as_float(hi.z) * f, __uint_as_float(hi.w) * f);
-        } else {
-          b[nt][j][0] = b[nt][j][1] = b[nt][j][2] = b[nt][j][3] = 0u;
         }
-      }
     // the next stage's h
     bool newv = false;
     if (ks + 1 < nks) {
       load_h(cur, ks + 1);
     } else if (i + 1 < nv) {
-      dn_lane<NT>(a, v + 1 == nv ? 0 : v + 1, g, sig, nxt);
+      dn_lane<NT>(a, v + 1 == nv ? 0 : v + 1, g, tab, fp, nxt);
       load_h(nxt, 0);
       newv = true;
     }
@@ -737,6 +740,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           const uint32_t a6 = e2m1x2_to_f16x2<3>(w0), a7 = e2m1x2_to_f16x2<3>(w1);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
+            if (!((cur.act >> nt) & 1u)) continue;  // none of the n tile's tokens is in this virtual expert
             float t[4];
             mma_f16_z(t, a0, a1, a2, a3, b[nt][j][0], b[nt][j][1]);
             mma_f16(t, a4, a5, a6, a7, b[nt][j][2], b[nt][j][3]);
@@ -795,7 +799,7 @@ struct MxDnPlan {
   size_t smem;
 };
 
-MxDnPlan plan_down(int T, int H, int I, int nvmax, int sms) {
+MxDnPlan plan_down(int T, int H, int I, int top_k, int nvmax, int sms) {
   MxDnPlan p{};
   // rows per CTA: a multiple of 16 that gives about one range per SM
   p.MT = std::min(4, std::max(1, (H + 16 * sms - 1) / (16 * sms)));
@@ -805,7 +809,8 @@ MxDnPlan plan_down(int T, int H, int I, int nvmax, int sms) {
   p.BPW = (p.NT == 1 && I % 2048 == 0) ? 4 : (I % 1024 == 0 ? 2 : 1);
   p.o_s = 256u * p.R * p.BPW;  // codes: [2 BPW chunks][R rows][128 B], then scales [R][16 BPW]
   p.stage_bytes = (272u * p.R * p.BPW + 1023u) & ~1023u;
-  const size_t fixed = 1024 + 4 * 8 * p.NT + 4 * (size_t)nvmax + 64;
+  const size_t fixed = 1024 + 4 * 8 * p.NT + 4 * (size_t)nvmax + 4 * (size_t)T * top_k +
+                       2 * (size_t)nvmax * 8 * p.NT + 64;
   p.ST = (int)std::min<size_t>(8, (kMxSmem - fixed) / (p.stage_bytes + 16));
   p.smem = fixed + (size_t)p.ST * (p.stage_bytes + 16);
   return p;
@@ -851,7 +856,7 @@ cudaError_t launch_gateup(const CUtensorMap* tm, const MxGuArgs& ga, int grid, s
 bool moe_mx_mma_ok(int T, int H, int I, int E, int top_k) {
   if (T < 1 || T > 16 || E < 1 || E > 1024 || top_k < 1 || top_k > 32 || top_k > E) return false;
   if (H < 512 || I < 512 || H % 512 || I % 512) return false;
-  const MxDnPlan pd = plan_down(T, H, I, moe_nvirt_max(T, E, top_k), device_sm_count());
+  const MxDnPlan pd = plan_down(T, H, I, top_k, moe_nvirt_max(T, E, top_k), device_sm_count());
   if (pd.ST < 2 || (size_t)kMxWarps * pd.MT * pd.NT * 512 > (size_t)pd.ST * pd.stage_bytes) return false;
   return plan_gateup_stages() >= 2;
 }
@@ -875,7 +880,7 @@ cudaError_t launch_moe_mx_mma(const uint16_t* x, const float* logits, const uint
   if (e != cudaSuccess) return e;
   // E2M1 codes as [rows][128-byte chunks] with 128B swizzle; E8M0 scales as 16 BPW-byte boxes
   const int gbpw = H % 1024 == 0 ? 2 : 1;
-  const MxDnPlan pd = plan_down(T, H, I, moe_nvirt_max(T, E, top_k), sms);
+  const MxDnPlan pd = plan_down(T, H, I, top_k, moe_nvirt_max(T, E, top_k), sms);
   CUtensorMap tm_gq, tm_uq, tm_gs, tm_us, tm_dq, tm_ds;
   const uint64_t rows_gu = (uint64_t)E * I, rows_d = (uint64_t)E * H;
   const uint32_t gb = 2 * gbpw, db = 2 * pd.BPW;
@@ -896,7 +901,8 @@ cudaError_t launch_moe_mx_mma(const uint16_t* x, const float* logits, const uint
   e = gbpw == 2 ? launch_gateup<2>(gmaps, ga, gu_grid, gateup_smem(gst), stream, pdl)
                 : launch_gateup<1>(gmaps, ga, gu_grid, gateup_smem(gst), stream, pdl);
   if (e != cudaSuccess) return e;
-  const MxDnArgs da{h, hmax, wts, vexp, nvirt, y, T, H, I, top_k, pd.R, pd.ST, pd.BPW, pd.stage_bytes, pd.o_s, err};
+  const MxDnArgs da{h,     hmax,  wts,   vexp,   nvirt,    y, T, H, I, top_k, pd.R, pd.ST, pd.BPW,
+                    moe_nvirt_max(T, E, top_k), pd.stage_bytes, pd.o_s, err};
   if (pd.NT == 1)
     return pd.BPW == 4   ? launch_down_mt<1, 4>(tm_dq, tm_ds, da, pd, stream, pdl)
            : pd.BPW == 2 ? launch_down_mt<1, 2>(tm_dq, tm_ds, da, pd, stream, pdl)
