@@ -119,6 +119,21 @@ __device__ __forceinline__ bool release_is_last(uint32_t* cnt, uint32_t warps) {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic reads before the async-proxy writes
   return true;
 }
+// E8M0 scales land with the TMA swizzle that matches their row length S
+// (S = 32: 32-byte swizzle, 16-byte unit ^= row bit 2; S = 64: 64-byte swizzle,
+// unit ^= row bits 1..2; S = 16: none), so the 8 rows a warp reads at once sit
+// in different banks. For the rows the kernels read (8 m + g, 16 m + g,
+// 16 m + g + 8) the unit flip depends on g only.
+template <uint32_t S>
+__device__ __forceinline__ uint32_t scale_byte(uint32_t g, uint32_t b) {
+  if (S == 32) return b ^ (((g >> 2) & 1u) << 4);
+  if (S == 64) return b ^ (((g >> 1) & 3u) << 4);
+  return b;
+}
+constexpr CUtensorMapSwizzle scale_swizzle(uint32_t S) {
+  return S == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : (S == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 // TMA 3D load with an L2 eviction-priority hint (streamed weights: evict first)
 __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void* tm, int x, int y, int z, uint64_t* bar,
                                                  uint64_t pol) {
@@ -437,7 +452,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   for (int j = 0; j < BPW; ++j) {
     const uint32_t blk = BPW * warp + j;
     coff[j] = (blk >> 3) * 4096u + g * 128u + (((blk & 7u) ^ (uint32_t)g) << 4) + 4u * c;
-    soff[j] = 2 * kGuCodes + g * kSRow + blk;
+    soff[j] = 2 * kGuCodes + g * kSRow + scale_byte<kSRow>(g, blk);
   }
   int st = 0, q = 0, buf = 0;
   uint32_t par = 0;
@@ -668,7 +683,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   for (int j = 0; j < BPW; ++j) {
     const uint32_t blk = BPW * warp + j;
     coff[j] = (blk >> 3) * (128u * R) + g * 128u + (((blk & 7u) ^ (uint32_t)g) << 4) + 4u * c;
-    soff[j] = kOS + g * kSRow + blk;
+    soff[j] = kOS + g * kSRow + scale_byte<kSRow>(g, blk);
   }
   float acc[MT][NT][4];
 #pragma unroll
@@ -887,12 +902,12 @@ cudaError_t launch_moe_mx_mma(const uint16_t* x, const float* logits, const uint
   if (!tmap_3d(&tm_gq, CU_TENSOR_MAP_DATA_TYPE_UINT8, gq, 128, rows_gu, H / 256, H / 2, 128, 128, 32, gb) ||
       !tmap_3d(&tm_uq, CU_TENSOR_MAP_DATA_TYPE_UINT8, uq, 128, rows_gu, H / 256, H / 2, 128, 128, 32, gb) ||
       !tmap_2d(&tm_gs, CU_TENSOR_MAP_DATA_TYPE_UINT8, gs, H / 32, rows_gu, H / 32, 8 * gb, 32,
-               CU_TENSOR_MAP_SWIZZLE_NONE) ||
+               scale_swizzle(8 * gb)) ||
       !tmap_2d(&tm_us, CU_TENSOR_MAP_DATA_TYPE_UINT8, us, H / 32, rows_gu, H / 32, 8 * gb, 32,
-               CU_TENSOR_MAP_SWIZZLE_NONE) ||
+               scale_swizzle(8 * gb)) ||
       !tmap_3d(&tm_dq, CU_TENSOR_MAP_DATA_TYPE_UINT8, dq, 128, rows_d, I / 256, I / 2, 128, 128, pd.R, db) ||
       !tmap_2d(&tm_ds, CU_TENSOR_MAP_DATA_TYPE_UINT8, ds, I / 32, rows_d, I / 32, 8 * db, pd.R,
-               CU_TENSOR_MAP_SWIZZLE_NONE))
+               scale_swizzle(8 * db)))
     return cudaErrorInvalidValue;
   const int gst = plan_gateup_stages();
   const MxGuArgs ga{xh, xexp, vexp, nvirt, h, hmax, H, I, top_k, gst, gbpw, err};

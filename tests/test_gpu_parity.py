@@ -237,7 +237,8 @@ def check_moe(q, x, lg, w, top_k, tokens=None):
 
 @pytest.mark.parametrize("E,H,I,T,k", [(8, 256, 128, 3, 2), (16, 512, 256, 5, 4), (4, 64, 64, 1, 4),
                                        (32, 1024, 512, 16, 8), (24, 1536, 1024, 7, 6), (8, 512, 512, 32, 4),
-                                       (40, 2048, 512, 12, 8), (300, 7168, 512, 2, 16)])
+                                       (40, 2048, 512, 12, 8), (300, 7168, 512, 2, 16),
+                                       (16, 4096, 1024, 3, 4), (8, 8192, 512, 2, 2), (700, 512, 512, 2, 8)])
 def test_moe_small(q, E, H, I, T, k):
     x, lg, w = moe_inputs(E, H, I, T, seed=30 + E)
     check_moe(q, x, lg, w, k)
@@ -251,6 +252,25 @@ def test_moe_tied_logits_pick_lower_index(q):
     y, idx = check_moe(q, x, lg, w, k)
     assert idx[0].tolist() == [0, 1, 2, 3, 4]
     assert idx[1].tolist() == [3, 9, 12, 0, 1]
+
+
+def test_moe_ties_at_the_threshold_main_path(q):
+    # H, I multiples of 512: the warp radix-select router. Equal logits
+    # straddle the k-th place; -0.0 and +0.0 compare equal.
+    E, H, I, T, k = 64, 512, 512, 4, 8
+    x, lg, w = moe_inputs(E, H, I, T, seed=43)
+    lg[0] = 0.0
+    lg[1] = 0.0
+    lg[1, [3, 9, 12, 40, 41]] = 1.0
+    lg[2] = -1.0
+    lg[2, 5] = -0.0
+    lg[2, 6] = 0.0
+    lg[2, [20, 21, 30]] = 2.0
+    y, idx = check_moe(q, x, lg, w, k)
+    assert idx[0].tolist() == list(range(8))
+    assert idx[1].tolist() == [3, 9, 12, 40, 41, 0, 1, 2]
+    assert idx[2].tolist()[:5] == [20, 21, 30, 5, 6]
+    assert idx[2].tolist()[5:] == [0, 1, 2]
 
 
 def test_moe_shared_experts_split_into_virtual_experts(q):
