@@ -15,22 +15,27 @@
 //    max |x| in [2^14, 2^15)), the per-expert grouping and the "virtual
 //    experts": runs of at most kMxTC = 8 pairs (token, slot) of one expert,
 //    the N = 8 columns of one MMA.
-//  * gate/up: persistent; a tile is (virtual expert, 32 rows of I) with both
-//    matrices. A producer warp moves 512-k stages with TMA: the E2M1 codes of
-//    the 32 gate and 32 up rows (128B-swizzled), their E8M0 scales and the fp16
-//    x rows of the tile's pairs. Eight consumer warps own two 32-k blocks of
-//    every stage each; one mma.sync.m16n8k16 row block holds 8 gate rows (MMA
-//    rows 0..7) and the same 8 up rows (rows 8..15), so g and u of a row meet
-//    in one accumulator fragment. Per block: 2 MMAs from zero, then
-//    acc += result * 2^(scale - 127) per row (the block scale is a row factor
-//    of the MMA result). At the end of a tile the warps' partial sums are added
-//    in warp order through shared memory and h = silu(g) u is written in fp32
-//    with the pair's max |h|.
-//  * down: one CTA per range of R = 16 * MT rows of H, over every virtual
-//    expert; the MMA columns are the batch's tokens, so one accumulator per
-//    (row, token) collects all of a token's experts. B is p * h * 2^-sigma_t in
-//    fp16 (sigma_t per token from max_j p_j max|h_j|), converted from the
-//    staged fp32 h by the warp that owns the block. One cross-warp sum at the
+//  * gate/up: persistent, 16 warps; a tile is (virtual expert, 32 rows of I)
+//    with both matrices, CTAs take contiguous tile ranges. A stage is 1024 k
+//    (512 if H is not a multiple of 1024) of the tile's 32 gate and 32 up rows:
+//    E2M1 codes by TMA (128B-swizzled) and E8M0 scales, in a ring of 4. Every
+//    warp owns two 32-k blocks of every stage; one mma.sync.m16n8k16 row block
+//    holds 8 gate rows (MMA rows 0..7) and the same 8 up rows (rows 8..15), so
+//    g and u of a row meet in one accumulator fragment. B is the fp16 x of the
+//    tile's pairs, loaded from L2 one stage ahead. Per block: 2 MMAs from
+//    zero, then acc += result * 2^(scale - 127) per row (the block scale is a
+//    row factor of the MMA result). No warp is set aside for the copies: the
+//    last warp to release a slot issues the stage that goes into it. At the end
+//    of a tile the warps' partial sums are added in warp order through shared
+//    memory by one half of the warps (alternating per tile) and h = silu(g) u
+//    is written in fp32 with the pair's max |h|.
+//  * down: one CTA of 16 warps per range of R = 16 * MT rows of H, over every
+//    virtual expert, stages of 2048 k (T <= 8) or 1024 k of its R rows; the MMA
+//    columns are the batch's tokens, so one accumulator per (row, token)
+//    collects all of a token's experts. B is p * h * 2^-sigma_t in fp16
+//    (sigma_t per token from max_j p_j max|h_j|), converted from fp32 h (loaded
+//    from L2 one stage ahead) by the warp that owns the block; n tiles with none
+//    of their tokens in a virtual expert are skipped. One cross-warp sum at the
 //    end, then y = acc * 2^sigma_t.
 // E2M1 codes go through the hardware cvt.rn.f16x2.e2m1x2 (exact); products are
 // f16 x f16 with fp32 accumulation. Lane (g, c) of an MMA takes the 4 code
