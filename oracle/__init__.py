@@ -82,6 +82,7 @@ def _L():
             lib.oracle_hadamard32_quant_i8.argtypes = [P, P, I, I, P, P, P, I]
             lib.oracle_quant_i8_row.argtypes = [P, I, P, P]
             lib.oracle_w8a8.argtypes = [P, P, I, I, I, P, I]
+            lib.oracle_w8a16.argtypes = [P, P, P, I, I, I, P, P, I]
             lib.oracle_w8a8.restype = I
             _lib = lib
     return _lib
@@ -344,6 +345,24 @@ def hadamard32_quant_i8(x, sign_bits, threads=0):
     _L().oracle_hadamard32_quant_i8(_ptr(xs), _ptr(sb), M, K, _ptr(q), _ptr(s), _ptr(z),
                                     threads)
     return q, s, z
+
+
+def w8a16(wq, scales, x, threads=0):
+    """Row-int8 GEMV: y[m][n] = sum_k s[n] q[n][k] x[m][k] in float64, plus
+    sum_k |w x| (the tolerance's scale). wq int8 [N][K], scales fp32 [N],
+    x bf16 bits [M][K] (or [K]). Returns (y [M][N], absdot [M][N])."""
+    wq = _np(wq, np.int8)
+    s = _np(scales, np.float32)
+    x = _np(x, np.uint16)
+    if x.ndim == 1:
+        x = x[None, :]
+    M, K = x.shape
+    N = wq.shape[0]
+    assert wq.shape == (N, K) and s.shape == (N,)
+    y = np.zeros((M, N), np.float64)
+    ad = np.zeros((M, N), np.float64)
+    _L().oracle_w8a16(_ptr(wq), _ptr(s), _ptr(x), M, N, K, _ptr(y), _ptr(ad), threads)
+    return y, ad
 
 
 def w8a8(a, w, threads=0):

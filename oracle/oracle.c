@@ -243,6 +243,32 @@ void oracle_hadamard32_quant_i8(const uint16_t *x, const uint32_t *sign_bits, in
 }
 
 /* ------------------------------------------------------------------------
+ * W8A16 row-int8 GEMV (K3, "Technical approach / compute": the packed int8
+ * output head, row-int8 weights with one scale per row, a weight-only
+ * quantized matmul): y[m][n] = sum_k (s[n] * q[n][k]) * x[m][k], q int8,
+ * s fp32, x bf16; absdot[m][n] = sum_k |w[n][k] * x[m][k]|.
+ * ---------------------------------------------------------------------- */
+void oracle_w8a16(const int8_t *wq, const float *scales, const uint16_t *x, int M, int N, int K,
+                  double *y, double *absdot, int nthreads) {
+    set_threads(nthreads);
+#pragma omp parallel for schedule(static)
+    for (int n = 0; n < N; ++n) {
+        const double s = (double)scales[n];
+        for (int m = 0; m < M; ++m) {
+            double acc = 0.0, aacc = 0.0;
+            for (int k = 0; k < K; ++k) {
+                const double w = s * (double)wq[(size_t)n * K + k];
+                const double xv = (double)bf16_to_float(x[(size_t)m * K + k]);
+                acc += w * xv;
+                aacc += fabs(w * xv);
+            }
+            y[(size_t)m * N + n] = acc;
+            if (absdot) absdot[(size_t)m * N + n] = aacc;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------
  * W8A8 int32 (UZU int8 matrix path): C[m][n] = sum_k a[m][k] * w[n][k],
  * accumulated in int64; returns 0 if every result fits in int32, else 1.
  * ---------------------------------------------------------------------- */

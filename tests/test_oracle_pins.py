@@ -9,6 +9,8 @@ Each group names the page passage the oracle function follows:
     "How it works" / "Technical approach / compute".
   * Hadamard + int8, W8A8: Uzu article, "How Uzu optimizes bytes and tokens
     per pass".
+  * W8A16 row-int8 GEMV: "Running Kimi K3 (2.8T) on one Apple Silicon Mac"
+    (Deltafin), "Technical approach / compute" (packed int8 output head).
 """
 import json
 import math
@@ -444,3 +446,56 @@ def test_w8a8_extremes_and_overflow_detection():
     a = np.full((1, 140000), 127, np.int8)
     with pytest.raises(OverflowError):
         oracle.w8a8(a, a)
+
+
+# ---------------------------------------------------------------- W8A16 row-int8 GEMV
+
+def test_w8a16_one_hot_selects_scaled_column():
+    # x = e_k: y[n] = s[n] * q[n][k] (catches a transposed operand or a lost scale)
+    rng = np.random.default_rng(5)
+    N, K = 7, 48
+    q = rng.integers(-128, 128, size=(N, K), dtype=np.int8)
+    s = np.array([0.5, 2.0, 0.25, 1.0, 3.0, 0.125, 8.0], np.float32)
+    for k in (0, 17, 47):
+        x = np.zeros(K, np.float32)
+        x[k] = 1.0
+        y, ad = oracle.w8a16(q, s, bf16_bits(x))
+        assert np.array_equal(y[0], s.astype(np.float64) * q[:, k])
+        assert np.array_equal(ad[0], np.abs(s.astype(np.float64) * q[:, k]))
+
+
+def test_w8a16_all_ones_codes_give_scaled_sum():
+    rng = np.random.default_rng(6)
+    N, K = 5, 64
+    x = rng.integers(-8, 9, size=K).astype(np.float32)  # integers: exact in bf16 and double
+    s = np.array([1.0, 0.5, -2.0, 4.0, 0.75], np.float32)
+    for code in (1, -1, 127, -128):
+        q = np.full((N, K), code, np.int8)
+        y, _ = oracle.w8a16(q, s, bf16_bits(x))
+        assert np.array_equal(y[0], s.astype(np.float64) * code * x.sum())
+
+
+def test_w8a16_agrees_with_w4a16_on_shared_cases():
+    # codes 0..15, scale representable in fp16, zero bias: both definitions coincide
+    rng = np.random.default_rng(7)
+    N, K = 6, 128
+    q = rng.integers(0, 16, size=(N, K))
+    s16 = np.array([0.5, 0.25, 1.5, 0.125, 2.0, 0.375], np.float16)
+    x = bf16_bits(rng.standard_normal(K))
+    y8, _ = oracle.w8a16(q.astype(np.int8), s16.astype(np.float32), x)
+    scales = np.repeat(s16[:, None], K // 64, axis=1).view(np.uint16)
+    biases = np.zeros_like(scales)
+    y4, _ = oracle.w4a16(pack_codes(q), scales, biases, x)
+    assert np.allclose(y8, y4, rtol=1e-12, atol=0)
+
+
+def test_w8a16_rows_of_x_are_independent():
+    rng = np.random.default_rng(8)
+    N, K, M = 4, 32, 3
+    q = rng.integers(-128, 128, size=(N, K), dtype=np.int8)
+    s = rng.random(N).astype(np.float32)
+    x = bf16_bits(rng.standard_normal((M, K)))
+    y, _ = oracle.w8a16(q, s, x)
+    for m in range(M):
+        ym, _ = oracle.w8a16(q, s, x[m])
+        assert np.array_equal(y[m], ym[0])
