@@ -320,6 +320,19 @@ def bench_single_gemv(q, dev, stream, l2_bytes):
     return {"us_per_call": t * 1e6, "GB_per_s": per / t / 1e9, "weight_copies_rotated": int(copies)}
 
 
+def bench_w8a16(q, dev, stream, hbm_peak):
+    """The row-int8 output head, 151936 x 4096 (622 MB of weights > L2)."""
+    N, K = 151936, 4096
+    wq, s = synth.w8_row_weights(N, K, seed=3, slot=1, device=dev)
+    x = synth.bf16_normal((K,), 3, 2, dev)
+    y = torch.empty(N, device=dev)
+    t, _ = time_graph(lambda: q.qgemv_w8a16(wq, s, x, y, stream=stream), 20, stream)
+    nbytes = N * K + 4 * N + 2 * K + 4 * N
+    del wq, s
+    return {"us_per_call": t * 1e6, "GB_per_s": nbytes / t / 1e9, "frac": nbytes / t / 1e9 / hbm_peak,
+            "algorithmic_bytes": nbytes}
+
+
 def bench_moe(q, dev, stream, T, moe_w):
     E, H, I, k = 384, 7168, 2048, 16
     x = synth.bf16_normal((T, H), 3, 0, dev)
@@ -369,6 +382,7 @@ def bench_w8a8(q, dev, stream, N, l2_bytes):
 # --------------------------------------------------------------------------- single cases (profiling)
 
 CASES = ["gemv_lm_head", "gemv_down", "gemv_q", "skinny16_gate_up", "skinny16_down", "moe_T1", "moe_T16",
+         "w8a16_lm_head",
          "w8a8_12288", "hadamard_16x4096", "gemv_group_4layers", "skinny16_group_4layers"]
 
 
@@ -416,6 +430,13 @@ def run_case(args):
         lg = synth.router_logits(T, E, 3, 1, dev)
         f = lambda: q.moe_mxfp4_expert_forward(x, lg, *w, top_k=k)  # noqa: E731
         nbytes = None
+    elif c == "w8a16_lm_head":
+        N, K = 151936, 4096
+        wq, s = synth.w8_row_weights(N, K, 3, 1, dev)
+        x = synth.bf16_normal((K,), 3, 2, dev)
+        y = torch.empty(N, device=dev)
+        f = lambda: q.qgemv_w8a16(wq, s, x, y)  # noqa: E731
+        nbytes = N * K + 8 * N + 2 * K
     elif c == "w8a8_12288":
         N, K = 12288, 4096
         a = torch.randint(-127, 128, (16, K), dtype=torch.int8, device=dev)
@@ -602,6 +623,7 @@ def main():
         del xs16, ys16, grp16
         extras["m1_stack_tokens_per_s"] = 1.0 / t_step
         extras["single_gemv_1024"] = bench_single_gemv(q, dev, stream, l2)
+        extras["w8a16_lm_head_151936x4096"] = bench_w8a16(q, dev, stream, hbm_peak)
         torch.cuda.empty_cache()
         E, H, I = 384, 7168, 2048
         with torch.cuda.stream(stream):

@@ -230,6 +230,24 @@ QG_API qg_status qgemm_w4a16_skinny_group_run(const qg_w4_skinny_group *group, v
 QG_API void qgemm_w4a16_skinny_group_destroy(qg_w4_skinny_group *group);
 
 /*
+ * qgemv_w8a16 -- y = W x for one activation row with row-int8 weights: the
+ * packed int8 output head of "Running Kimi K3 (2.8T) on one Apple Silicon Mac"
+ * (Deltafin), "Technical approach / compute" (the row-int8 checkpoint used
+ * directly by a weight-only quantized matmul).
+ *
+ *   wq         int8 [N][K], row-major, 16-byte aligned; any int8 code.
+ *   scales     fp32 [N]: scale s[n] of row n.
+ *   x_bf16     bf16 [K], 16-byte aligned.
+ *   y          fp32 [N] (output): y[n] = s[n] * sum_k q[n][k] * x[k].
+ *   K          multiple of 16, at most 65536; N >= 1.
+ *   Float results meet |y - y_ref| <= 2e-3 * sum_k |s q x| + 1e-5 against an
+ *   exact evaluation (products are exact; the sum is fp32).
+ * Errors: QG_ERR_INVALID_ARG (null pointer, bad N or K), QG_ERR_MISALIGNED.
+ */
+QG_API qg_status qgemv_w8a16(const int8_t *wq, const float *scales, const uint16_t *x_bf16, float *y,
+                             int N, int K, void *stream);
+
+/*
  * moe_mxfp4_expert_forward -- routed-expert MoE layer with MXFP4 experts
  * ("Running Kimi K3 ...", "How it works" and "Technical approach / compute").
  *

@@ -31,6 +31,7 @@ EXPORTS = [
     "moe_mxfp4_expert_forward_noalloc", "qg_moe_noalloc_max_bytes",
     "qgemv_w4a16_group_create", "qgemv_w4a16_group_run", "qgemv_w4a16_group_destroy",
     "qgemm_w4a16_skinny_group_create", "qgemm_w4a16_skinny_group_run", "qgemm_w4a16_skinny_group_destroy",
+    "qgemv_w8a16",
 ]
 
 
@@ -68,6 +69,8 @@ def lib() -> ctypes.CDLL:
         L.qg_version.restype = I
         L.qgemv_w4a16.restype = I
         L.qgemv_w4a16.argtypes = [P, P, P, P, P, I, I, I, P, Z, P]
+        L.qgemv_w8a16.restype = I
+        L.qgemv_w8a16.argtypes = [P, P, P, P, I, I, P]
         L.qg_gemv_workspace_size.restype = Z
         L.qg_gemv_workspace_size.argtypes = [I, I, I]
         L.qgemm_w4a16_skinny.restype = I
@@ -154,6 +157,18 @@ def qgemv_w4a16(wq, scales, biases, x, y=None, workspace=None, stream=None):
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().qgemv_w4a16(_p(wq), _p(scales), _p(biases), _p(x), _p(y), N, K, K // scales.shape[1],
                              _p(workspace), ws_bytes, _stream(stream)), "qgemv_w4a16")
+    return y
+
+
+def qgemv_w8a16(wq, scales, x, y=None, stream=None):
+    """y[n] = s[n] sum_k q[n][k] x[k]; wq int8 [N][K], scales fp32 [N],
+    x bf16 [K] -> y fp32 [N] (the row-int8 output head)."""
+    N, K = wq.shape
+    for t, b, n in ((wq, 1, "wq"), (scales, 4, "scales"), (x, 2, "x")):
+        _need(t, b, n)
+    if y is None:
+        y = torch.empty(N, device=wq.device, dtype=torch.float32)
+    _check(lib().qgemv_w8a16(_p(wq), _p(scales), _p(x), _p(y), N, K, _stream(stream)), "qgemv_w8a16")
     return y
 
 

@@ -137,6 +137,14 @@ qg_status qgemv_w4a16(const uint32_t* wq, const uint16_t* scales_f16, const uint
   return run_w4(wq, scales_f16, biases_f16, x_bf16, y, 1, N, K, workspace, ws_bytes, stream);
 }
 
+qg_status qgemv_w8a16(const int8_t* wq, const float* scales, const uint16_t* x_bf16, float* y, int N, int K,
+                      void* stream) {
+  if (!wq || !scales || !x_bf16 || !y) return QG_ERR_INVALID_ARG;
+  if (N < 1 || K < 16 || K % 16 || K > 65536) return QG_ERR_INVALID_ARG;
+  if (!aligned16(wq) || !aligned16(x_bf16)) return QG_ERR_MISALIGNED;
+  return from_cuda(qg::launch_w8a16_gemv(wq, scales, x_bf16, y, N, K, static_cast<cudaStream_t>(stream), g_pdl));
+}
+
 struct qg_w4_group {
   qg::GroupPlan plan;
 };

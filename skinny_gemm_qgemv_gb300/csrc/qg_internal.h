@@ -142,6 +142,10 @@ bool tmap_3d(CUtensorMap* tm, CUtensorMapDataType dt, const void* ptr, uint64_t 
              uint64_t chunks, uint64_t row_bytes, uint64_t chunk_bytes, uint32_t box_inner, uint32_t box_rows,
              uint32_t box_chunks);
 
+// W8A16 row-int8 GEMV (w8a16_gemv.cu)
+cudaError_t launch_w8a16_gemv(const int8_t* wq, const float* scales, const uint16_t* x, float* y, int N, int K,
+                              cudaStream_t stream, bool pdl);
+
 // MXFP4 MoE (moe_mxfp4.cu, moe_mx_mma.cu)
 constexpr int kMxTC = 8;                // pairs of one virtual expert: the N = 8 columns of one MMA
 constexpr int kMxVexpInts = 2 + kMxTC;  // virtual-expert table entry: expert, pair count, pairs

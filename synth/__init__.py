@@ -103,6 +103,25 @@ def w4_weights(N, K, seed, slot, device="cpu", group=64, std=0.02):
     return _chunked(N, K, std, seed, slot, device, lambda w: affine_w4_encode(w, group))
 
 
+def row_int8_encode(w: torch.Tensor):
+    """Row-int8 encoding of fp32 weights [N][K] (a row-int8 checkpoint):
+    s = max|w| / 127 per row (fp32), q = round-half-even(w / s) clamped to
+    [-127, 127]; an all-zero row gets s = 0 and codes 0.
+    Returns (q int8 [N][K], s fp32 [N])."""
+    w = w.float()
+    amax = w.abs().amax(dim=1)
+    s = amax / 127.0
+    safe = torch.where(s > 0, s, torch.ones_like(s))
+    q = torch.clamp(torch.round(w / safe[:, None]), -127, 127).to(torch.int8)
+    q = torch.where((s > 0)[:, None], q, torch.zeros_like(q))
+    return q, s
+
+
+def w8_row_weights(N, K, seed, slot, device="cpu", std=0.02):
+    """Weights ~ N(0, std) as row-int8 (see row_int8_encode)."""
+    return _chunked(N, K, std, seed, slot, device, row_int8_encode)
+
+
 # --------------------------------------------------------------------------
 # MXFP4: E2M1 codes (2 per byte, low nibble = even index), E8M0 per 32
 # --------------------------------------------------------------------------

@@ -64,6 +64,17 @@ def test_w4a16_validation(L):
     assert g(P(A), P(A), P(A), P(B + 2), P(A), 4, 16, 128, 64, None, 0, None) == 2
 
 
+def test_w8a16_validation(L):
+    f = L.qgemv_w8a16
+    assert f(None, P(A), P(A), P(A), 16, 128, None) == 1
+    assert f(P(A), P(A), P(A), P(A), 0, 128, None) == 1
+    assert f(P(A), P(A), P(A), P(A), 16, 100, None) == 1      # K % 16
+    assert f(P(A), P(A), P(A), P(A), 16, 8, None) == 1        # K < 16
+    assert f(P(A), P(A), P(A), P(A), 16, 65552, None) == 1    # K > 65536
+    assert f(P(A + 4), P(A), P(A), P(A), 16, 128, None) == 2  # weights misaligned
+    assert f(P(A), P(A), P(A + 2), P(A), 16, 128, None) == 2  # x misaligned
+
+
 def test_moe_validation(L):
     f = L.moe_mxfp4_expert_forward
     ptrs = [P(A)] * 8

@@ -192,6 +192,51 @@ def test_w8a8_extremes(q, N):
     assert np.array_equal(c.cpu().numpy(), oracle.w8a8(a, w))
 
 
+# ---------------------------------------------------------------- W8A16 row-int8 GEMV
+
+@pytest.mark.parametrize("N,K", [(1, 16), (3, 48), (1000, 4096), (4099, 1024), (257, 12288), (33, 65536)])
+def test_w8a16_vs_oracle(q, N, K):
+    wq, s = synth.w8_row_weights(N, K, seed=500 + N, slot=1)
+    x = synth.bf16_normal((K,), seed=500 + N, slot=2)
+    y = q.qgemv_w8a16(wq.to(DEV), s.to(DEV), x.to(DEV))
+    torch.cuda.synchronize()
+    ref, ad = oracle.w8a16(wq, s, x)
+    d = np.abs(y.cpu().double().numpy() - ref[0])
+    assert np.all(d <= oracle.tolerance(ad[0])), f"worst {np.max(d / oracle.tolerance(ad[0])):.3g}x"
+
+
+def test_w8a16_extremes_and_scales(q):
+    # full int8 range, tiny and large activations (the fp16 prescale), zero x
+    N, K = 96, 2048
+    g = torch.Generator().manual_seed(7)
+    wq = torch.randint(-128, 128, (N, K), generator=g, dtype=torch.int16).to(torch.int8)
+    wq[0] = -128
+    wq[1] = 127
+    s = torch.rand(N, generator=g) * 4 + 1e-3
+    for xscale in (1e-6, 1.0, 3e4):
+        x = (torch.randn(K, generator=g) * xscale).to(torch.bfloat16)
+        y = q.qgemv_w8a16(wq.to(DEV), s.to(DEV), x.view(torch.int16).to(DEV).view(torch.bfloat16))
+        torch.cuda.synchronize()
+        ref, ad = oracle.w8a16(wq, s, x)
+        d = np.abs(y.cpu().double().numpy() - ref[0])
+        assert np.all(d <= oracle.tolerance(ad[0]))
+    y = q.qgemv_w8a16(wq.to(DEV), s.to(DEV), torch.zeros(K, dtype=torch.bfloat16, device=DEV))
+    assert torch.count_nonzero(y).item() == 0
+
+
+def test_w8a16_full_size_lm_head(q):
+    # the int8 output head of the 9B-class decoder: 151936 x 4096
+    N, K = 151936, 4096
+    wq, s = synth.w8_row_weights(N, K, seed=3, slot=1, device=DEV)
+    x = synth.bf16_normal((K,), seed=3, slot=2, device=DEV)
+    y = q.qgemv_w8a16(wq, s, x)
+    torch.cuda.synchronize()
+    rows = np.concatenate([np.arange(0, 64), np.arange(N - 64, N), np.arange(1000, N, 4999)])
+    ref, ad = oracle.w8a16(wq[rows].cpu(), s[rows].cpu(), x.cpu())
+    d = np.abs(y.cpu().double().numpy()[rows] - ref[0])
+    assert np.all(d <= oracle.tolerance(ad[0]))
+
+
 # ---------------------------------------------------------------- MXFP4 MoE
 
 def moe_inputs(E, H, I, T, seed, device="cpu"):
