@@ -825,8 +825,10 @@ MxDnPlan plan_down(int T, int H, int I, int top_k, int nvmax, int sms) {
   p.MT = std::min(4, std::max(1, (H + 16 * sms - 1) / (16 * sms)));
   p.R = 16 * p.MT;
   p.grid = (H + p.R - 1) / p.R;
-  p.NT = T <= 8 ? 1 : 2;
-  p.BPW = (p.NT == 1 && I % 2048 == 0) ? 4 : (I % 1024 == 0 ? 2 : 1);
+  p.NT = T <= 8 ? 1 : (T <= 16 ? 2 : 4);
+  // more token columns, fewer blocks per warp (registers): 2048 k stages at
+  // NT = 1, 1024 at NT = 2, 512 at NT = 4 (as far as I allows)
+  p.BPW = p.NT == 4 ? 1 : ((p.NT == 1 && I % 2048 == 0) ? 4 : (I % 1024 == 0 ? 2 : 1));
   p.o_s = 256u * p.R * p.BPW;  // codes: [2 BPW chunks][R rows][128 B], then scales [R][16 BPW]
   p.stage_bytes = (272u * p.R * p.BPW + 1023u) & ~1023u;
   const size_t fixed = 1024 + 4 * 8 * p.NT + 4 * (size_t)nvmax + 4 * (size_t)T * top_k +
@@ -874,7 +876,7 @@ cudaError_t launch_gateup(const CUtensorMap* tm, const MxGuArgs& ga, int grid, s
 }  // namespace
 
 bool moe_mx_mma_ok(int T, int H, int I, int E, int top_k) {
-  if (T < 1 || T > 16 || E < 1 || E > 1024 || top_k < 1 || top_k > 32 || top_k > E) return false;
+  if (T < 1 || T > 32 || E < 1 || E > 1024 || top_k < 1 || top_k > 32 || top_k > E) return false;
   if (H < 512 || I < 512 || H % 512 || I % 512) return false;
   const MxDnPlan pd = plan_down(T, H, I, top_k, moe_nvirt_max(T, E, top_k), device_sm_count());
   if (pd.ST < 2 || (size_t)kMxWarps * pd.MT * pd.NT * 512 > (size_t)pd.ST * pd.stage_bytes) return false;
@@ -927,8 +929,10 @@ cudaError_t launch_moe_mx_mma(const uint16_t* x, const float* logits, const uint
     return pd.BPW == 4   ? launch_down_mt<1, 4>(tm_dq, tm_ds, da, pd, stream, pdl)
            : pd.BPW == 2 ? launch_down_mt<1, 2>(tm_dq, tm_ds, da, pd, stream, pdl)
                          : launch_down_mt<1, 1>(tm_dq, tm_ds, da, pd, stream, pdl);
-  return pd.BPW == 2 ? launch_down_mt<2, 2>(tm_dq, tm_ds, da, pd, stream, pdl)
-                     : launch_down_mt<2, 1>(tm_dq, tm_ds, da, pd, stream, pdl);
+  if (pd.NT == 2)
+    return pd.BPW == 2 ? launch_down_mt<2, 2>(tm_dq, tm_ds, da, pd, stream, pdl)
+                       : launch_down_mt<2, 1>(tm_dq, tm_ds, da, pd, stream, pdl);
+  return launch_down_mt<4, 1>(tm_dq, tm_ds, da, pd, stream, pdl);
 }
 
 }  // namespace qg

@@ -328,12 +328,12 @@ def test_moe_shared_experts_split_into_virtual_experts(q):
     assert (idx == torch.tensor([0, 1, 2], dtype=idx.dtype, device=idx.device)).all()
 
 
-@pytest.mark.parametrize("T", [1, 16])
+@pytest.mark.parametrize("T", [1, 16, 24])
 def test_moe_full_size(q, T):
     # hidden 7168, intermediate 2048, 384 experts, top-16; tokens sampled
     E, H, I, k = 384, 7168, 2048, 16
     x, lg, w = moe_inputs(E, H, I, T, seed=3, device=DEV)
-    check_moe(q, x, lg, w, k, tokens=[0] if T == 1 else [0, 7, 15])
+    check_moe(q, x, lg, w, k, tokens=[0] if T == 1 else [0, 7, T - 1])
 
 
 # ---------------------------------------------------------------- grouped M = 1 GEMV
