@@ -94,7 +94,10 @@ QG_API int qg_version(void);
  *   biases_f16 fp16 [N][K/group_size]: bias b of the same group.
  *   x_bf16     bf16 [K].
  *   y          fp32 [N] (output): y[n] = sum_k (s * q[n][k] + b) * x[k].
- *   group_size 64 (other sizes return QG_ERR_UNSUPPORTED).
+ *   group_size 32, 64 or 128 (other values: QG_ERR_INVALID_ARG). 64 runs on the
+ *              fast kernels; 32 and 128 (the other group sizes of the affine
+ *              format, "MLX Runner ...") run on a generic one-warp-per-row
+ *              kernel: correct, not tuned.
  *   K          multiple of group_size; N >= 1.
  *   workspace  may be NULL when ws_bytes == 0; qg_gemv_workspace_size()
  *              gives the size needed (currently 0 for every shape).
@@ -121,7 +124,8 @@ QG_API size_t qg_gemv_workspace_size(int N, int K, int group_size);
  *                    aligned device memory of the current device; N >= 1;
  *                    K a multiple of 2048 and at most 16384 (other K return
  *                    QG_ERR_UNSUPPORTED).
- *   qgemv_w4a16_group_create  validates the count descriptors (group_size 64),
+ *   qgemv_w4a16_group_create  validates the count descriptors (group_size 64;
+ *                             32 and 128 return QG_ERR_UNSUPPORTED),
  *                    splits the tiles of all projections into one range per
  *                    CTA with equal bytes, and copies that plan to device
  *                    memory it allocates (cudaMalloc, synchronous copies).
@@ -195,7 +199,8 @@ QG_API size_t qg_skinny_workspace_size(int M, int N, int K, int group_size);
  *                    17..32 (other shapes, and mixed classes, return
  *                    QG_ERR_UNSUPPORTED).
  *   qgemm_w4a16_skinny_group_create  validates the count descriptors
- *                    (group_size 64), encodes their TMA descriptors, splits
+ *                    (group_size 64; 32 and 128 return QG_ERR_UNSUPPORTED),
+ *                    encodes their TMA descriptors, splits
  *                    the row tiles of all projections into one contiguous
  *                    range per SM with equal work, and copies that plan to
  *                    device memory it allocates (cudaMalloc, synchronous

@@ -102,7 +102,7 @@ static qg_status check_w4(const uint32_t* wq, const uint16_t* s, const uint16_t*
                           const float* y, int M, int N, int K, int group) {
   if (!wq || !s || !b || !x || !y) return QG_ERR_INVALID_ARG;
   if (M < 1 || M > 32 || N < 1 || K < 1) return QG_ERR_INVALID_ARG;
-  if (group != 64) return group == 32 || group == 128 ? QG_ERR_UNSUPPORTED : QG_ERR_INVALID_ARG;
+  if (group != 32 && group != 64 && group != 128) return QG_ERR_INVALID_ARG;
   if (K % group != 0) return QG_ERR_INVALID_ARG;
   if ((long long)N * (K / 8) >= (1LL << 40)) return QG_ERR_INVALID_ARG;
   if (!aligned16(wq) || !aligned16(s) || !aligned16(b) || !aligned16(x) || !aligned16(y)) return QG_ERR_MISALIGNED;
@@ -110,10 +110,13 @@ static qg_status check_w4(const uint32_t* wq, const uint16_t* s, const uint16_t*
 }
 
 static qg_status run_w4(const uint32_t* wq, const uint16_t* s, const uint16_t* b, const uint16_t* x, float* y,
-                        int M, int N, int K, void* ws, size_t ws_bytes, void* stream) {
+                        int M, int N, int K, int group, void* ws, size_t ws_bytes, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (qg::gemv_fast_path_ok(M, N, K)) {
+  if (group != 64) {
+    // groups of 32 or 128: the generic kernel (the fast paths fold per 64-code group)
+    e = qg::launch_w4a16_generic(wq, s, b, x, y, M, N, K, group, st, g_pdl);
+  } else if (qg::gemv_fast_path_ok(M, N, K)) {
     uint32_t* err = err_word();
     if (!err) return QG_ERR_CUDA;
     e = qg::launch_w4a16_fast(wq, s, b, x, y, M, N, K, err, st, g_pdl);
@@ -122,7 +125,7 @@ static qg_status run_w4(const uint32_t* wq, const uint16_t* s, const uint16_t* b
     if (!err) return QG_ERR_CUDA;
     e = qg::launch_w4a16_tc(wq, s, b, x, y, M, N, K, ws, ws_bytes, err, st, g_pdl);
   } else {
-    e = qg::launch_w4a16_generic(wq, s, b, x, y, M, N, K, st, g_pdl);
+    e = qg::launch_w4a16_generic(wq, s, b, x, y, M, N, K, 64, st, g_pdl);
   }
   return from_cuda(e);
 }
@@ -134,7 +137,7 @@ qg_status qgemv_w4a16(const uint32_t* wq, const uint16_t* scales_f16, const uint
   if (st != QG_OK) return st;
   if (ws_bytes < qg_gemv_workspace_size(N, K, group_size)) return QG_ERR_WORKSPACE;
   if (ws_bytes && !workspace) return QG_ERR_INVALID_ARG;
-  return run_w4(wq, scales_f16, biases_f16, x_bf16, y, 1, N, K, workspace, ws_bytes, stream);
+  return run_w4(wq, scales_f16, biases_f16, x_bf16, y, 1, N, K, group_size, workspace, ws_bytes, stream);
 }
 
 qg_status qgemv_w8a16(const int8_t* wq, const float* scales, const uint16_t* x_bf16, float* y, int N, int K,
@@ -152,6 +155,7 @@ struct qg_w4_group {
 qg_status qgemv_w4a16_group_create(const qg_w4_gemv_desc* descs, int count, int group_size, qg_w4_group** group) {
   if (!descs || !group || count < 1) return QG_ERR_INVALID_ARG;
   std::vector<qg::GroupGemv> list(count);
+  if (group_size == 32 || group_size == 128) return QG_ERR_UNSUPPORTED;  // grouped launches: g64 only
   for (int i = 0; i < count; ++i) {
     const qg_w4_gemv_desc& d = descs[i];
     qg_status st = check_w4(d.wq, d.scales_f16, d.biases_f16, d.x_bf16, d.y, 1, d.N, d.K, group_size);
@@ -198,7 +202,7 @@ qg_status qgemm_w4a16_skinny(const uint32_t* wq, const uint16_t* scales_f16, con
   if (ws_bytes < qg_skinny_workspace_size(M, N, K, group_size)) return QG_ERR_WORKSPACE;
   if (ws_bytes && !workspace) return QG_ERR_INVALID_ARG;
   if (workspace && !aligned16(workspace)) return QG_ERR_MISALIGNED;
-  return run_w4(wq, scales_f16, biases_f16, x_bf16, y, M, N, K, workspace, ws_bytes, stream);
+  return run_w4(wq, scales_f16, biases_f16, x_bf16, y, M, N, K, group_size, workspace, ws_bytes, stream);
 }
 
 struct qg_w4_skinny_group {
@@ -208,6 +212,7 @@ struct qg_w4_skinny_group {
 qg_status qgemm_w4a16_skinny_group_create(const qg_w4_gemm_desc* descs, int count, int group_size,
                                           qg_w4_skinny_group** group) {
   if (!descs || !group || count < 1) return QG_ERR_INVALID_ARG;
+  if (group_size == 32 || group_size == 128) return QG_ERR_UNSUPPORTED;  // grouped launches: g64 only
   std::vector<qg::TcGroupItem> list(count);
   for (int i = 0; i < count; ++i) {
     const qg_w4_gemm_desc& d = descs[i];

@@ -92,8 +92,9 @@ int tc_group_check(const TcGroupItem* list, int n);
 cudaError_t tc_group_plan_build(const TcGroupItem* list, int n, int sms, TcGroupPlan* out);
 void tc_group_plan_free(TcGroupPlan* p);
 cudaError_t tc_group_launch(const TcGroupPlan& p, uint32_t* err, cudaStream_t stream, bool pdl);
+// any M <= 32, group 32, 64 or 128 (one warp per row)
 cudaError_t launch_w4a16_generic(const uint32_t* wq, const uint16_t* sc, const uint16_t* bi, const uint16_t* x,
-                                 float* y, int M, int N, int K, cudaStream_t stream, bool pdl);
+                                 float* y, int M, int N, int K, int group, cudaStream_t stream, bool pdl);
 
 // Hadamard + int8 (hadamard_i8.cu)
 cudaError_t launch_hadamard32_quant_i8(const uint16_t* x, const uint32_t* sign_bits, int8_t* q, float* scale,

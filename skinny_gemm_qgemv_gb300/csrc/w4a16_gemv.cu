@@ -281,18 +281,18 @@ __global__ void __launch_bounds__(256) w4a16_generic_kernel(const uint32_t* __re
                                                             const uint16_t* __restrict__ scales,
                                                             const uint16_t* __restrict__ biases,
                                                             const uint16_t* __restrict__ x, float* __restrict__ y,
-                                                            int M, int N, int K) {
+                                                            int M, int N, int K, int lg_group) {
   pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = blockIdx.x * 8 + warp;
   if (n >= N) return;
-  const int words = K / 8, groups = K / 64;
+  const int words = K / 8, groups = K >> lg_group;  // group = 2^lg_group codes (32, 64 or 128)
   float acc[MMAX];
 #pragma unroll
   for (int m = 0; m < MMAX; ++m) acc[m] = 0.f;
   for (int j = lane; j < words; j += 32) {
     const uint32_t w = wq[(size_t)n * words + j];
-    const int g = j / 8;
+    const int g = (8 * j) >> lg_group;
     const float s = f16_bits_to_f32(scales[(size_t)n * groups + g]);
     const float b = f16_bits_to_f32(biases[(size_t)n * groups + g]);
 #pragma unroll
@@ -415,14 +415,19 @@ cudaError_t launch_w4a16_fast(const uint32_t* wq, const uint16_t* sc, const uint
 }
 
 cudaError_t launch_w4a16_generic(const uint32_t* wq, const uint16_t* sc, const uint16_t* bi, const uint16_t* x,
-                                 float* y, int M, int N, int K, cudaStream_t stream, bool pdl) {
+                                 float* y, int M, int N, int K, int group, cudaStream_t stream, bool pdl) {
+  if (group != 32 && group != 64 && group != 128) return cudaErrorInvalidValue;
+  const int lg = group == 32 ? 5 : (group == 64 ? 6 : 7);
   dim3 grid((N + 7) / 8), block(256);
-  if (M <= 1) return launch_kernel(w4a16_generic_kernel<1>, grid, block, 0, stream, pdl, wq, sc, bi, x, y, M, N, K);
-  if (M <= 4) return launch_kernel(w4a16_generic_kernel<4>, grid, block, 0, stream, pdl, wq, sc, bi, x, y, M, N, K);
-  if (M <= 8) return launch_kernel(w4a16_generic_kernel<8>, grid, block, 0, stream, pdl, wq, sc, bi, x, y, M, N, K);
+  if (M <= 1)
+    return launch_kernel(w4a16_generic_kernel<1>, grid, block, 0, stream, pdl, wq, sc, bi, x, y, M, N, K, lg);
+  if (M <= 4)
+    return launch_kernel(w4a16_generic_kernel<4>, grid, block, 0, stream, pdl, wq, sc, bi, x, y, M, N, K, lg);
+  if (M <= 8)
+    return launch_kernel(w4a16_generic_kernel<8>, grid, block, 0, stream, pdl, wq, sc, bi, x, y, M, N, K, lg);
   if (M <= 16)
-    return launch_kernel(w4a16_generic_kernel<16>, grid, block, 0, stream, pdl, wq, sc, bi, x, y, M, N, K);
-  return launch_kernel(w4a16_generic_kernel<32>, grid, block, 0, stream, pdl, wq, sc, bi, x, y, M, N, K);
+    return launch_kernel(w4a16_generic_kernel<16>, grid, block, 0, stream, pdl, wq, sc, bi, x, y, M, N, K, lg);
+  return launch_kernel(w4a16_generic_kernel<32>, grid, block, 0, stream, pdl, wq, sc, bi, x, y, M, N, K, lg);
 }
 
 }  // namespace qg

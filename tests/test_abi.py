@@ -55,7 +55,9 @@ def test_w4a16_validation(L):
     assert f(None, P(A), P(A), P(A), P(A), 16, 128, 64, None, 0, None) == 1
     assert f(P(A), P(A), P(A), P(A), P(A), 0, 128, 64, None, 0, None) == 1
     assert f(P(A), P(A), P(A), P(A), P(A), 16, 100, 64, None, 0, None) == 1     # K % 64
-    assert f(P(A), P(A), P(A), P(A), P(A), 16, 128, 32, None, 0, None) == 3     # group 32 later
+    assert f(P(A), P(A), P(A), P(A), P(A), 16, 112, 32, None, 0, None) == 1     # K % 32
+    assert f(P(A), P(A), P(A), P(A), P(A), 16, 192, 128, None, 0, None) == 1    # K % 128
+    assert f(P(A), P(A), P(A), P(A), P(A), 16, 256, 256, None, 0, None) == 1    # group 256
     assert f(P(A), P(A), P(A), P(A), P(A), 16, 128, 48, None, 0, None) == 1
     assert f(P(A + 4), P(A), P(A), P(A), P(A), 16, 128, 64, None, 0, None) == 2
     g = L.qgemm_w4a16_skinny

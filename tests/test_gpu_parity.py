@@ -192,6 +192,23 @@ def test_w8a8_extremes(q, N):
     assert np.array_equal(c.cpu().numpy(), oracle.w8a8(a, w))
 
 
+# ---------------------------------------------------------------- other affine group sizes
+
+@pytest.mark.parametrize("group", [32, 128])
+@pytest.mark.parametrize("M,N,K", [(1, 300, 1024), (1, 77, 4096), (5, 130, 2048), (32, 64, 512)])
+def test_w4a16_group_sizes_32_128(q, group, M, N, K):
+    wq, s, b = synth.w4_weights(N, K, seed=600 + M, slot=group, group=group)
+    x = synth.bf16_normal((M, K), seed=600 + M, slot=1)
+    if M == 1:
+        y = q.qgemv_w4a16(wq.to(DEV), s.to(DEV), b.to(DEV), x[0].to(DEV))[None, :]
+    else:
+        y = q.qgemm_w4a16_skinny(wq.to(DEV), s.to(DEV), b.to(DEV), x.to(DEV))
+    torch.cuda.synchronize()
+    ref, ad = oracle.w4a16(wq, s, b, x, group=group)
+    d = np.abs(y.cpu().double().numpy() - ref)
+    assert np.all(d <= oracle.tolerance(ad)), f"worst {np.max(d / oracle.tolerance(ad)):.3g}x"
+
+
 # ---------------------------------------------------------------- W8A16 row-int8 GEMV
 
 @pytest.mark.parametrize("N,K", [(1, 16), (3, 48), (1000, 4096), (4099, 1024), (257, 12288), (33, 65536)])

@@ -132,6 +132,32 @@ def test_w4a16_zero_codes_reduce_to_bias_times_group_sums():
     assert np.allclose(y, exp, rtol=1e-13, atol=1e-13)
 
 
+@pytest.mark.parametrize("group", [32, 128])
+def test_w4a16_other_group_sizes_zero_codes_and_one_hot(group):
+    # zero codes: y = sum_g b_g * (sum of x over group g); one-hot x: the
+    # dequantized column with the scale and bias of group k // group
+    rng = np.random.default_rng(4)
+    N, K = 5, 512
+    G = K // group
+    words = np.zeros((N, K // 8), np.uint32)
+    s = f16_bits(rng.normal(size=(N, G)) * 0.01)
+    b = f16_bits(rng.normal(size=(N, G)) * 0.05)
+    x = bf16_bits(rng.normal(size=(2, K)))
+    y, _ = oracle.w4a16(words, s, b, x, group=group)
+    xf = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+    exp = xf.reshape(2, G, group).sum(axis=2) @ b.view(np.float16).astype(np.float64).T
+    assert np.allclose(y, exp, rtol=1e-13, atol=1e-13)
+    q = rng.integers(0, 16, size=(N, K))
+    wq = pack_codes(q)
+    for k in (0, group - 1, group, K - 1):
+        xh = np.zeros((1, K), np.uint16)
+        xh[0, k] = 0x3F80  # 1.0
+        y1, _ = oracle.w4a16(wq, s, b, xh, group=group)
+        col = s.view(np.float16).astype(np.float64)[:, k // group] * q[:, k] + \
+            b.view(np.float16).astype(np.float64)[:, k // group]
+        assert np.array_equal(y1[0], col)
+
+
 def test_w4a16_integer_inputs_exact():
     # s = 1, b = 0 and small integer x: y is an exact integer sum
     rng = np.random.default_rng(5)
