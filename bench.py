@@ -63,6 +63,14 @@ def dist_info():
     return rank, world, local
 
 
+def max_over_ranks(t, world, device):
+    """The job's step time: the largest per-rank time over all ranks."""
+    tmax = torch.tensor([float(t)], device=device, dtype=torch.float64)
+    if world > 1:
+        torch.distributed.all_reduce(tmax, op=torch.distributed.ReduceOp.MAX)
+    return float(tmax.item())
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -531,10 +539,7 @@ def main():
     t_step = e0.elapsed_time(e1) * 1e-3 / args.steps
     time.sleep(0.25)
     clocks.stop()
-    tmax = torch.tensor([t_step], device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(tmax, op=torch.distributed.ReduceOp.MAX)
-    t_step = float(tmax.item())
+    t_step = max_over_ranks(t_step, world, dev)
     value = world * step_bytes / t_step / 1e9
 
     # ---------------- the same step as 217 launches (one per projection) in one graph
