@@ -192,31 +192,6 @@ __device__ __forceinline__ float e8m0_to_f32(uint32_t e) {
   return e ? __uint_as_float(e << 23) : __uint_as_float(0x00400000u);
 }
 
-// Mixed-precision FMA: acc + a * b with a, b the low/high bf16 halves of
-// 32-bit registers, accumulated in fp32 (one rounding, sm_100+).
-__device__ __forceinline__ float fma_bf16_lo_lo(uint32_t a, uint32_t b, float acc) {
-  asm("{.reg .b16 al, ah, bl, bh; mov.b32 {al, ah}, %1; mov.b32 {bl, bh}, %2;\n\t"
-      "fma.rn.f32.bf16 %0, al, bl, %0;}"
-      : "+f"(acc)
-      : "r"(a), "r"(b));
-  return acc;
-}
-__device__ __forceinline__ float fma_bf16_hi_hi(uint32_t a, uint32_t b, float acc) {
-  asm("{.reg .b16 al, ah, bl, bh; mov.b32 {al, ah}, %1; mov.b32 {bl, bh}, %2;\n\t"
-      "fma.rn.f32.bf16 %0, ah, bh, %0;}"
-      : "+f"(acc)
-      : "r"(a), "r"(b));
-  return acc;
-}
-// acc += a.lo * b.lo + a.hi * b.hi (bf16 x bf16 products, two fp32 roundings),
-// both halves unpacked in one block.
-__device__ __forceinline__ float fma_bf16x2_dot(uint32_t a, uint32_t b, float acc) {
-  asm("{.reg .b16 al, ah, bl, bh; mov.b32 {al, ah}, %1; mov.b32 {bl, bh}, %2;\n\t"
-      "fma.rn.f32.bf16 %0, al, bl, %0;\n\tfma.rn.f32.bf16 %0, ah, bh, %0;}"
-      : "+f"(acc)
-      : "r"(a), "r"(b));
-  return acc;
-}
 __device__ __forceinline__ float fma_f16_lo_lo(uint32_t a, uint32_t b, float acc) {
   asm("{.reg .b16 al, ah, bl, bh; mov.b32 {al, ah}, %1; mov.b32 {bl, bh}, %2;\n\t"
       "fma.rn.f32.f16 %0, al, bl, %0;}"
@@ -245,18 +220,6 @@ __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t word) {
   else
     asm("{.reg .b8 b0, b1, b2, b3; mov.b32 {b0, b1, b2, b3}, %1; cvt.rn.f16x2.e2m1x2 %0, b3;}" : "=r"(r) : "r"(word));
   return r;
-}
-
-// A uint32 word of eight 4-bit codes (code i in bits 4i..4i+3) -> four bf16x2
-// registers holding 128 + code (exact in bf16: 0x4300 is 128.0 with an ulp of
-// 1). Register j holds codes j (low half) and j+4 (high half).
-__device__ __forceinline__ void nib8_to_bf16x2_biased(uint32_t w, uint32_t (&o)[4]) {
-  constexpr uint32_t kMask = 0x000F000Fu, kMagic = 0x43004300u;
-  uint32_t s1 = w >> 4, s2 = w >> 8, s3 = w >> 12;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(o[0]) : "r"(w), "r"(kMask), "r"(kMagic));
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(o[1]) : "r"(s1), "r"(kMask), "r"(kMagic));
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(o[2]) : "r"(s2), "r"(kMask), "r"(kMagic));
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(o[3]) : "r"(s3), "r"(kMask), "r"(kMagic));
 }
 
 // Two fp32 lanes in one 64-bit register, for the paired fp32 FMA (fma.rn.f32x2).
