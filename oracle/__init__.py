@@ -83,6 +83,7 @@ def _L():
             lib.oracle_quant_i8_row.argtypes = [P, I, P, P]
             lib.oracle_w8a8.argtypes = [P, P, I, I, I, P, I]
             lib.oracle_w8a16.argtypes = [P, P, P, I, I, I, P, P, I]
+            lib.oracle_affine.argtypes = [P, I, P, P, P, I, I, I, I, P, P, I]
             lib.oracle_w8a8.restype = I
             _lib = lib
     return _lib
@@ -173,6 +174,28 @@ def w4a16_rows(wq, scales, biases, x, rows, group=64, threads=0, row_base=0):
     ad = np.zeros((M, len(rows)), np.float64)
     _L().oracle_w4a16_rows(_ptr(wq), _ptr(s), _ptr(b), _ptr(x), M, K, group,
                            _ptr(rows), len(rows), int(row_base), _ptr(y), _ptr(ad), threads)
+    return y, ad
+
+
+def affine(wq, bits, scales, biases, x, group=64, threads=0):
+    """Affine quantized matvec at 2, 3, 4, 5, 6 or 8 bits: y[m][n] = sum_k
+    (s q + b) x[m][k] in float64 plus sum_k |w x|. wq uint32 [N][K*bits/32]
+    (each row one little-endian bit stream of K codes), scales/biases fp16
+    bits [N][K/group], x bf16 bits [M][K] (or [K])."""
+    assert bits in (2, 3, 4, 5, 6, 8) and group in (32, 64, 128)
+    wq = _np(wq, np.uint32)
+    s = _np(scales, np.uint16)
+    b = _np(biases, np.uint16)
+    x = _np(x, np.uint16)
+    if x.ndim == 1:
+        x = x[None, :]
+    M, K = x.shape
+    N = wq.shape[0]
+    assert K % 32 == 0 and K % group == 0
+    assert wq.shape == (N, K * bits // 32) and s.shape == (N, K // group) and b.shape == s.shape
+    y = np.zeros((M, N), np.float64)
+    ad = np.zeros((M, N), np.float64)
+    _L().oracle_affine(_ptr(wq), bits, _ptr(s), _ptr(b), _ptr(x), M, N, K, group, _ptr(y), _ptr(ad), threads)
     return y, ad
 
 

@@ -103,6 +103,45 @@ void oracle_w4a16(const uint32_t *wq, const uint16_t *scales, const uint16_t *bi
     }
 }
 
+/* ------------------------------------------------------------------------
+ * Affine quantization at any of the widths MLXR lists (2, 3, 4, 5, 6 or 8
+ * bits; groups of 32, 64 or 128): weight = scale x code + bias. The codes of
+ * a row form one little-endian bit stream: code k occupies bits
+ * [bits*k, bits*k + bits) of the row, bit j of the stream being bit j % 32 of
+ * word j / 32 (for 4 bits this is the W4A16 layout above). K is a multiple
+ * of 32 and of the group, so every row is a whole number of words
+ * (K * bits / 32). y and absdot as in oracle_w4a16.
+ * ---------------------------------------------------------------------- */
+void oracle_affine(const uint32_t *wq, int bits, const uint16_t *scales, const uint16_t *biases,
+                   const uint16_t *x, int M, int N, int K, int group, double *y, double *absdot,
+                   int nthreads) {
+    set_threads(nthreads);
+    const size_t words = (size_t)K * bits / 32;
+    const int groups = K / group;
+    const uint32_t mask = (1u << bits) - 1u;
+#pragma omp parallel for schedule(static)
+    for (int n = 0; n < N; ++n) {
+        const uint32_t *row = wq + (size_t)n * words;
+        for (int m = 0; m < M; ++m) {
+            double acc = 0.0, aacc = 0.0;
+            for (int k = 0; k < K; ++k) {
+                const size_t bit = (size_t)bits * k;
+                uint64_t two = row[bit / 32];
+                if (bit / 32 + 1 < words) two |= (uint64_t)row[bit / 32 + 1] << 32;
+                const int q = (int)((two >> (bit % 32)) & mask);
+                const double s = oracle_f16_to_double(scales[(size_t)n * groups + k / group]);
+                const double b = oracle_f16_to_double(biases[(size_t)n * groups + k / group]);
+                const double w = s * q + b;
+                const double xv = (double)bf16_to_float(x[(size_t)m * K + k]);
+                acc += w * xv;
+                aacc += fabs(w * xv);
+            }
+            y[(size_t)m * N + n] = acc;
+            if (absdot) absdot[(size_t)m * N + n] = aacc;
+        }
+    }
+}
+
 /* Same definition for a list of rows only (sampled checks at full size). */
 void oracle_w4a16_rows(const uint32_t *wq, const uint16_t *scales, const uint16_t *biases,
                        const uint16_t *x, int M, int K, int group,

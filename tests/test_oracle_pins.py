@@ -525,3 +525,63 @@ def test_w8a16_rows_of_x_are_independent():
     for m in range(M):
         ym, _ = oracle.w8a16(q, s, x[m])
         assert np.array_equal(y[m], ym[0])
+
+
+# ---------------------------------------------------------------- affine 2/3/4/5/6/8 bits
+
+def pack_bitstream(q, bits):
+    """codes [N][K] -> uint32 [N][K*bits/32]: each row one little-endian bit
+    stream (numpy.packbits with little bit order, then little-endian words)."""
+    q = np.asarray(q, dtype=np.uint64)
+    N, K = q.shape
+    bitarr = ((q[:, :, None] >> np.arange(bits, dtype=np.uint64)) & np.uint64(1)).astype(np.uint8)
+    by = np.packbits(bitarr.reshape(N, K * bits), axis=1, bitorder="little")
+    return np.ascontiguousarray(by).view("<u4").astype(np.uint32)
+
+
+@pytest.mark.parametrize("bits", [2, 3, 5, 6, 8])
+@pytest.mark.parametrize("group", [32, 128])
+def test_affine_one_hot_returns_dequantized_column(bits, group):
+    rng = np.random.default_rng(bits * 10 + group)
+    N, K = 6, 256
+    q = rng.integers(0, 1 << bits, size=(N, K))
+    wq = pack_bitstream(q, bits)
+    s = f16_bits(rng.normal(size=(N, K // group)) * 0.01)
+    b = f16_bits(rng.normal(size=(N, K // group)) * 0.05)
+    sf = s.view(np.float16).astype(np.float64)
+    bf = b.view(np.float16).astype(np.float64)
+    for k in (0, 1, 10, 31, 32, 100, 255):  # codes that straddle word boundaries for 3, 5, 6 bits
+        x = np.zeros((1, K), np.uint16)
+        x[0, k] = 0x3F80
+        y, _ = oracle.affine(wq, bits, s, b, x, group=group)
+        assert np.array_equal(y[0], sf[:, k // group] * q[:, k] + bf[:, k // group])
+
+
+@pytest.mark.parametrize("bits", [2, 3, 5, 6, 8])
+def test_affine_constant_codes_closed_form(bits):
+    rng = np.random.default_rng(40 + bits)
+    N, K, group = 3, 512, 64
+    x = bf16_bits(rng.integers(-4, 5, size=(2, K)).astype(np.float32))  # small integers: exact
+    xf = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+    gsum = xf.reshape(2, K // group, group).sum(axis=2)
+    s = f16_bits(np.full((N, K // group), 0.5))
+    b = f16_bits(np.full((N, K // group), -0.25))
+    for code in (0, (1 << bits) - 1):
+        wq = pack_bitstream(np.full((N, K), code), bits)
+        y, _ = oracle.affine(wq, bits, s, b, x, group=group)
+        exp = (0.5 * code - 0.25) * gsum.sum(axis=1)
+        assert np.array_equal(y, np.repeat(exp[:, None], N, axis=1))
+
+
+@pytest.mark.parametrize("group", [32, 64, 128])
+def test_affine_four_bits_is_the_w4a16_definition(group):
+    rng = np.random.default_rng(90 + group)
+    N, K = 5, 512
+    q = rng.integers(0, 16, size=(N, K))
+    s = f16_bits(rng.normal(size=(N, K // group)) * 0.01)
+    b = f16_bits(rng.normal(size=(N, K // group)) * 0.05)
+    x = bf16_bits(rng.normal(size=(3, K)))
+    ya, _ = oracle.affine(pack_bitstream(q, 4), 4, s, b, x, group=group)
+    y4, _ = oracle.w4a16(pack_codes(q), s, b, x, group=group)
+    assert np.array_equal(pack_bitstream(q, 4), pack_codes(q))
+    assert np.allclose(ya, y4, rtol=1e-14, atol=1e-14)
