@@ -235,6 +235,30 @@ QG_API qg_status qgemm_w4a16_skinny_group_run(const qg_w4_skinny_group *group, v
 QG_API void qgemm_w4a16_skinny_group_destroy(qg_w4_skinny_group *group);
 
 /*
+ * qgemm_affine -- Y = X W^T for 1..32 activation rows with affine weights at
+ * any width of the format: "MLX Runner ...", "Architecture: one command buffer
+ * per token" (weight = scale x code + bias at 2, 3, 4, 5, 6 or 8 bits, groups
+ * of 32, 64 or 128; the codes are multiplied directly).
+ *
+ *   wq         uint32 [N][K*bits/32]: the codes of row n as one little-endian
+ *              bit stream, code k in bits [bits*k, bits*k + bits) and bit j of
+ *              the stream in bit j % 32 of word j / 32 (at 4 bits: the
+ *              qgemv_w4a16 layout).
+ *   bits       2, 3, 4, 5, 6 or 8.
+ *   scales_f16, biases_f16  fp16 [N][K/group_size].
+ *   x_bf16     bf16 [M][K]; y fp32 [M][N] (output):
+ *              y[m][n] = sum_k (s * q[n][k] + b) * x[m][k].
+ *   M 1..32; N >= 1; K a multiple of 32 and of group_size, at most 2^20;
+ *   group_size 32, 64 or 128. Every pointer 16-byte aligned.
+ * A generic kernel (one warp per output row, correct, not tuned); 4-bit g64
+ * projections have the fast entry points above.
+ * Errors: QG_ERR_INVALID_ARG, QG_ERR_MISALIGNED.
+ */
+QG_API qg_status qgemm_affine(const uint32_t *wq, int bits, const uint16_t *scales_f16,
+                              const uint16_t *biases_f16, const uint16_t *x_bf16, float *y, int M, int N,
+                              int K, int group_size, void *stream);
+
+/*
  * qgemv_w8a16 -- y = W x for one activation row with row-int8 weights: the
  * packed int8 output head of "Running Kimi K3 (2.8T) on one Apple Silicon Mac"
  * (Deltafin), "Technical approach / compute" (the row-int8 checkpoint used

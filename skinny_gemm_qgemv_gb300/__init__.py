@@ -31,7 +31,7 @@ EXPORTS = [
     "moe_mxfp4_expert_forward_noalloc", "qg_moe_noalloc_max_bytes",
     "qgemv_w4a16_group_create", "qgemv_w4a16_group_run", "qgemv_w4a16_group_destroy",
     "qgemm_w4a16_skinny_group_create", "qgemm_w4a16_skinny_group_run", "qgemm_w4a16_skinny_group_destroy",
-    "qgemv_w8a16",
+    "qgemv_w8a16", "qgemm_affine",
 ]
 
 
@@ -69,6 +69,8 @@ def lib() -> ctypes.CDLL:
         L.qg_version.restype = I
         L.qgemv_w4a16.restype = I
         L.qgemv_w4a16.argtypes = [P, P, P, P, P, I, I, I, P, Z, P]
+        L.qgemm_affine.restype = I
+        L.qgemm_affine.argtypes = [P, I, P, P, P, P, I, I, I, I, P]
         L.qgemv_w8a16.restype = I
         L.qgemv_w8a16.argtypes = [P, P, P, P, I, I, P]
         L.qg_gemv_workspace_size.restype = Z
@@ -158,6 +160,25 @@ def qgemv_w4a16(wq, scales, biases, x, y=None, workspace=None, stream=None):
     _check(lib().qgemv_w4a16(_p(wq), _p(scales), _p(biases), _p(x), _p(y), N, K, K // scales.shape[1],
                              _p(workspace), ws_bytes, _stream(stream)), "qgemv_w4a16")
     return y
+
+
+def qgemm_affine(wq, bits, scales, biases, x, y=None, stream=None):
+    """Y[m][n] = sum_k (s q + b) X[m][k] with `bits`-bit codes (2, 3, 4, 5, 6
+    or 8) packed as one little-endian bit stream per row: wq int32
+    [N][K*bits/32], scales/biases fp16 [N][K/group], X bf16 [M][K] or [K] ->
+    Y fp32 [M][N] (or [N])."""
+    N, W = wq.shape
+    K = W * 32 // bits
+    vec = x.dim() == 1
+    xx = x[None, :] if vec else x
+    M = xx.shape[0]
+    for t, b, n in ((wq, 4, "wq"), (scales, 2, "scales"), (biases, 2, "biases"), (xx, 2, "x")):
+        _need(t, b, n)
+    if y is None:
+        y = torch.empty(M, N, device=wq.device, dtype=torch.float32)
+    _check(lib().qgemm_affine(_p(wq), int(bits), _p(scales), _p(biases), _p(xx), _p(y), M, N, K,
+                              K // scales.shape[1], _stream(stream)), "qgemm_affine")
+    return y[0] if vec and y.dim() == 2 else y
 
 
 def qgemv_w8a16(wq, scales, x, y=None, stream=None):

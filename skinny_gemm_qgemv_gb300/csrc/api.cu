@@ -140,6 +140,19 @@ qg_status qgemv_w4a16(const uint32_t* wq, const uint16_t* scales_f16, const uint
   return run_w4(wq, scales_f16, biases_f16, x_bf16, y, 1, N, K, group_size, workspace, ws_bytes, stream);
 }
 
+qg_status qgemm_affine(const uint32_t* wq, int bits, const uint16_t* scales_f16, const uint16_t* biases_f16,
+                       const uint16_t* x_bf16, float* y, int M, int N, int K, int group_size, void* stream) {
+  if (!wq || !scales_f16 || !biases_f16 || !x_bf16 || !y) return QG_ERR_INVALID_ARG;
+  if (bits != 2 && bits != 3 && bits != 4 && bits != 5 && bits != 6 && bits != 8) return QG_ERR_INVALID_ARG;
+  if (group_size != 32 && group_size != 64 && group_size != 128) return QG_ERR_INVALID_ARG;
+  if (M < 1 || M > 32 || N < 1 || K < 32 || K % 32 || K % group_size || K > (1 << 20)) return QG_ERR_INVALID_ARG;
+  if ((long long)N * (K / 32) * bits >= (1LL << 40)) return QG_ERR_INVALID_ARG;
+  if (!aligned16(wq) || !aligned16(scales_f16) || !aligned16(biases_f16) || !aligned16(x_bf16) || !aligned16(y))
+    return QG_ERR_MISALIGNED;
+  return from_cuda(qg::launch_affine_generic(wq, bits, scales_f16, biases_f16, x_bf16, y, M, N, K, group_size,
+                                             static_cast<cudaStream_t>(stream), g_pdl));
+}
+
 qg_status qgemv_w8a16(const int8_t* wq, const float* scales, const uint16_t* x_bf16, float* y, int N, int K,
                       void* stream) {
   if (!wq || !scales || !x_bf16 || !y) return QG_ERR_INVALID_ARG;

@@ -143,6 +143,11 @@ bool tmap_3d(CUtensorMap* tm, CUtensorMapDataType dt, const void* ptr, uint64_t 
              uint64_t chunks, uint64_t row_bytes, uint64_t chunk_bytes, uint32_t box_inner, uint32_t box_rows,
              uint32_t box_chunks);
 
+// affine codes at 2, 3, 4, 5, 6 or 8 bits, groups 32/64/128, M <= 32 (affine_gemv.cu)
+cudaError_t launch_affine_generic(const uint32_t* wq, int bits, const uint16_t* sc, const uint16_t* bi,
+                                  const uint16_t* x, float* y, int M, int N, int K, int group, cudaStream_t stream,
+                                  bool pdl);
+
 // W8A16 row-int8 GEMV (w8a16_gemv.cu)
 cudaError_t launch_w8a16_gemv(const int8_t* wq, const float* scales, const uint16_t* x, float* y, int N, int K,
                               cudaStream_t stream, bool pdl);

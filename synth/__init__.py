@@ -3,10 +3,10 @@
 This module draws random numbers and encodes weights into the stored formats
 the kernels and the oracle consume. It holds no step of the hot path itself:
 neither the GEMV/GEMM contractions, the router, SwiGLU, the Hadamard transform
-nor the per-token activation quantizer live here. The two weight encoders below
-(affine uint4 and MXFP4) are the input recipe of the workloads, i.e. how the
-stored codes are produced from fp32 weights before any kernel runs; the hot path
-only ever decodes them.
+nor the per-token activation quantizer live here. The weight encoders below
+(affine at 2..8 bits, row-int8 and MXFP4) are the input recipe of the
+workloads, i.e. how the stored codes are produced from fp32 weights before any
+kernel runs; the hot path only ever decodes them.
 
 Sources of the recipes:
   * "MLX Runner: An Inference Engine You Can Read", section "Architecture: one
@@ -29,9 +29,9 @@ import math
 import torch
 
 __all__ = [
-    "gen", "normal_f32", "bf16_normal", "affine_w4_encode", "w4_weights",
-    "mxfp4_encode", "mxfp4_weights", "router_logits", "outlier_activations",
-    "sign_bits", "STACK_SHAPES", "stack_layer_shapes",
+    "gen", "normal_f32", "bf16_normal", "affine_w4_encode", "w4_weights", "affine_encode",
+    "affine_weights", "row_int8_encode", "w8_row_weights", "mxfp4_encode", "mxfp4_weights",
+    "router_logits", "outlier_activations", "sign_bits", "STACK_SHAPES", "stack_layer_shapes",
 ]
 
 
@@ -81,6 +81,39 @@ def affine_w4_encode(w: torch.Tensor, group: int = 64):
     words = (q << shifts).sum(dim=2)                     # 0 .. 2^32-1
     words = words - ((words >> 31) & 1) * (1 << 32)      # same bits, int32 range
     return words.to(torch.int32).contiguous(), scale.contiguous(), bias.contiguous()
+
+
+def affine_encode(w: torch.Tensor, bits: int, group: int = 64):
+    """Encode fp32 weights [N][K] per K-group by min/max into `bits`-bit codes
+    (2, 3, 4, 5, 6 or 8): the recipe of affine_w4_encode with 2^bits - 1
+    levels. Each row's codes form one little-endian bit stream: code k in bits
+    [bits*k, bits*k + bits), bit j of the stream in bit j % 32 of word j / 32.
+    Returns (wq int32 [N][K*bits/32] holding the uint32 bit patterns, scales
+    fp16 [N][K/group], biases fp16 [N][K/group])."""
+    N, K = w.shape
+    assert K % group == 0 and K % 32 == 0 and bits in (2, 3, 4, 5, 6, 8)
+    levels = (1 << bits) - 1
+    wg = w.float().reshape(N, K // group, group)
+    mn = wg.amin(dim=2)
+    mx = wg.amax(dim=2)
+    scale = torch.clamp((mx - mn) / levels, min=0.0).to(torch.float16)
+    bias = mn.to(torch.float16)
+    sf = scale.float().unsqueeze(2)
+    bf = bias.float().unsqueeze(2)
+    safe = torch.where(sf > 0, sf, torch.ones_like(sf))
+    q = torch.round((wg - bf) / safe).clamp_(0, levels)
+    q = torch.where(sf > 0, q, torch.zeros_like(q)).to(torch.int64).reshape(N, K)
+    # bit stream: bit t of code k goes to stream bit bits*k + t
+    bitv = (q.unsqueeze(2) >> torch.arange(bits, device=w.device, dtype=torch.int64)) & 1   # [N][K][bits]
+    bitv = bitv.reshape(N, K * bits // 32, 32)
+    words = (bitv << torch.arange(32, device=w.device, dtype=torch.int64)).sum(dim=2)
+    words = words - ((words >> 31) & 1) * (1 << 32)
+    return words.to(torch.int32).contiguous(), scale.contiguous(), bias.contiguous()
+
+
+def affine_weights(N, K, bits, seed, slot, device="cpu", group=64, std=0.02):
+    """Weights ~ N(0, std) encoded as `bits`-bit affine codes (see affine_encode)."""
+    return _chunked(N, K, std, seed, slot, device, lambda w: affine_encode(w, bits, group))
 
 
 def _chunked(R, C, std, seed, slot, device, encode, max_elems=1 << 28):

@@ -66,6 +66,19 @@ def test_w4a16_validation(L):
     assert g(P(A), P(A), P(A), P(B + 2), P(A), 4, 16, 128, 64, None, 0, None) == 2
 
 
+def test_affine_validation(L):
+    f = L.qgemm_affine
+    assert f(None, 3, P(A), P(A), P(A), P(A), 1, 16, 128, 64, None) == 1
+    for bits in (0, 1, 7, 16):
+        assert f(P(A), bits, P(A), P(A), P(A), P(A), 1, 16, 128, 64, None) == 1
+    assert f(P(A), 3, P(A), P(A), P(A), P(A), 1, 16, 128, 48, None) == 1     # group 48
+    assert f(P(A), 3, P(A), P(A), P(A), P(A), 1, 16, 80, 32, None) == 1      # K % 32
+    assert f(P(A), 3, P(A), P(A), P(A), P(A), 1, 16, 96, 64, None) == 1      # K % group
+    assert f(P(A), 3, P(A), P(A), P(A), P(A), 0, 16, 128, 64, None) == 1     # M < 1
+    assert f(P(A), 3, P(A), P(A), P(A), P(A), 33, 16, 128, 64, None) == 1    # M > 32
+    assert f(P(A + 4), 3, P(A), P(A), P(A), P(A), 1, 16, 128, 64, None) == 2  # misaligned
+
+
 def test_w8a16_validation(L):
     f = L.qgemv_w8a16
     assert f(None, P(A), P(A), P(A), 16, 128, None) == 1
