@@ -370,6 +370,22 @@ def hadamard32_quant_i8(x, sign_bits, threads=0):
     return q, s, z
 
 
+def w8a8_dequant(x, w, sign_bits, threads=0):
+    """The whole int8 matrix path in float64 (Uzu article, "How Uzu optimizes
+    bytes and tokens per pass"): both operands take the same sign flip and
+    block-32 Walsh-Hadamard transform and are quantized per row to int8
+    (hadamard32_quant_i8), multiplied exactly (w8a8), and dequantized. The
+    transform is invertible, (H D a) . (H D w) = 32 a . w (D^2 = I, H H^T =
+    32 I), so y[m][n] = C[m][n] s_a[m] s_w[n] / 32 approximates x . w.
+    x, w bf16 bits [M][K], [N][K]. Returns (y [M][N] float64, parts) with the
+    quantized operands and scales in `parts`."""
+    qa, sa, za = hadamard32_quant_i8(x, sign_bits, threads)
+    qw, sw, zw = hadamard32_quant_i8(w, sign_bits, threads)
+    c = w8a8(qa, qw, threads)
+    y = c.astype(np.float64) * sa.astype(np.float64)[:, None] * sw.astype(np.float64)[None, :] / 32.0
+    return y, {"qa": qa, "sa": sa, "za": za, "qw": qw, "sw": sw, "zw": zw, "c": c}
+
+
 def w8a16(wq, scales, x, threads=0):
     """Row-int8 GEMV: y[m][n] = sum_k s[n] q[n][k] x[m][k] in float64, plus
     sum_k |w x| (the tolerance's scale). wq int8 [N][K], scales fp32 [N],

@@ -585,3 +585,40 @@ def test_affine_four_bits_is_the_w4a16_definition(group):
     y4, _ = oracle.w4a16(pack_codes(q), s, b, x, group=group)
     assert np.array_equal(pack_bitstream(q, 4), pack_codes(q))
     assert np.allclose(ya, y4, rtol=1e-14, atol=1e-14)
+
+
+# ---------------------------------------------------------------- fused int8 path (Hadamard -> int8 -> W8A8 -> dequant)
+
+def test_w8a8_dequant_within_the_quantization_bound():
+    # |y - x.w| is bounded by the int8 rounding of both transformed operands:
+    # with z = H D v and |z/s - q| <= 1/2 per element,
+    # 32 |y - x.w| <= sum_k (|z_a| s_w + |z_w| s_a) / 2 + K s_a s_w / 4.
+    rng = np.random.default_rng(11)
+    M, N, K = 3, 5, 256
+    x = bf16_bits(rng.normal(size=(M, K)))
+    w = bf16_bits(rng.normal(size=(N, K)) * 0.02)
+    sb = synth.sign_bits(K, seed=11, slot=0).numpy()
+    y, p = oracle.w8a8_dequant(x, w, sb)
+    xf = torch.from_numpy(x.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+    wf = torch.from_numpy(w.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+    exact = xf @ wf.T
+    za, zw = p["za"].astype(np.float64), p["zw"].astype(np.float64)
+    sa, sw = p["sa"].astype(np.float64), p["sw"].astype(np.float64)
+    bound = (np.abs(za).sum(1)[:, None] * sw[None, :] + np.abs(zw).sum(1)[None, :] * sa[:, None]) / 2 \
+        + K * sa[:, None] * sw[None, :] / 4
+    assert np.all(np.abs(y - exact) * 32 <= bound * (1 + 1e-9) + 1e-12)
+    # and the transform is what makes it work: the same rows without outliers agree closely
+    assert np.max(np.abs(y - exact)) < 0.05 * np.max(np.abs(exact))
+
+
+def test_w8a8_dequant_scales_with_the_activations():
+    # per-token symmetric quantization is scale-invariant: x -> 2x gives y -> 2y exactly
+    rng = np.random.default_rng(12)
+    M, N, K = 2, 4, 128
+    xv = rng.normal(size=(M, K)).astype(np.float32)
+    x1, x2 = bf16_bits(xv), bf16_bits(2 * xv)
+    w = bf16_bits(rng.normal(size=(N, K)) * 0.02)
+    sb = synth.sign_bits(K, seed=12, slot=0).numpy()
+    y1, _ = oracle.w8a8_dequant(x1, w, sb)
+    y2, _ = oracle.w8a8_dequant(x2, w, sb)
+    assert np.array_equal(y2, 2 * y1)
