@@ -209,20 +209,6 @@ def test_w4a16_group_sizes_32_128(q, group, M, N, K):
     assert np.all(d <= oracle.tolerance(ad)), f"worst {np.max(d / oracle.tolerance(ad)):.3g}x"
 
 
-# ---------------------------------------------------------------- affine 2/3/4/5/6/8 bits
-
-@pytest.mark.parametrize("bits", [2, 3, 4, 5, 6, 8])
-@pytest.mark.parametrize("M,N,K,group", [(1, 300, 1024, 64), (4, 77, 2048, 128), (7, 50, 512, 32)])
-def test_affine_bits_vs_oracle(q, bits, M, N, K, group):
-    wq, s, b = synth.affine_weights(N, K, bits, seed=700 + M, slot=bits, group=group)
-    x = synth.bf16_normal((M, K), seed=700 + M, slot=1)
-    y = q.qgemm_affine(wq.to(DEV), bits, s.to(DEV), b.to(DEV), x.to(DEV))
-    torch.cuda.synchronize()
-    ref, ad = oracle.affine(wq, bits, s, b, x, group=group)
-    d = np.abs(y.cpu().double().numpy() - ref)
-    assert np.all(d <= oracle.tolerance(ad)), f"worst {np.max(d / oracle.tolerance(ad)):.3g}x"
-
-
 # ---------------------------------------------------------------- W8A16 row-int8 GEMV
 
 @pytest.mark.parametrize("N,K", [(1, 16), (3, 48), (1000, 4096), (4099, 1024), (257, 12288), (33, 65536)])
