@@ -25,6 +25,9 @@ constexpr int kMaxDevices = 64;
 uint32_t* g_err_ptr[kMaxDevices] = {};
 std::mutex g_err_mu;
 
+}  // namespace
+
+namespace qg {
 // Device address of the error word for the current device (looked up once).
 uint32_t* err_word() {
   int dev = 0;
@@ -37,6 +40,10 @@ uint32_t* err_word() {
   }
   return g_err_ptr[dev];
 }
+}  // namespace qg
+
+namespace {
+using qg::err_word;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

@@ -63,6 +63,11 @@ MoeLayout moe_layout(int T, int H, int I, int E, int top_k) {
   L.nvirt = take(sizeof(int32_t) * 4);
   L.hmax = take(sizeof(uint32_t) * P);
   L.partial = take(0);
+  L.has_tc = !moe_mx_mma_ok(T, H, I, E, top_k) && moe_mx_tc_ok(T, H, I, E, top_k);
+  if (L.has_tc) {
+    L.tc = moe_tc_layout(T, H, I, E, top_k, off);
+    off = L.tc.end;
+  }
   L.total = off;
   return L;
 }
@@ -389,12 +394,19 @@ cudaError_t launch_moe_mxfp4(const uint16_t* x, const float* logits, const uint8
                          reinterpret_cast<uintptr_t>(uq) | reinterpret_cast<uintptr_t>(us) |
                          reinterpret_cast<uintptr_t>(dq) | reinterpret_cast<uintptr_t>(ds) |
                          reinterpret_cast<uintptr_t>(x)) & 15u) == 0;
+  const bool aligned32 = ((reinterpret_cast<uintptr_t>(gq) | reinterpret_cast<uintptr_t>(uq) |
+                           reinterpret_cast<uintptr_t>(dq)) & 31u) == 0;
   if (aligned && moe_mx_mma_ok(T, H, I, E, top_k)) {
-    // main path: routing + grouping in one CTA, then gate/up and down on warp-level MMA
+    // main path (T <= 32): routing + grouping in one CTA, then gate/up and down on warp-level MMA
     return launch_moe_mx_mma(x, logits, gq, gs, uq, us, dq, ds, T, H, I, E, top_k, y, idx, wts, I32(L.xexp),
                              reinterpret_cast<uint16_t*>(base + L.xh), I32(L.vexp), I32(L.nvirt),
                              reinterpret_cast<uint32_t*>(base + L.hmax), reinterpret_cast<float*>(base + L.h), err,
                              stream, pdl);
+  }
+  if (aligned && aligned32 && L.has_tc) {
+    // larger batches (33..64 tokens): block-scaled tcgen05 MMAs on the stored E2M1 codes and E8M0 scales
+    return launch_moe_mx_tc(x, logits, gq, gs, uq, us, dq, ds, T, H, I, E, top_k, y, idx, wts, base, L.tc,
+                            reinterpret_cast<float*>(base + L.h), err, stream, pdl);
   }
   // shapes outside the main path's tiling: one warp per row
   e = launch_kernel(moe_router_kernel, dim3(T), dim3(256), 0, stream, pdl, logits, x, H, E, top_k, idx, wts,

@@ -77,11 +77,15 @@ qg_status moe_mxfp4_expert_forward_noalloc(const uint16_t* x_bf16, const float* 
   if (qg::moe_layout(T, H, I, E, top_k).total > kNoallocBytes) return QG_ERR_WORKSPACE;
   void* scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) return QG_ERR_CUDA;
+  // device-side timeouts go to the library's error word, read by qg_device_error
+  uint32_t* err = qg::err_word();
+  if (!err) return QG_ERR_CUDA;
   // Every MoE stage writes each scratch byte it later reads (routing lists,
-  // fp16 activations, h), so stale contents from an earlier call are harmless
-  // and nothing needs clearing.
+  // operand images, h), and the counters that must start at zero are cleared
+  // by the first kernel of every call, so stale contents from an earlier call
+  // are harmless.
   const cudaError_t e = qg::launch_moe_mxfp4(x_bf16, router_logits, gate_q, gate_e8m0, up_q, up_e8m0, down_q,
-                                             down_e8m0, T, H, I, E, top_k, y, topk_idx, topk_w, scratch, nullptr,
+                                             down_e8m0, T, H, I, E, top_k, y, topk_idx, topk_w, scratch, err,
                                              static_cast<cudaStream_t>(stream), false);
   return e == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }

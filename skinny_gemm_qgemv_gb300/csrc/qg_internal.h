@@ -32,6 +32,10 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 
 int device_sm_count();
 
+// Device address of the library's sticky error word on the current device
+// (looked up once per device), or null if it cannot be found.
+uint32_t* err_word();
+
 // Largest dynamic shared memory one CTA may opt into on the current device.
 int device_max_smem_optin();
 
@@ -161,13 +165,25 @@ inline int moe_nvirt_max(int T, int E, int top_k) {
   const int P = T * top_k;
   return (P < E ? P : E) + P / kMxTC;
 }
+// scratch of the tcgen05 block-scaled path (moe_mx_tc.cu), byte offsets in the workspace
+struct MoeTcLayout {
+  size_t elist, nexp, epair, gspan, dspan, ximg, xsf, dimg, dsf, gpart, dpart, gcnt, dcnt, end;
+};
 struct MoeLayout {
   size_t pair_expert, pair_weight, counts, offsets, active, order, nactive, xh, xexp, h, hh, hexp, partial;
   size_t vexp, nvirt, hmax;
+  bool has_tc;     // the tcgen05 path's scratch follows
+  MoeTcLayout tc;
   size_t total;
 };
 MoeLayout moe_layout(int T, int H, int I, int E, int top_k);
 bool moe_mx_mma_ok(int T, int H, int I, int E, int top_k);
+bool moe_mx_tc_ok(int T, int H, int I, int E, int top_k);
+MoeTcLayout moe_tc_layout(int T, int H, int I, int E, int top_k, size_t off);
+cudaError_t launch_moe_mx_tc(const uint16_t* x, const float* logits, const uint8_t* gq, const uint8_t* gs,
+                             const uint8_t* uq, const uint8_t* us, const uint8_t* dq, const uint8_t* ds, int T,
+                             int H, int I, int E, int top_k, float* y, int32_t* idx, float* wts, uint8_t* ws,
+                             const MoeTcLayout& L, float* h, uint32_t* err, cudaStream_t stream, bool pdl);
 cudaError_t launch_moe_mx_mma(const uint16_t* x, const float* logits, const uint8_t* gq, const uint8_t* gs,
                               const uint8_t* uq, const uint8_t* us, const uint8_t* dq, const uint8_t* ds, int T,
                               int H, int I, int E, int top_k, float* y, int32_t* idx, float* wts, int32_t* xexp,

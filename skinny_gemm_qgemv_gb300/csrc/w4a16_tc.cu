@@ -382,6 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = max(0, issued - a.ST); j < issued; ++j)
         mbar_wait(&full[j % a.ST], (j / a.ST) & 1, a.err, kErrTcDrain);
     }
+    __syncwarp();  // the lane's role loop ends here: the warp reaches the final barrier converged
   } else if (warp <= 2) {
     // ------------------------- MMA issuers: warp 1 groups 0, 1 of every chunk, warp 2 groups 2, 3
     if (lane == 0) {
@@ -420,6 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&done[h]);
       mbar_wait(&done[h], 0, a.err, kErrTcDrain);
     }
+    __syncwarp();  // the lane's role loop ends here: the warp reaches the final barrier converged
   } else if (warp < 11) {
     // ------------------------------------------ converters: warps 3..10, every chunk
     // a warp may only touch TMEM lanes 32 * (warp % 4) .. + 31: row = its lane;
@@ -825,6 +827,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       for (int j = max(0, issued - a.ST); j < issued; ++j)
         mbar_wait(&full[j % a.ST], (j / a.ST) & 1, a.err, kErrTcDrain);
     }
+    __syncwarp();  // the lane's role loop ends here: the warp reaches the final barrier converged
   } else {
     // ---------------------------------------------------------------- consumers
     const int g = lane >> 2, c = lane & 3;

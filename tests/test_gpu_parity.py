@@ -353,6 +353,23 @@ def test_moe_full_size(q, T):
     check_moe(q, x, lg, w, k, tokens=[0] if T == 1 else [0, 7, T - 1])
 
 
+# Batches of 33..64 tokens run on the block-scaled tensor-core path (one
+# accumulator buffer once a batch's columns no longer fit two; B spans that
+# start past the first 16-column block; ranges that start mid-window).
+@pytest.mark.parametrize("E,H,I,T,k", [(24, 1024, 512, 33, 6), (64, 512, 512, 40, 8), (48, 1536, 1024, 64, 4),
+                                       (16, 2048, 512, 48, 2)])
+def test_moe_tc_batches(q, E, H, I, T, k):
+    x, lg, w = moe_inputs(E, H, I, T, seed=60 + T, device=DEV)
+    check_moe(q, x, lg, w, k)
+
+
+def test_moe_tc_full_size(q):
+    # the full layer (384 experts of 7168 x 2048, top-16) at a 48-token batch; tokens sampled
+    E, H, I, T, k = 384, 7168, 2048, 48, 16
+    x, lg, w = moe_inputs(E, H, I, T, seed=3, device=DEV)
+    check_moe(q, x, lg, w, k, tokens=[0, 17, 33, T - 1])
+
+
 # ---------------------------------------------------------------- grouped M = 1 GEMV
 
 def test_gemv_group_vs_oracle(q):
