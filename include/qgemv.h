@@ -297,10 +297,16 @@ QG_API qg_status qgemv_w8a16(const int8_t *wq, const float *scales, const uint16
  *       g = Wg[e] x_t, u = Wu[e] x_t, h = silu(g) * u (kept in fp32),
  *       y[t] = sum_j p * (Wd[e] h).
  *   The summation order is fixed (repeated calls give identical results) but
- *   is the kernels' own: the main path (H and I multiples of 512, T <= 16)
- *   accumulates each token's experts on the tensor cores per K slice and adds
- *   the slices in a fixed order. Float outputs meet |y - y_ref| <=
+ *   is the kernels' own. Kernel paths: H and I multiples of 512 and T <= 32
+ *   run on warp-level MMAs; 33 <= T <= 64 (T * top_k <= 1024, code arrays
+ *   32-byte aligned) on block-scaled tensor-core MMAs that take the E2M1 codes
+ *   and E8M0 scales as stored (activations enter as exact sums of e4m3 terms);
+ *   other shapes on one warp per output row. Float outputs meet |y - y_ref| <=
  *   2e-3 * sum |p w h| + 1e-5 against an exact evaluation.
+ *   Scale range: any E8M0 byte 0..254 is accepted; the warp-level MMA path
+ *   reads e = 0 (2^-127) as 0, which changes a result by less than
+ *   6 * 2^-127 * sum|x| per block. Weights, activations and scales must keep
+ *   every product and partial sum inside the fp32 range.
  *   workspace      at least qg_moe_workspace_size(T, H, I, E, top_k) bytes,
  *                  16-byte aligned; clobbered. The fp32 activations h of pair
  *                  (t, j) are left at byte offset qg_moe_workspace_h_offset()
@@ -334,13 +340,15 @@ QG_API size_t qg_moe_workspace_h_offset(int T, int H, int I, int E, int top_k);
  *   - Problems whose workspace (qg_moe_workspace_size) exceeds
  *     QG_MOE_NOALLOC_MAX_BYTES are refused with QG_ERR_WORKSPACE before any
  *     launch; with 384 experts of 7168 x 2048 and top-16 routing that admits
- *     up to T = 39 tokens.
+ *     up to T = 32 tokens.
+ *   - Device-side timeouts are reported through qg_device_error, as for the
+ *     other entry points.
  *   - The first call on a device looks up the scratch array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture begins.
  *   - All calls on a device share the one array and it keeps the previous
- *     call's contents; every stage writes what it later reads, so nothing has
- *     to start zeroed. Calls that may run at the same time on the GPU (on
+ *     call's contents; every stage writes what it later reads, and the first
+ *     kernel of each call clears the counters that must start at zero. Calls that may run at the same time on the GPU (on
  *     different streams, or from different threads without ordering) race on
  *     the array: order them on one stream.
  *   - Launches never use programmatic dependent launch (qg_set_pdl is

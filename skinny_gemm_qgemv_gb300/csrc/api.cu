@@ -63,9 +63,10 @@ int device_max_smem_optin() {
 
 int device_sm_count() {
   int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  return sms;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                 cudaSuccess)
+    sms = 0;
+  return sms > 0 ? sms : 1;  // planners divide by it; without a device, size queries still answer
 }
 }  // namespace qg
 
