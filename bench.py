@@ -365,6 +365,71 @@ def bench_skinny_stacks(q, mats, dev, stream, hbm_peak):
     return out
 
 
+def decoder_chain_items(q, mats, x0, dev):
+    """The decode step of the dense stack in dependency order: per layer
+    {q, k, v} at level 4l reading the layer input, o reading q's output (the
+    stand-in for attention), gate_up reading o's output, down reading the gate
+    half of gate_up's output; the next layer and the lm_head read down's
+    output. Every input is a copy scaled by 1 / (0.02 sqrt(K_src)) (the
+    weights' std is 0.02) in place of the norm layers, so the activations stay
+    O(1) through the 36 layers (a fixed-scale SwiGLU would square them every
+    layer)."""
+    items, level, layer_in, by = [], 0, (q.X_BF16, x0, 1.0), {}
+    for name, N, K, wq, s, b in mats:
+        kind = name.split(".")[-1]
+        y = torch.empty(N, device=dev)
+        if kind in ("q", "k", "v", "lm_head"):
+            (op, x, alpha), lvl = layer_in, level
+        elif kind == "o":
+            op, x, alpha, lvl = q.X_COPY, by["q"], 1.0 / (0.02 * 64.0), level + 1
+        elif kind == "gate_up":
+            op, x, alpha, lvl = q.X_COPY, by["o"], 1.0 / (0.02 * 64.0), level + 2
+        else:
+            op, x, alpha, lvl = q.X_COPY, by["gate_up"], 1.0 / (0.02 * 64.0), level + 3
+        items.append(dict(wq=wq, scales=s, biases=b, level=lvl, op=op, x=x, alpha=alpha, y=y))
+        by[kind] = y
+        if kind == "down":
+            level += 4
+            layer_in = (q.X_COPY, y, 1.0 / (0.02 * 12288 ** 0.5))
+    return items
+
+
+def bench_dependent_stack(q, mats, dev, stream, hbm_peak, steps):
+    """The M = 1 stack in dependency order (145 levels: per layer {q, k, v}, o,
+    gate_up, down; then lm_head) as one chain launch per token, and the same
+    217 projections as one level (all independent) through the same kernel."""
+    step_bytes = sum(w4_bytes(N, K) for (_, N, K, *_r) in mats)
+    x0 = synth.bf16_normal((4096,), 1, 4999, device=dev)
+    out = {}
+    for key, one_level in (("dependent_stack_m1", False), ("chain_one_level_m1", True)):
+        items = decoder_chain_items(q, mats, x0, dev)
+        if one_level:
+            xs = [synth.bf16_normal((it["wq"].shape[1] * 8,), 1, 6000 + i, device=dev) for i, it in enumerate(items)]
+            for it, x in zip(items, xs):
+                it.update(level=0, op=q.X_BF16, x=x, alpha=1.0)
+        ch = q.GemvChain(items)
+        g = capture(lambda: ch.run(stream), stream)
+        reps = []
+        for _ in range(5):
+            reps.append(replay_timed(g, max(20, steps), stream, warmup=3))
+        reps.sort()
+        t = reps[len(reps) // 2]
+        assert q.device_error() == 0
+        levels = items[-1]["level"] + 1
+        out[key] = {"value": step_bytes / t / 1e9, "unit": "GB/s", "frac": step_bytes / t / 1e9 / hbm_peak,
+                    "ms_per_step": t * 1e3, "tokens_per_s": 1.0 / t, "bytes_per_step": step_bytes,
+                    "levels": levels, "launches_per_step": 1,
+                    "min_ms_per_step": reps[0] * 1e3, "max_ms_per_step": reps[-1] * 1e3,
+                    "form": ("one w4a16_chain_kernel launch per token; per layer {q, k, v} -> o -> gate_up -> "
+                             "down -> next layer, each level awaited in the kernel" if not one_level else
+                             "the 217 projections as one level of the same chain kernel (independent inputs)")}
+        del g
+        ch.close()
+        del items
+        torch.cuda.empty_cache()
+    return out
+
+
 def bench_moe(q, dev, stream, T, moe_w):
     E, H, I, k = 384, 7168, 2048, 16
     x = synth.bf16_normal((T, H), 3, 0, dev)
@@ -415,7 +480,8 @@ def bench_w8a8(q, dev, stream, N, l2_bytes):
 
 CASES = ["gemv_lm_head", "gemv_down", "gemv_q", "skinny16_gate_up", "skinny16_down", "moe_T1", "moe_T16",
          "w8a16_lm_head",
-         "w8a8_12288", "hadamard_16x4096", "gemv_group_4layers", "skinny16_group_4layers"]
+         "w8a8_12288", "hadamard_16x4096", "gemv_group_4layers", "skinny16_group_4layers", "chain_4layers",
+         "chain_flat_4layers"]
 
 
 def run_case(args):
@@ -432,6 +498,18 @@ def run_case(args):
         xs, ys = stack_io(mats, dev, 1)
         grp = q.GemvGroup([(wq, s, b, x[0], y[0]) for (_, N, K, wq, s, b), x, y in zip(mats, xs, ys)])
         f = grp.run
+        nbytes = sum(w4_bytes(N, K) for (_, N, K, *_r) in mats)
+    elif c in ("chain_4layers", "chain_flat_4layers"):
+        # the dependent-order chain over 4 decoder layers + the lm_head (0.78 GB, 17 levels),
+        # or the same projections as one level with independent inputs
+        mats = build_stack(q, dev, 1, layers=4)
+        x0 = synth.bf16_normal((4096,), 1, 4999, device=dev)
+        items = decoder_chain_items(q, mats, x0, dev)
+        if c == "chain_flat_4layers":
+            for i, it in enumerate(items):
+                it.update(level=0, op=q.X_BF16, x=synth.bf16_normal((it["wq"].shape[1] * 8,), 1, 6000 + i, device=dev))
+        ch = q.GemvChain(items)
+        f = ch.run
         nbytes = sum(w4_bytes(N, K) for (_, N, K, *_r) in mats)
     elif c == "skinny16_group_4layers":
         # the grouped skinny launch, M = 16 (warp-level MMA), over 4 decoder layers + the lm_head
@@ -660,6 +738,7 @@ def main():
         grp16.close()
         del xs16, ys16, grp16
         extras["skinny_stack"] = bench_skinny_stacks(q, mats, dev, stream, hbm_peak)
+        extras.update(bench_dependent_stack(q, mats, dev, stream, hbm_peak, args.steps))
         extras["m1_stack_tokens_per_s"] = 1.0 / t_step
         extras["single_gemv_1024"] = bench_single_gemv(q, dev, stream, l2)
         extras["w8a16_lm_head_151936x4096"] = bench_w8a16(q, dev, stream, hbm_peak)

@@ -157,6 +157,81 @@ QG_API qg_status qgemv_w4a16_group_run(const qg_w4_group *group, void *stream);
 QG_API void qgemv_w4a16_group_destroy(qg_w4_group *group);
 
 /*
+ * qgemv_w4a16_chain_* -- the M = 1 projections of a decode step in dependency
+ * order, as one persistent launch. "MLX Runner ...", section "Architecture:
+ * one command buffer per token", issues a whole token as one unit; in a
+ * decoder most projections consume the previous one's output (q, k, v -> o ->
+ * gate_up -> down -> the next layer), so each projection here carries a
+ * dependency level, and a projection of level L starts only after every
+ * projection of the levels below L has written its y. The levels are awaited
+ * inside the kernel (one counter per level in device memory) while the
+ * weights keep streaming, so the weight stream does not stop between
+ * dependent projections. The weights are those of qgemv_w4a16 (affine 4-bit,
+ * group 64); each projection computes y = W x with x one of:
+ *   QG_X_BF16    x = x_src as bf16 [K];
+ *   QG_X_COPY    x[k] = bf16(x_alpha * x_src[k]), x_src fp32 [K] (an earlier
+ *                level's y: the product in fp32, rounded to nearest even);
+ *   QG_X_SWIGLU  x[k] = bf16(silu(g) * u * x_alpha), g = x_src[k],
+ *                u = x_src[K + k], x_src fp32 [2K] (the gate/up output of a
+ *                feed-forward layer), evaluated in fp32 as
+ *                ((g / (1 + exp(-g))) * u) * x_alpha and rounded to nearest
+ *                even.
+ *
+ *   qg_w4_chain_desc  one projection: wq uint32 [N][K/8], scales/biases fp16
+ *                    [N][K/64] (the layouts of qgemv_w4a16), level >= 0 and
+ *                    non-decreasing along the list, x_op / x_src / x_alpha as
+ *                    above, y fp32 [N]; every pointer 16-byte aligned device
+ *                    memory of the current device; N >= 1; K a multiple of
+ *                    64 (else QG_ERR_INVALID_ARG) and at most 16384 (else
+ *                    QG_ERR_UNSUPPORTED). Within one level the projections are
+ *                    independent: no y may overlap another y or an x_src read
+ *                    at the same level; a projection may read the y of any
+ *                    lower level.
+ *   qgemv_w4a16_chain_create  validates the descriptors (group_size 64; 32 and
+ *                    128 return QG_ERR_UNSUPPORTED, other values
+ *                    QG_ERR_INVALID_ARG), allocates device memory for a copy
+ *                    of every projection's weights in the kernel's layout (the
+ *                    same number of bytes as the stored weights, plus small
+ *                    tables), fills it on the legacy default stream and waits
+ *                    for it. The stored weights are not read afterwards (they
+ *                    may be freed); x_src and y are used by every run and must
+ *                    stay allocated until the chain is destroyed. *chain is
+ *                    set on QG_OK.
+ *   qgemv_w4a16_chain_run     one cooperative launch on stream (one CTA per
+ *                    SM, all resident at once) computing every level in order
+ *                    from the current x_src contents; no allocation,
+ *                    capturable in a CUDA graph. Runs of one chain must not
+ *                    overlap (its level counters are shared); each run leaves
+ *                    them at zero, also after a device timeout. Results are
+ *                    deterministic. Run it on the device current at create.
+ *   qgemv_w4a16_chain_destroy frees the chain (NULL is ignored); no run may be
+ *                    pending.
+ *   qgemv_w4a16_chain_bytes   device bytes the chain holds.
+ */
+typedef enum { QG_X_BF16 = 0, QG_X_COPY = 1, QG_X_SWIGLU = 2 } qg_x_op;
+
+typedef struct qg_w4_chain_desc {
+  const uint32_t *wq;
+  const uint16_t *scales_f16;
+  const uint16_t *biases_f16;
+  int N;
+  int K;
+  int level;
+  int x_op;
+  const void *x_src;
+  float x_alpha;
+  float *y;
+} qg_w4_chain_desc;
+
+typedef struct qg_w4_chain qg_w4_chain;
+
+QG_API qg_status qgemv_w4a16_chain_create(const qg_w4_chain_desc *descs, int count, int group_size,
+                                          qg_w4_chain **chain);
+QG_API qg_status qgemv_w4a16_chain_run(const qg_w4_chain *chain, void *stream);
+QG_API void qgemv_w4a16_chain_destroy(qg_w4_chain *chain);
+QG_API size_t qgemv_w4a16_chain_bytes(const qg_w4_chain *chain);
+
+/*
  * qgemm_w4a16_skinny -- Y = X W^T for a few activation rows, each weight read
  * once for all rows ("Krill Teardown", "Core mechanisms"; Uzu article,
  * "Producing several tokens from one model pass").
@@ -414,6 +489,31 @@ QG_API void qg_set_pdl(int enable);
  * is reset to 0. Returns QG_ERR_DEVICE_TIMEOUT when the word was nonzero.
  */
 QG_API qg_status qg_device_error(uint32_t *code, int clear);
+
+/*
+ * qg_last_cuda_error -- the CUDA runtime error code (cudaError_t value) behind
+ * the most recent QG_ERR_CUDA returned to the calling thread, 0 if none has
+ * been returned; qg_last_cuda_error_string gives its text. Diagnostic only.
+ */
+QG_API int qg_last_cuda_error(void);
+QG_API const char *qg_last_cuda_error_string(void);
+
+/*
+ * qg_selftest_wait_timeout -- exercises the device-side failure reporting on
+ * the current device: one small kernel on stream whose wait can never be
+ * satisfied gives up after a short bound, records a code in the error word
+ * and returns, so the context stays usable.
+ *   kind 0  an mbarrier phase nothing arrives at, bounded by `limit` polls
+ *           (1..2^22); code 0x501.
+ *   kind 1  a counter in device memory nothing raises, bounded by `limit`
+ *           microseconds (1..10^6); code 0x502.
+ * Afterwards qg_device_error reports QG_ERR_DEVICE_TIMEOUT with that code
+ * (unless an earlier code is still set: the word keeps the first). Returns
+ * QG_ERR_INVALID_ARG for another kind or limit, QG_ERR_CUDA if the launch (or
+ * the 4-byte counter's allocation) fails. Diagnostic only: no other entry
+ * point's results depend on it.
+ */
+QG_API qg_status qg_selftest_wait_timeout(int kind, uint32_t limit, void *stream);
 
 #ifdef __cplusplus
 }

@@ -204,6 +204,61 @@ def tolerance(absdot):
 
 
 # --------------------------------------------------------------------------
+# Inputs of the dependent projections of a decode step
+# --------------------------------------------------------------------------
+# "MLX Runner: An Inference Engine You Can Read", "Architecture: one command
+# buffer per token": a token runs the layer's projections one after another,
+# each consuming the previous one's output. Between the fp32 output of one
+# projection and the bf16 activation of the next the chain applies either a
+# scaled copy or the SwiGLU of a fused gate/up output (the expert FFN form
+# down(silu(gate x) * up x) used for the MoE below); both end in one rounding
+# to bf16, nearest even.
+
+X_BF16, X_COPY, X_SWIGLU = 0, 1, 2
+
+
+def bf16_bits(v):
+    """Round real values (float64 or float32 arrays) to bf16 in ONE step,
+    nearest with ties to even; returns the uint16 bit patterns.
+
+    Normal range: the float64 significand is rounded at bit 45 (bf16 keeps 7
+    of float64's 52 fraction bits); magnitudes below 2^-126 are bf16
+    subnormals, multiples of 2^-133 rounded with ties to even. Results beyond
+    the largest bf16 become infinities."""
+    v = np.ascontiguousarray(np.asarray(v, dtype=np.float64))
+    b = v.view(np.uint64)
+    lsb = (b >> np.uint64(45)) & np.uint64(1)
+    r = (b + np.uint64((1 << 44) - 1) + lsb) & ~np.uint64((1 << 45) - 1)
+    normal = r.view(np.float64)
+    sub = np.round(v / 2.0 ** -133) * 2.0 ** -133  # np.round: ties to even
+    out = np.where(np.abs(v) < 2.0 ** -126, sub, normal)
+    with np.errstate(over="ignore"):
+        f = out.astype(np.float32)
+    return (f.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+def chain_x(src, op, alpha, K):
+    """The bf16 activation (uint16 bits [K]) a projection reads from an earlier
+    projection's fp32 output `src`:
+      X_COPY:   bf16(alpha * src[k]), the product taken in fp32 (one IEEE
+                rounding, as the kernel does), then rounded to bf16;
+      X_SWIGLU: bf16(silu(g) * u * alpha) with g = src[k], u = src[K + k], the
+                value computed in float64 and rounded once (the kernel
+                evaluates it in fp32, so a value within a few fp32 ulps of a
+                bf16 rounding boundary may land one bf16 ulp apart)."""
+    src = _np(src, np.float32).reshape(-1)
+    if op == X_COPY:
+        assert src.size >= K
+        return bf16_bits((np.float32(alpha) * src[:K]).astype(np.float64))
+    if op == X_SWIGLU:
+        assert src.size >= 2 * K
+        g = src[:K].astype(np.float64)
+        u = src[K:2 * K].astype(np.float64)
+        return bf16_bits(silu(g) * u * float(alpha))
+    raise ValueError(f"unknown op {op}")
+
+
+# --------------------------------------------------------------------------
 # MXFP4 routed-expert MoE
 # --------------------------------------------------------------------------
 

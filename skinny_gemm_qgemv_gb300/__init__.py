@@ -32,7 +32,11 @@ EXPORTS = [
     "qgemv_w4a16_group_create", "qgemv_w4a16_group_run", "qgemv_w4a16_group_destroy",
     "qgemm_w4a16_skinny_group_create", "qgemm_w4a16_skinny_group_run", "qgemm_w4a16_skinny_group_destroy",
     "qgemv_w8a16", "qgemm_affine",
+    "qgemv_w4a16_chain_create", "qgemv_w4a16_chain_run", "qgemv_w4a16_chain_destroy", "qgemv_w4a16_chain_bytes",
+    "qg_last_cuda_error", "qg_last_cuda_error_string", "qg_selftest_wait_timeout",
 ]
+
+X_BF16, X_COPY, X_SWIGLU = 0, 1, 2
 
 
 class _GemvDesc(ctypes.Structure):
@@ -44,6 +48,12 @@ class _GemmDesc(ctypes.Structure):
     _fields_ = [("wq", ctypes.c_void_p), ("scales_f16", ctypes.c_void_p), ("biases_f16", ctypes.c_void_p),
                 ("x_bf16", ctypes.c_void_p), ("y", ctypes.c_void_p), ("M", ctypes.c_int), ("N", ctypes.c_int),
                 ("K", ctypes.c_int)]
+
+
+class _ChainDesc(ctypes.Structure):
+    _fields_ = [("wq", ctypes.c_void_p), ("scales_f16", ctypes.c_void_p), ("biases_f16", ctypes.c_void_p),
+                ("N", ctypes.c_int), ("K", ctypes.c_int), ("level", ctypes.c_int), ("x_op", ctypes.c_int),
+                ("x_src", ctypes.c_void_p), ("x_alpha", ctypes.c_float), ("y", ctypes.c_void_p)]
 
 
 class QGError(RuntimeError):
@@ -109,12 +119,28 @@ def lib() -> ctypes.CDLL:
         L.qgemm_w4a16_skinny_group_run.argtypes = [P, P]
         L.qgemm_w4a16_skinny_group_destroy.restype = None
         L.qgemm_w4a16_skinny_group_destroy.argtypes = [P]
+        L.qgemv_w4a16_chain_create.restype = I
+        L.qgemv_w4a16_chain_create.argtypes = [ctypes.POINTER(_ChainDesc), I, I, ctypes.POINTER(P)]
+        L.qgemv_w4a16_chain_run.restype = I
+        L.qgemv_w4a16_chain_run.argtypes = [P, P]
+        L.qgemv_w4a16_chain_destroy.restype = None
+        L.qgemv_w4a16_chain_destroy.argtypes = [P]
+        L.qg_selftest_wait_timeout.restype = I
+        L.qg_selftest_wait_timeout.argtypes = [I, ctypes.c_uint32, P]
+        L.qg_last_cuda_error.restype = I
+        L.qg_last_cuda_error.argtypes = []
+        L.qg_last_cuda_error_string.restype = ctypes.c_char_p
+        L.qg_last_cuda_error_string.argtypes = []
+        L.qgemv_w4a16_chain_bytes.restype = Z
+        L.qgemv_w4a16_chain_bytes.argtypes = [P]
         _lib = L
     return _lib
 
 
 def _check(status: int, where: str):
     if status != QG_OK:
+        if status == 5:  # QG_ERR_CUDA: name the runtime error behind it
+            where = f"{where} ({lib().qg_last_cuda_error_string().decode()})"
         raise QGError(status, where)
 
 
@@ -257,6 +283,51 @@ class GemvGroup:
     def close(self):
         if self._h:
             lib().qgemv_w4a16_group_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class GemvChain:
+    """M = 1 projections in dependency order as one persistent launch.
+
+    `items` is a list of dicts with keys wq, scales, biases (the layouts of
+    qgemv_w4a16), level (non-decreasing), op (X_BF16, X_COPY or X_SWIGLU), x
+    (bf16 [K] for X_BF16, fp32 [K] / [2K] for X_COPY / X_SWIGLU, typically an
+    earlier level's y), alpha (float, default 1) and y (fp32 [N], written).
+    The weights are copied into the kernel's layout at construction; the x
+    and y tensors are held and used by every run."""
+
+    def __init__(self, items):
+        descs = (_ChainDesc * len(items))()
+        for d, it in zip(descs, items):
+            wq, s, b, x, y = it["wq"], it["scales"], it["biases"], it["x"], it["y"]
+            for t, nb, n in ((wq, 4, "wq"), (s, 2, "scales"), (b, 2, "biases"), (y, 4, "y")):
+                _need(t, nb, n)
+            op = it.get("op", X_BF16)
+            _need(x, 2 if op == X_BF16 else 4, "x")
+            d.wq, d.scales_f16, d.biases_f16 = wq.data_ptr(), s.data_ptr(), b.data_ptr()
+            d.N, d.K = wq.shape[0], wq.shape[1] * 8
+            d.level, d.x_op, d.x_alpha = int(it["level"]), int(op), float(it.get("alpha", 1.0))
+            d.x_src, d.y = x.data_ptr(), y.data_ptr()
+        self._items = [dict(x=it["x"], y=it["y"]) for it in items]
+        self._h = ctypes.c_void_p()
+        _check(lib().qgemv_w4a16_chain_create(descs, len(items), 64, ctypes.byref(self._h)),
+               "qgemv_w4a16_chain_create")
+
+    def run(self, stream=None):
+        _check(lib().qgemv_w4a16_chain_run(self._h, _stream(stream)), "qgemv_w4a16_chain_run")
+
+    def device_bytes(self):
+        return lib().qgemv_w4a16_chain_bytes(self._h)
+
+    def close(self):
+        if self._h:
+            lib().qgemv_w4a16_chain_destroy(self._h)
             self._h = ctypes.c_void_p()
 
     def __del__(self):

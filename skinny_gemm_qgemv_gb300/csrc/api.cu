@@ -47,7 +47,13 @@ using qg::err_word;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-qg_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QG_OK : QG_ERR_CUDA; }
+thread_local cudaError_t t_last_cuda = cudaSuccess;  // behind the last QG_ERR_CUDA of this thread
+
+qg_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return QG_OK;
+  t_last_cuda = e;
+  return QG_ERR_CUDA;
+}
 
 bool g_pdl = false;  // programmatic dependent launch for every kernel (see qg_set_pdl)
 
@@ -215,6 +221,58 @@ void qgemv_w4a16_group_destroy(qg_w4_group* group) {
   delete group;
 }
 
+struct qg_w4_chain {
+  qg::ChainPlan plan;
+};
+
+qg_status qgemv_w4a16_chain_create(const qg_w4_chain_desc* descs, int count, int group_size, qg_w4_chain** chain) {
+  if (!descs || !chain || count < 1) return QG_ERR_INVALID_ARG;
+  if (group_size == 32 || group_size == 128) return QG_ERR_UNSUPPORTED;
+  if (group_size != 64) return QG_ERR_INVALID_ARG;
+  std::vector<qg::ChainItem> list(count);
+  for (int i = 0; i < count; ++i) {
+    const qg_w4_chain_desc& d = descs[i];
+    if (!d.wq || !d.scales_f16 || !d.biases_f16 || !d.x_src || !d.y) return QG_ERR_INVALID_ARG;
+    if (d.N < 1 || d.K < 64 || d.K % 64 != 0 || d.level < 0) return QG_ERR_INVALID_ARG;
+    if (i > 0 && d.level < descs[i - 1].level) return QG_ERR_INVALID_ARG;
+    if (d.x_op != QG_X_BF16 && d.x_op != QG_X_COPY && d.x_op != QG_X_SWIGLU) return QG_ERR_INVALID_ARG;
+    if (!aligned16(d.wq) || !aligned16(d.scales_f16) || !aligned16(d.biases_f16) || !aligned16(d.x_src) ||
+        !aligned16(d.y))
+      return QG_ERR_MISALIGNED;
+    if (!qg::chain_proj_ok(d.N, d.K)) return QG_ERR_UNSUPPORTED;
+    list[i] = qg::ChainItem{d.wq, d.scales_f16, d.biases_f16, d.N, d.K, d.level, d.x_op, d.x_src, d.x_alpha, d.y};
+  }
+  auto* out = new (std::nothrow) qg_w4_chain();
+  if (!out) return QG_ERR_CUDA;
+  const cudaError_t e = qg::chain_plan_build(list.data(), count, qg::device_sm_count(), &out->plan);
+  if (e != cudaSuccess) {
+    delete out;
+    return from_cuda(e);
+  }
+  *chain = out;
+  return QG_OK;
+}
+
+qg_status qgemv_w4a16_chain_run(const qg_w4_chain* chain, void* stream) {
+  if (!chain) return QG_ERR_INVALID_ARG;
+  uint32_t* err = err_word();
+  if (!err) return QG_ERR_CUDA;
+  return from_cuda(qg::chain_launch(chain->plan, err, static_cast<cudaStream_t>(stream)));
+}
+
+void qgemv_w4a16_chain_destroy(qg_w4_chain* chain) {
+  if (!chain) return;
+  qg::chain_plan_free(&chain->plan);
+  delete chain;
+}
+
+size_t qgemv_w4a16_chain_bytes(const qg_w4_chain* chain) {
+  if (!chain) return 0;
+  const qg::ChainPlan& p = chain->plan;
+  return p.packed_bytes + sizeof(qg::ChainProj) * p.nproj + sizeof(int) * (p.grid + 1 + p.nlevels) +
+         sizeof(unsigned) * (p.nlevels + 1);
+}
+
 qg_status qgemm_w4a16_skinny(const uint32_t* wq, const uint16_t* scales_f16, const uint16_t* biases_f16,
                              const uint16_t* x_bf16, float* y, int M, int N, int K, int group_size,
                              void* workspace, size_t ws_bytes, void* stream) {
@@ -316,6 +374,33 @@ qg_status gemm_w8a8_i32(const int8_t* a, const int8_t* w, int32_t* c, int M, int
   if (!aligned16(a) || !aligned16(w) || !aligned16(c)) return QG_ERR_MISALIGNED;
   return from_cuda(qg::launch_w8a8_i32(a, w, c, M, N, K, err_word(), static_cast<cudaStream_t>(stream), g_pdl));
 }
+
+int qg_last_cuda_error(void) { return static_cast<int>(t_last_cuda); }
+
+qg_status qg_selftest_wait_timeout(int kind, uint32_t limit, void* stream) {
+  if (kind == 0 ? (limit < 1 || limit > (1u << 22)) : kind == 1 ? (limit < 1 || limit > 1000000u) : true)
+    return QG_ERR_INVALID_ARG;
+  uint32_t* err = err_word();
+  if (!err) return QG_ERR_CUDA;
+  // a zero counter that nothing writes: the library's own 4 bytes, per device
+  static unsigned* zero[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QG_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (!zero[dev]) {
+      void* p = nullptr;
+      cudaError_t e = cudaMalloc(&p, sizeof(unsigned));
+      if (e == cudaSuccess) e = cudaMemset(p, 0, sizeof(unsigned));
+      if (e != cudaSuccess) return from_cuda(e);
+      zero[dev] = static_cast<unsigned*>(p);
+    }
+  }
+  return from_cuda(qg::launch_selftest_wait(kind, limit, zero[dev], err, static_cast<cudaStream_t>(stream)));
+}
+
+const char* qg_last_cuda_error_string(void) { return cudaGetErrorString(t_last_cuda); }
 
 qg_status qg_device_error(uint32_t* code, int clear) {
   uint32_t* p = err_word();

@@ -25,6 +25,12 @@ enum DeviceError : uint32_t {
   kErrTcAccWait = 0x204,
   kErrTcDrain = 0x205,
   kErrMoeWait = 0x301,
+  kErrChainFullWait = 0x401,
+  kErrChainEmptyWait = 0x402,
+  kErrChainDrain = 0x403,
+  kErrChainLevelWait = 0x404,
+  kErrSelftestBarrier = 0x501,
+  kErrSelftestFlag = 0x502,
 };
 
 // Upper bound on polls of one mbarrier phase before a kernel reports a timeout
@@ -74,13 +80,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity to complete. Returns false
-// (after recording `code` in the error word) if it did not complete in time.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t code) {
-  for (uint32_t i = 0; i < kMaxPolls; ++i) {
+// (after recording `code` in the error word) if it did not complete within
+// `polls` polls.
+__device__ __forceinline__ bool mbar_wait_n(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t code,
+                                            uint32_t polls) {
+  for (uint32_t i = 0; i < polls; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
   }
   report_error(err, code);
   return false;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t code) {
+  return mbar_wait_n(bar, parity, err, code, kMaxPolls);
 }
 
 // ---------------------------------------------------------------------------

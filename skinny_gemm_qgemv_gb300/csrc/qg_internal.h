@@ -139,6 +139,57 @@ cudaError_t group_plan_build(const GroupGemv* list, int n, int sms, GroupPlan* o
 void group_plan_free(GroupPlan* p);
 cudaError_t group_launch(const GroupPlan& p, uint32_t* err, cudaStream_t stream, bool pdl);
 
+// W4A16 GEMV chain (w4a16_chain.cu): the M = 1 projections of a decode step
+// with dependency levels, one persistent launch; the weights are copied into
+// a fragment-major layout at plan build.
+constexpr int kChainXBf16 = 0;    // x given as bf16 [K]
+constexpr int kChainXCopy = 1;    // x = bf16(alpha * src[k]), src fp32 [K]
+constexpr int kChainXSwiglu = 2;  // x = bf16(silu(src[k]) * src[K + k] * alpha), src fp32 [2K]
+constexpr int kChainMaxK = 16384;
+struct ChainItem {
+  const uint32_t* wq;
+  const uint16_t* scales;
+  const uint16_t* biases;
+  int N, K, level, op;
+  const void* xsrc;
+  float alpha;
+  float* y;
+};
+struct ChainProj {        // device copy of one projection
+  const uint8_t* packed;  // fragment-major weights
+  const void* xsrc;
+  float* y;
+  float alpha;
+  int op, N, K, level;
+};
+struct ChainSeg {         // a run of row blocks of one projection for one CTA
+  int proj, b0, b1, level;
+};
+struct ChainPlan {
+  uint8_t* d_packed;
+  ChainProj* d_proj;
+  ChainSeg* d_seg;
+  int* d_cta;       // [grid + 1] first segment of each CTA
+  int* d_ltiles;    // [nlevels] row blocks per level
+  unsigned* d_cnt;  // [nlevels + 1] level counters, CTAs finished
+  int nproj, nlevels, grid, ST;
+  uint32_t bfr_bytes;
+  size_t smem, packed_bytes;
+};
+bool chain_proj_ok(int N, int K);
+size_t chain_packed_bytes(int N, int K);
+// items sorted by level (non-decreasing); the repack runs on the legacy
+// stream and is complete when this returns
+cudaError_t chain_plan_build(const ChainItem* items, int n, int sms, ChainPlan* out);
+void chain_plan_free(ChainPlan* p);
+cudaError_t chain_launch(const ChainPlan& p, uint32_t* err, cudaStream_t stream);
+
+// Failure-reporting self-test (selftest.cu): kind 0 waits on an mbarrier no
+// one arrives at for `limit` polls, kind 1 on `flag` (which must stay 0) for
+// `limit` microseconds; both record their code in err and return.
+cudaError_t launch_selftest_wait(int kind, uint32_t limit, const unsigned* flag, uint32_t* err,
+                                 cudaStream_t stream);
+
 // TMA tensor maps (tmap.cu): 2D {inner, outer} with a row stride, 3D
 // {inner, rows, chunks} with row and chunk strides; false if encoding fails.
 bool tmap_2d(CUtensorMap* tm, CUtensorMapDataType dt, const void* ptr, uint64_t inner, uint64_t outer,

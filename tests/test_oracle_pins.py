@@ -622,3 +622,96 @@ def test_w8a8_dequant_scales_with_the_activations():
     y1, _ = oracle.w8a8_dequant(x1, w, sb)
     y2, _ = oracle.w8a8_dequant(x2, w, sb)
     assert np.array_equal(y2, 2 * y1)
+
+
+# ------------------------------------------------ decode-step chain inputs
+# "MLX Runner: An Inference Engine You Can Read", "Architecture: one command
+# buffer per token": each projection consumes the previous one's output,
+# rounded to bf16 (scaled copy, or the SwiGLU of a fused gate/up output).
+
+def test_bf16_rounding_single_step_ties_even_and_subnormals():
+    # 1 + 2^-8 lies halfway between bf16 1 and 1 + 2^-7: ties go to the even 1.0
+    assert oracle.bf16_bits([1 + 2 ** -8])[0] == 0x3F80
+    # 1 + 3 * 2^-8 is halfway between mantissas 1 and 2: the even one
+    assert oracle.bf16_bits([1 + 3 * 2 ** -8])[0] == 0x3F82
+    # just above the tie (by far less than an fp32 ulp): rounds up. Rounding
+    # to fp32 first would land on the tie and give 0x3F80.
+    assert oracle.bf16_bits([1 + 2 ** -8 + 2 ** -40])[0] == 0x3F81
+    assert oracle.bf16_bits([-(1 + 2 ** -8 + 2 ** -40)])[0] == 0xBF81
+    # bf16 subnormals are multiples of 2^-133
+    assert oracle.bf16_bits([2.0 ** -130])[0] == 0x0008
+    assert oracle.bf16_bits([2.5 * 2.0 ** -133])[0] == 0x0002   # tie -> even
+    assert oracle.bf16_bits([3.5 * 2.0 ** -133])[0] == 0x0004
+    # beyond the largest bf16 (0x7F7F): infinity
+    assert oracle.bf16_bits([3.5e38])[0] == 0x7F80
+    assert oracle.bf16_bits([0.0, -0.0]).tolist() == [0x0000, 0x8000]
+
+
+def test_bf16_rounding_of_fp32_values_matches_torch():
+    # from fp32 there is no second rounding: torch's fp32 -> bf16 conversion
+    # (nearest even) must agree on every value
+    r = np.random.default_rng(3)
+    v = (r.standard_normal(200000) * np.exp(r.uniform(-40, 40, 200000))).astype(np.float32)
+    ours = oracle.bf16_bits(v.astype(np.float64))
+    assert np.array_equal(ours, bf16_bits(v))
+
+
+def test_chain_copy_is_scaled_fp32_product_then_bf16():
+    r = np.random.default_rng(4)
+    src = r.standard_normal(640).astype(np.float32)
+    for alpha in (1.0, 0.5, 0.7):
+        prod = (torch.from_numpy(src[:512]) * torch.tensor(alpha, dtype=torch.float32))
+        want = prod.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(oracle.chain_x(src, oracle.X_COPY, alpha, 512), want)
+
+
+def test_chain_swiglu_identities():
+    K = 256
+    r = np.random.default_rng(5)
+    g = r.uniform(-6, 6, K).astype(np.float32)
+    ones = np.ones(K, np.float32)
+    # u = 0: zero activations; g = 0: silu(0) = 0
+    assert not (oracle.chain_x(np.concatenate([g, 0 * ones]), oracle.X_SWIGLU, 1.0, K) & 0x7FFF).any()
+    assert not (oracle.chain_x(np.concatenate([0 * g, ones]), oracle.X_SWIGLU, 1.0, K) & 0x7FFF).any()
+    # silu(g) - silu(-g) = g (sigmoid(g) + sigmoid(-g) = 1): catches a sign or
+    # a dropped factor
+    def val(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).double().numpy()
+    xp = val(oracle.chain_x(np.concatenate([g, ones]), oracle.X_SWIGLU, 1.0, K))
+    xm = val(oracle.chain_x(np.concatenate([-g, ones]), oracle.X_SWIGLU, 1.0, K))
+    assert np.all(np.abs((xp - xm) - g) <= 2.0 ** -8 * (np.abs(xp) + np.abs(xm)) + 1e-30)
+    # large positive gate: silu(g) -> g, so x -> bf16(g u alpha)
+    big = np.full(K, 40.0, np.float32)
+    u = r.standard_normal(K).astype(np.float32)
+    got = val(oracle.chain_x(np.concatenate([big, u]), oracle.X_SWIGLU, 0.25, K))
+    assert np.allclose(got, 10.0 * u, rtol=2 ** -8)
+
+
+def test_chain_of_two_levels_composes_gemv_and_rounding():
+    # level 0: y0 = W0 x; level 1 reads bf16(alpha y0) -- the same as calling the
+    # pinned W4A16 definition on an input rounded by torch
+    N0, K0, N1 = 96, 128, 40
+    w0 = synth.w4_weights(N0, K0, seed=7, slot=1)
+    w1 = synth.w4_weights(N1, N0 - 32, seed=7, slot=2)
+    x = synth.bf16_normal((K0,), 7, 3)
+    y0, _ = oracle.w4a16(*w0, x)
+    y0f = y0[0].astype(np.float32)
+    x1 = oracle.chain_x(y0f, oracle.X_COPY, 0.5, N0 - 32)
+    x1_t = (torch.from_numpy(y0f[:N0 - 32]) * 0.5).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(x1, x1_t)
+    y1, _ = oracle.w4a16(*w1, x1)
+    W1 = synth_dequant(w1)
+    want = W1 @ torch.from_numpy(x1_t.view(np.int16)).view(torch.bfloat16).double().numpy()
+    assert np.allclose(y1[0], want, rtol=1e-12, atol=1e-12)
+
+
+def synth_dequant(w):
+    """Dense float64 weights of an affine W4 g64 matrix, unpacked with numpy."""
+    wq, s, b = (t.numpy() for t in w)
+    N = wq.shape[0]
+    K = wq.shape[1] * 8
+    words = wq.view(np.uint32)
+    q = np.stack([(words >> np.uint32(4 * i)) & np.uint32(15) for i in range(8)], axis=-1).reshape(N, K)
+    sc = s.view(np.float16).astype(np.float64).repeat(64, axis=1)
+    bi = b.view(np.float16).astype(np.float64).repeat(64, axis=1)
+    return sc * q + bi
