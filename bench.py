@@ -35,6 +35,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 import synth  # noqa: E402
@@ -195,12 +196,12 @@ def stack_io(mats, dev, M, seed=1):
     return xs, ys
 
 
-def prime_skinny_workspace(q, mats, M, dev):
+def prime_skinny_workspace(q, mats, M, dev, stream):
     """Allocate (outside any capture) the zero-filled skinny workspace every
-    projection of the stack will share."""
+    projection of the stack will share on `stream`."""
     need = max(q.lib().qg_skinny_workspace_size(M, N, K, 64) for (_, N, K, *_r) in mats)
     if need:
-        q.skinny_workspace(need, dev)
+        q.skinny_workspace(need, dev, stream)
 
 
 def run_stack(q, mats, xs, ys, M, stream):
@@ -343,22 +344,16 @@ def bench_w8a16(q, dev, stream, hbm_peak):
 
 def bench_skinny_stacks(q, mats, dev, stream, hbm_peak):
     """The layer stack at M in {2, 4, 8, 16, 32} activation rows (continuous-batch
-    rows or speculative-tree tokens): one grouped skinny launch per step for
-    M >= 3 (warp-level MMA up to 16 rows, tcgen05 above), 217 launches of the
-    M <= 2 GEMV kernel for M = 2."""
+    rows or speculative-tree tokens): one grouped skinny launch per step
+    (warp-level MMA up to 16 rows, tcgen05 above)."""
     out = {}
     for M in (2, 4, 8, 16, 32):
         xsM, ysM = stack_io(mats, dev, M)
         step = sum(w4_bytes(N, K, M) for (_, N, K, *_r) in mats)
-        if M >= 3:
-            grp = q.SkinnyGroup([(wq, s, b, x, y) for (_, N, K, wq, s, b), x, y in zip(mats, xsM, ysM)])
-            t, _ = time_graph(lambda: grp.run(stream), 10, stream)
-            grp.close()
-            form = "one grouped skinny launch over the 217 projections"
-        else:
-            prime_skinny_workspace(q, mats, M, dev)
-            t, _ = time_graph(lambda: run_stack(q, mats, xsM, ysM, M, stream), 10, stream)
-            form = "217 launches of the M <= 2 GEMV kernel in one graph"
+        grp = q.SkinnyGroup([(wq, s, b, x, y) for (_, N, K, wq, s, b), x, y in zip(mats, xsM, ysM)])
+        t, _ = time_graph(lambda: grp.run(stream), 10, stream)
+        grp.close()
+        form = "one grouped skinny launch over the 217 projections"
         out[f"M{M}"] = {"value": step / t / 1e9, "unit": "GB/s", "frac": step / t / 1e9 / hbm_peak,
                         "ms_per_step": t * 1e3, "tokens_per_s": M / t, "bytes_per_step": step, "form": form}
         del xsM, ysM
@@ -481,7 +476,48 @@ def bench_w8a8(q, dev, stream, N, l2_bytes):
 CASES = ["gemv_lm_head", "gemv_down", "gemv_q", "skinny16_gate_up", "skinny16_down", "moe_T1", "moe_T16",
          "w8a16_lm_head",
          "w8a8_12288", "hadamard_16x4096", "gemv_group_4layers", "skinny16_group_4layers", "chain_4layers",
-         "chain_flat_4layers"]
+         "chain_flat_4layers", "chain_trace"]
+
+
+def chain_trace_summary(q, dev):
+    """The dependency-ordered chain of the full stack with its level trace on:
+    per level kind (q/k/v, o, gate_up, down, lm_head) the mean over layers of
+    the level's duration (previous level's last publish to this one's) and of
+    its parts, medians over the CTAs: release (previous level complete -> this
+    CTA's wait ends), build (wait end -> input fragments built) and tiles
+    (built -> the CTA's last publish), plus the slowest CTA's tiles."""
+    mats = build_stack(q, dev, 1)
+    x0 = synth.bf16_normal((4096,), 1, 4999, device=dev)
+    ch = q.GemvChain(decoder_chain_items(q, mats, x0, dev))
+    for _ in range(3):
+        ch.run()
+    ch.trace(True)
+    ch.run()
+    torch.cuda.synchronize()
+    tr = ch.trace_read().astype(np.float64)
+    ch.close()
+    tr[tr == 0] = np.nan
+    tr = (tr - np.nanmin(tr)) / 1e3  # us
+    done = np.nanmax(tr[:, :, 3], axis=0)
+    L = tr.shape[1]
+    kinds = ["qkv", "o", "gate_up", "down"]
+    rows = {}
+    for l in range(1, L):
+        k = kinds[l % 4] if l < L - 1 else "lm_head"
+        prev = done[l - 1]
+        wait_end, built, pub = tr[:, l, 1], tr[:, l, 2], tr[:, l, 3]
+        built = np.where(np.isnan(built), wait_end, built)
+        r = rows.setdefault(k, {"n": 0, "level_us": 0.0, "release_us": 0.0, "build_us": 0.0, "tiles_us": 0.0,
+                                "tiles_max_us": 0.0})
+        r["n"] += 1
+        r["level_us"] += done[l] - prev
+        r["release_us"] += np.nanmedian(wait_end - prev)
+        r["build_us"] += np.nanmedian(built - wait_end)
+        r["tiles_us"] += np.nanmedian(pub - built)
+        r["tiles_max_us"] += np.nanmax(pub - built)
+    out = {k: {f: (round(v / r["n"], 2) if f != "n" else v) for f, v in r.items()} for k, r in rows.items()}
+    out["total_us"] = round(float(np.nanmax(tr)), 1)
+    return out
 
 
 def run_case(args):
@@ -492,6 +528,9 @@ def run_case(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     c = args.case
+    if c == "chain_trace":
+        print(json.dumps(chain_trace_summary(q, dev)), flush=True)
+        return
     if c == "gemv_group_4layers":
         # the grouped launch over 4 decoder layers + the lm_head (0.78 GB)
         mats = build_stack(q, dev, 1, layers=4)
@@ -727,7 +766,7 @@ def main():
         step16 = sum(w4_bytes(N, K, 16) for (_, N, K, *_r) in mats)
         grp16 = q.SkinnyGroup([(wq, s, b, x, y) for (_, N, K, wq, s, b), x, y in zip(mats, xs16, ys16)])
         t16, _ = time_graph(lambda: grp16.run(stream), 20, stream)
-        prime_skinny_workspace(q, mats, 16, dev)
+        prime_skinny_workspace(q, mats, 16, dev, stream)
         t16s, _ = time_graph(lambda: run_stack(q, mats, xs16, ys16, 16, stream), 20, stream)
         extras["m16_stack"] = {"value": step16 / t16 / 1e9, "unit": "GB/s", "frac": step16 / t16 / 1e9 / hbm_peak,
                                "ms_per_step": t16 * 1e3, "tokens_per_s": 16 / t16, "bytes_per_step": step16,

@@ -232,6 +232,24 @@ QG_API void qgemv_w4a16_chain_destroy(qg_w4_chain *chain);
 QG_API size_t qgemv_w4a16_chain_bytes(const qg_w4_chain *chain);
 
 /*
+ * qgemv_w4a16_chain_trace_enable / _trace_read -- per-run timing of the chain's
+ * levels (off by default). enable != 0 allocates and zeroes a buffer of
+ * grid x levels x 4 uint64 (grid = qgemv_w4a16_chain_trace_shape's first
+ * value, levels the number of distinct levels); enable = 0 frees it. While it
+ * exists every run writes, per (CTA, level), the global timer in
+ * nanoseconds when: [0] the CTA's first consumer warp reaches the level, [1]
+ * its wait for the level below ends, [2] it has built the level's input, [3]
+ * the CTA published its last row block of the level (0 where a CTA has no
+ * work in a level; [3] keeps the latest stamp across runs until re-enabled).
+ * _trace_read synchronizes the device and copies `count` values (at most the
+ * buffer's) into host memory. _trace_shape writes grid and levels.
+ * No run may be pending when tracing is switched.
+ */
+QG_API qg_status qgemv_w4a16_chain_trace_enable(qg_w4_chain *chain, int enable);
+QG_API qg_status qgemv_w4a16_chain_trace_read(const qg_w4_chain *chain, uint64_t *host, size_t count);
+QG_API void qgemv_w4a16_chain_trace_shape(const qg_w4_chain *chain, int *grid, int *levels);
+
+/*
  * qgemm_w4a16_skinny -- Y = X W^T for a few activation rows, each weight read
  * once for all rows ("Krill Teardown", "Core mechanisms"; Uzu article,
  * "Producing several tokens from one model pass").
@@ -269,8 +287,8 @@ QG_API size_t qg_skinny_workspace_size(int M, int N, int K, int group_size);
  *   qg_w4_gemm_desc  one projection: wq uint32 [N][K/8], scales/biases fp16
  *                    [N][K/64], x bf16 [M][K], y fp32 [M][N]; every pointer
  *                    16-byte aligned device memory of the current device;
- *                    3 <= M <= 32, N >= 1, K a multiple of 512 and at most
- *                    32768. All M of one group lie in one class, 3..16 or
+ *                    2 <= M <= 32, N >= 1, K a multiple of 512 and at most
+ *                    32768. All M of one group lie in one class, 2..16 or
  *                    17..32 (other shapes, and mixed classes, return
  *                    QG_ERR_UNSUPPORTED).
  *   qgemm_w4a16_skinny_group_create  validates the count descriptors

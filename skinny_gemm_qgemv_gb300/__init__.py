@@ -34,6 +34,7 @@ EXPORTS = [
     "qgemv_w8a16", "qgemm_affine",
     "qgemv_w4a16_chain_create", "qgemv_w4a16_chain_run", "qgemv_w4a16_chain_destroy", "qgemv_w4a16_chain_bytes",
     "qg_last_cuda_error", "qg_last_cuda_error_string", "qg_selftest_wait_timeout",
+    "qgemv_w4a16_chain_trace_enable", "qgemv_w4a16_chain_trace_read", "qgemv_w4a16_chain_trace_shape",
 ]
 
 X_BF16, X_COPY, X_SWIGLU = 0, 1, 2
@@ -131,6 +132,12 @@ def lib() -> ctypes.CDLL:
         L.qg_last_cuda_error.argtypes = []
         L.qg_last_cuda_error_string.restype = ctypes.c_char_p
         L.qg_last_cuda_error_string.argtypes = []
+        L.qgemv_w4a16_chain_trace_enable.restype = I
+        L.qgemv_w4a16_chain_trace_enable.argtypes = [P, I]
+        L.qgemv_w4a16_chain_trace_read.restype = I
+        L.qgemv_w4a16_chain_trace_read.argtypes = [P, P, Z]
+        L.qgemv_w4a16_chain_trace_shape.restype = None
+        L.qgemv_w4a16_chain_trace_shape.argtypes = [P, ctypes.POINTER(I), ctypes.POINTER(I)]
         L.qgemv_w4a16_chain_bytes.restype = Z
         L.qgemv_w4a16_chain_bytes.argtypes = [P]
         _lib = L
@@ -222,12 +229,15 @@ def qgemv_w8a16(wq, scales, x, y=None, stream=None):
 _WS = {}
 
 
-def skinny_workspace(nbytes, device):
-    """A zero-filled workspace for qgemm_w4a16_skinny, cached per device and
-    reused (every call leaves it zero-filled). Calls sharing it must be
-    ordered on one stream. Inside a stream capture a fresh one is made (the
-    zero fill is captured too) and not cached."""
-    key = (str(device), )
+def skinny_workspace(nbytes, device, stream=None):
+    """A zero-filled workspace for qgemm_w4a16_skinny, cached per (device,
+    stream) and reused (every call leaves it zero-filled): calls on one stream
+    are ordered, so they may share it, and calls on different streams get
+    different ones. Inside a stream capture a fresh one is made (the zero fill
+    is captured too) and not cached."""
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    key = (str(device), stream.cuda_stream)
     ws = _WS.get(key)
     if ws is not None and ws.numel() >= nbytes:
         return ws
@@ -249,7 +259,7 @@ def qgemm_w4a16_skinny(wq, scales, biases, x, y=None, workspace=None, stream=Non
         y = torch.empty(M, N, device=wq.device, dtype=torch.float32)
     need = lib().qg_skinny_workspace_size(M, N, K, K // scales.shape[1])
     if workspace is None and need:
-        workspace = skinny_workspace(need, wq.device)
+        workspace = skinny_workspace(need, wq.device, stream)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().qgemm_w4a16_skinny(_p(wq), _p(scales), _p(biases), _p(x), _p(y), M, N, K,
                                     K // scales.shape[1], _p(workspace), ws_bytes, _stream(stream)),
@@ -325,6 +335,20 @@ class GemvChain:
     def device_bytes(self):
         return lib().qgemv_w4a16_chain_bytes(self._h)
 
+    def trace(self, enable=True):
+        """Switch per-(CTA, level) timestamps on or off (see the header)."""
+        _check(lib().qgemv_w4a16_chain_trace_enable(self._h, 1 if enable else 0), "qgemv_w4a16_chain_trace_enable")
+
+    def trace_read(self):
+        """The stamps of the last runs as a uint64 numpy array [grid][levels][4] (ns)."""
+        import numpy as np
+        g, lv = ctypes.c_int(0), ctypes.c_int(0)
+        lib().qgemv_w4a16_chain_trace_shape(self._h, ctypes.byref(g), ctypes.byref(lv))
+        out = np.zeros((g.value, lv.value, 4), dtype=np.uint64)
+        _check(lib().qgemv_w4a16_chain_trace_read(self._h, out.ctypes.data_as(ctypes.c_void_p), out.size),
+               "qgemv_w4a16_chain_trace_read")
+        return out
+
     def close(self):
         if self._h:
             lib().qgemv_w4a16_chain_destroy(self._h)
@@ -338,7 +362,7 @@ class GemvChain:
 
 
 class SkinnyGroup:
-    """Many independent skinny projections (3 <= M <= 32) as one persistent
+    """Many independent skinny projections (2 <= M <= 32) as one persistent
     tensor-core launch.
 
     `items` is a list of (wq, scales, biases, x, y) CUDA tensors with the

@@ -266,6 +266,25 @@ void qgemv_w4a16_chain_destroy(qg_w4_chain* chain) {
   delete chain;
 }
 
+qg_status qgemv_w4a16_chain_trace_enable(qg_w4_chain* chain, int enable) {
+  if (!chain) return QG_ERR_INVALID_ARG;
+  return from_cuda(qg::chain_set_trace(&chain->plan, enable != 0));
+}
+
+qg_status qgemv_w4a16_chain_trace_read(const qg_w4_chain* chain, uint64_t* host, size_t count) {
+  if (!chain || !host || !chain->plan.d_trace) return QG_ERR_INVALID_ARG;
+  const size_t n = (size_t)chain->plan.grid * chain->plan.nlevels * 4;
+  if (count > n) count = n;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(host, chain->plan.d_trace, count * sizeof(uint64_t), cudaMemcpyDeviceToHost);
+  return from_cuda(e);
+}
+
+void qgemv_w4a16_chain_trace_shape(const qg_w4_chain* chain, int* grid, int* levels) {
+  if (grid) *grid = chain ? chain->plan.grid : 0;
+  if (levels) *levels = chain ? chain->plan.nlevels : 0;
+}
+
 size_t qgemv_w4a16_chain_bytes(const qg_w4_chain* chain) {
   if (!chain) return 0;
   const qg::ChainPlan& p = chain->plan;

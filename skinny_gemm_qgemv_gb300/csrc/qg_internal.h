@@ -172,6 +172,7 @@ struct ChainPlan {
   int* d_cta;       // [grid + 1] first segment of each CTA
   int* d_ltiles;    // [nlevels] row blocks per level
   unsigned* d_cnt;  // [nlevels + 1] level counters, CTAs finished
+  unsigned long long* d_trace;  // null, or [grid][nlevels][4] timestamps
   int nproj, nlevels, grid, ST;
   uint32_t bfr_bytes;
   size_t smem, packed_bytes;
@@ -183,6 +184,8 @@ size_t chain_packed_bytes(int N, int K);
 cudaError_t chain_plan_build(const ChainItem* items, int n, int sms, ChainPlan* out);
 void chain_plan_free(ChainPlan* p);
 cudaError_t chain_launch(const ChainPlan& p, uint32_t* err, cudaStream_t stream);
+// allocate (zeroed) or free the per-(CTA, level) timestamp buffer
+cudaError_t chain_set_trace(ChainPlan* p, bool enable);
 
 // Failure-reporting self-test (selftest.cu): kind 0 waits on an mbarrier no
 // one arrives at for `limit` polls, kind 1 on `flag` (which must stay 0) for

@@ -47,6 +47,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <numeric>
 #include <vector>
 
 #include "qg_common.cuh"
@@ -74,6 +75,7 @@ struct ChainArgs {
   int ST;
   uint32_t bfr_bytes;      // B-fragment area: (max K / 64) x 128 bytes
   uint32_t* err;
+  unsigned long long* trace;  // null, or [grid][nlevels][4] globaltimer stamps (see chain_trace)
 };
 
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -110,10 +112,26 @@ __device__ __forceinline__ float2 ldcg_f2(const float* p) {
   asm volatile("ld.global.cg.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
   return v;
 }
+// Trace stamps of one (CTA, level), in globaltimer nanoseconds: 0 the first
+// consumer warp reaches the level, 1 its wait for the level below ends, 2 its
+// input fragments are built, 3 the CTA's last row block of the level is
+// published. Only with a trace buffer (off by default).
+__device__ __forceinline__ void stamp(unsigned long long* tr, int nlevels, int level, int field, bool latest);
+
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+
+__device__ __forceinline__ void stamp(unsigned long long* tr, int nlevels, int level, int field, bool latest) {
+  if (!tr) return;
+  unsigned long long* p = tr + ((size_t)blockIdx.x * nlevels + level) * 4 + field;
+  const unsigned long long t = globaltimer();
+  if (latest)
+    atomicMax(p, t);
+  else
+    *p = t;
 }
 
 // bf16 rounding (nearest even) of an fp32 value, returned as fp32
@@ -148,7 +166,7 @@ __device__ __forceinline__ bool wait_level(const unsigned* cnt, unsigned target,
       return false;
     }
     __nanosleep(ns);
-    if (ns < 128) ns <<= 1;
+    if (ns < 64) ns <<= 1;
   }
 }
 
@@ -194,23 +212,32 @@ __device__ __forceinline__ void load_x16(const ChainProj& p, int k0, int c, floa
 }
 
 // B fragments and the fold constants (P, Q, sum x) of this warp's groups of a
-// projection. Lane (j, c) = (lane / 4, lane % 4) handles group w + 8 (j0 + j).
+// projection. In pass ps lane (j, c) = (lane / 4, lane % 4) handles group
+// w + 8 (8 ps + j).
 __device__ void build_x(const ChainProj& p, int w, int lane, uint32_t bfr_s, uint32_t kc_s) {
+  constexpr int kPass = kChainMaxK / 64 / kChWarps / 8;  // passes of 8 groups a warp may need
   const int G = p.K >> 6;
   const int c = lane & 3;
-  for (int j0 = 0; w + kChWarps * j0 < G; j0 += 8) {
-    const int gi = w + kChWarps * (j0 + (lane >> 2));
-    const bool act = gi < G;
-    float v[16];
-    if (act) {
-      load_x16(p, 64 * gi, c, v);
+  // every pass's loads first: one round trip to L2 for the whole input
+  float v[kPass][16];
+#pragma unroll
+  for (int ps = 0; ps < kPass; ++ps) {
+    const int gi = w + kChWarps * (8 * ps + (lane >> 2));
+    if (gi < G) {
+      load_x16(p, 64 * gi, c, v[ps]);
     } else {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = 0.f;
+      for (int i = 0; i < 16; ++i) v[ps][i] = 0.f;
     }
+  }
+#pragma unroll
+  for (int ps = 0; ps < kPass; ++ps) {
+    if (w + kChWarps * 8 * ps >= G) break;  // warp-uniform
+    const int gi = w + kChWarps * (8 * ps + (lane >> 2));
+    const bool act = gi < G;
     float amax = 0.f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[ps][i]));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
     const int sig = fp16_prescale_exp(amax);
@@ -219,11 +246,11 @@ __device__ void build_x(const ChainProj& p, int w, int lane, uint32_t bfr_s, uin
     float sa = 0.f, sb = 0.f, sx = 0.f;
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
-      bq[2 * s] = f16x2_rn(v[4 * s] * down, v[4 * s + 1] * down);
-      bq[2 * s + 1] = f16x2_rn(v[4 * s + 2] * down * 0.0625f, v[4 * s + 3] * down * 0.0625f);
+      bq[2 * s] = f16x2_rn(v[ps][4 * s] * down, v[ps][4 * s + 1] * down);
+      bq[2 * s + 1] = f16x2_rn(v[ps][4 * s + 2] * down * 0.0625f, v[ps][4 * s + 3] * down * 0.0625f);
       sa += f16x2_sum(bq[2 * s]);
       sb += f16x2_sum(bq[2 * s + 1]);
-      sx += (v[4 * s] + v[4 * s + 1]) + (v[4 * s + 2] + v[4 * s + 3]);
+      sx += (v[ps][4 * s] + v[ps][4 * s + 1]) + (v[ps][4 * s + 2] + v[ps][4 * s + 3]);
     }
 #pragma unroll
     for (int o = 1; o <= 2; o <<= 1) {
@@ -352,6 +379,7 @@ __global__ void __maxnreg__(168) w4a16_chain_kernel(const ChainArgs a) {
     for (int si = s0; si < s1 && ok; ++si) {
       const ChainSeg sg = a.seg[si];
       const ChainProj p = a.proj[sg.proj];
+      if (w == 0 && lane == 0 && sg.level != cur_level) stamp(a.trace, a.nlevels, sg.level, 0, false);
       if (sg.level > 0 && waited < sg.level - 1) {
         bool got = true;
         if (lane == 0) got = wait_level(&a.cnt[sg.level - 1], (unsigned)a.level_tiles[sg.level - 1], a.err, abortp);
@@ -362,6 +390,7 @@ __global__ void __maxnreg__(168) w4a16_chain_kernel(const ChainArgs a) {
           break;
         }
         waited = sg.level - 1;
+        if (w == 0 && lane == 0) stamp(a.trace, a.nlevels, sg.level, 1, false);
       }
       if (sg.proj != cur_proj) {
         // a new projection: new B fragments unless it reads the same input
@@ -371,6 +400,7 @@ __global__ void __maxnreg__(168) w4a16_chain_kernel(const ChainArgs a) {
         if (!same) {
           build_x(p, w, lane, bfr_s, kc_s);
           __syncwarp();
+          if (w == 0 && lane == 0) stamp(a.trace, a.nlevels, sg.level, 2, false);
         }
         cur_proj = sg.proj;
         cur_x = p.xsrc;
@@ -438,10 +468,12 @@ __global__ void __maxnreg__(168) w4a16_chain_kernel(const ChainArgs a) {
                 p.y[row] = tot;
               }
               __syncwarp();  // the lanes' stores precede lane 0's release below
-              if (b == sg.b1 - 1 && lane == 0)
+              if (b == sg.b1 - 1 && lane == 0) {
                 asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(&a.cnt[sg.level]),
                              "r"((unsigned)(sg.b1 - sg.b0))
                              : "memory");
+                stamp(a.trace, a.nlevels, sg.level, 3, true);
+              }
             }
             ++tiles;
           }
@@ -532,19 +564,20 @@ cudaError_t chain_plan_build(const ChainItem* items, int n, int sms, ChainPlan* 
   }
   const int grid = std::max(1, sms);
   // Tiles (one 16-row block of one projection, cost K) are handed out level by
-  // level. Per level the CTAs are filled to a common water level W (the work
-  // of every CTA below W after the level, CTAs already above it get none);
-  // CTA c takes, in CTA order, the contiguous run of the level's tiles whose
-  // ends are the tile boundaries nearest to the running sum of the fills, so
-  // every CTA's cumulative work stays within one tile of W at every level
-  // boundary and its tiles of one projection are consecutive (one segment).
+  // level: a level completes when its slowest CTA is done, so each level's
+  // tiles are split on their own into `grid` contiguous runs of equal cost
+  // (ends at the nearest tile boundary), and run r goes to CTA (r + rot) % grid
+  // with rot advancing by a step coprime to the grid, so that the CTAs taking
+  // one tile more than the others change from level to level. A CTA's tiles
+  // of one projection are consecutive (one segment).
   std::vector<std::vector<ChainSeg>> per(grid);
   std::vector<int> level_tiles(nlevels, 0);
-  std::vector<double> work(grid, 0.0);
+  int rot = 0, step = grid / 2 + 1;
+  while (step > 1 && std::gcd(step, grid) != 1) --step;
   for (int i0 = 0; i0 < n;) {
     int i1 = i0;
     while (i1 < n && lev[i1] == lev[i0]) ++i1;
-    std::vector<int> tp, tb;       // the level's tiles: projection, block
+    std::vector<int> tp, tb;  // the level's tiles: projection, block
     std::vector<double> prefix{0.0};
     for (int i = i0; i < i1; ++i)
       for (int b = 0; b < (items[i].N + 15) / 16; ++b) {
@@ -554,36 +587,23 @@ cudaError_t chain_plan_build(const ChainItem* items, int n, int sms, ChainPlan* 
       }
     const int T = (int)tp.size();
     level_tiles[lev[i0]] = T;
-    // water level: sum over c of max(0, W - work[c]) = level cost
-    std::vector<double> sorted(work);
-    std::sort(sorted.begin(), sorted.end());
-    double W = 0.0, acc = 0.0;
-    for (int k = 0; k < grid; ++k) {
-      acc += sorted[k];
-      const double w = (acc + prefix[T]) / (k + 1);
-      if (k + 1 == grid || w <= sorted[k + 1]) {
-        W = w;
-        break;
-      }
-    }
-    double fill = 0.0;
     int t = 0;
-    for (int c = 0; c < grid; ++c) {
-      fill += std::max(0.0, W - work[c]);
-      int e = (int)(std::lower_bound(prefix.begin(), prefix.end(), fill) - prefix.begin());
+    for (int r = 0; r < grid; ++r) {
+      const double end_cost = prefix[T] * (r + 1) / grid;
+      int e = (int)(std::lower_bound(prefix.begin(), prefix.end(), end_cost) - prefix.begin());
       if (e > T) e = T;
-      if (e > 0 && fill - prefix[e - 1] < prefix[e] - fill) --e;  // nearest boundary
-      if (c == grid - 1) e = T;
+      if (e > 0 && end_cost - prefix[e - 1] < prefix[e] - end_cost) --e;  // nearest boundary
+      if (r == grid - 1) e = T;
       e = std::max(e, t);
+      auto& v = per[(r + rot) % grid];
       for (; t < e; ++t) {
-        auto& v = per[c];
         if (!v.empty() && v.back().proj == tp[t] && v.back().b1 == tb[t])
           v.back().b1 = tb[t] + 1;
         else
           v.push_back(ChainSeg{tp[t], tb[t], tb[t] + 1, lev[tp[t]]});
-        work[c] += items[tp[t]].K;
       }
     }
+    rot = (rot + step) % grid;
     i0 = i1;
   }
   std::vector<ChainSeg> segs;
@@ -652,6 +672,7 @@ void chain_plan_free(ChainPlan* p) {
   cudaFree(p->d_cta);
   cudaFree(p->d_ltiles);
   cudaFree(p->d_cnt);
+  cudaFree(p->d_trace);
   *p = ChainPlan{};
 }
 
@@ -666,6 +687,7 @@ cudaError_t chain_launch(const ChainPlan& p, uint32_t* err, cudaStream_t stream)
   a.ST = p.ST;
   a.bfr_bytes = p.bfr_bytes;
   a.err = err;
+  a.trace = p.d_trace;
   cudaError_t e = allow_max_smem(w4a16_chain_kernel);
   if (e != cudaSuccess) return e;
   // every CTA must be resident at once (CTAs wait for each other's levels):
@@ -681,6 +703,19 @@ cudaError_t chain_launch(const ChainPlan& p, uint32_t* err, cudaStream_t stream)
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, w4a16_chain_kernel, a);
+}
+
+cudaError_t chain_set_trace(ChainPlan* p, bool enable) {
+  if (!enable) {
+    cudaError_t e = cudaFree(p->d_trace);
+    p->d_trace = nullptr;
+    return e;
+  }
+  if (p->d_trace) return cudaSuccess;
+  const size_t bytes = sizeof(unsigned long long) * (size_t)p->grid * p->nlevels * 4;
+  cudaError_t e = cudaMalloc(&p->d_trace, bytes);
+  if (e == cudaSuccess) e = cudaMemset(p->d_trace, 0, bytes);
+  return e;
 }
 
 }  // namespace qg

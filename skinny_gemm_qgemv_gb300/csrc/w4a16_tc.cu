@@ -1159,8 +1159,11 @@ cudaError_t launch_w4a16_tc(const uint32_t* wq, const uint16_t* sc, const uint16
 // persistent grid; each CTA takes a contiguous range of equal cost.
 // ---------------------------------------------------------------------------
 int tc_group_check(const TcGroupItem* list, int n) {
+  // a grouped launch also takes M = 2 (single calls of M <= 2 go to the GEMV
+  // kernel): the activation tile is padded to 16 rows either way
   for (int i = 0; i < n; ++i)
-    if (!tc_path_ok(list[i].M, list[i].N, list[i].K)) return 1;
+    if (!(list[i].M == 2 ? tc_path_ok(3, list[i].N, list[i].K) : tc_path_ok(list[i].M, list[i].N, list[i].K)))
+      return 1;
   for (int i = 1; i < n; ++i)
     if ((list[i].M <= 16) != (list[0].M <= 16)) return 2;
   return 0;

@@ -159,7 +159,7 @@ def test_skinny_group_validation(L):
     assert f(make((16, 128, 4096)), 1, 64, None) == 1
     assert f(make((16, 128, 4096), (16, 0, 4096)), 2, 64, ctypes.byref(out)) == 1    # N < 1
     assert f(make((33, 128, 4096)), 1, 64, ctypes.byref(out)) == 1                   # M > 32
-    assert f(make((2, 128, 4096)), 1, 64, ctypes.byref(out)) == 3                    # M < 3
+    assert f(make((1, 128, 4096)), 1, 64, ctypes.byref(out)) == 3                    # M < 2
     assert f(make((16, 128, 4096), (16, 128, 448)), 2, 64, ctypes.byref(out)) == 3   # K % 512
     assert f(make((16, 128, 65536)), 1, 64, ctypes.byref(out)) == 3                  # K > 32768
     assert f(make((16, 128, 4096), (17, 128, 4096)), 2, 64, ctypes.byref(out)) == 3  # mixed classes

@@ -422,7 +422,7 @@ def test_gemv_group_full_stack_layer_sampled(q):
 
 # ------------------------------------------- grouped skinny GEMM (tcgen05)
 
-@pytest.mark.parametrize("M", [3, 16, 17, 32])
+@pytest.mark.parametrize("M", [2, 3, 16, 17, 32])
 def test_skinny_group_vs_oracle(q, M):
     # several projections of mixed N (ragged last tiles, a one-row matrix) and
     # mixed K in one launch; each against the oracle
