@@ -467,8 +467,22 @@ def bench_w8a8(q, dev, stream, N, l2_bytes):
         for _ in range(50):
             q.hadamard32_quant_i8(xa, sb, qa, sa, stream=stream)
     th, _ = time_graph(fh, 3, stream)
+    # the fused path: transform + int8 + product + dequant in one launch (y fp32)
+    _, swq = q.hadamard32_quant_i8(wf, sb)
+    y = torch.empty(M, N, device=dev)
+    q.gemm_w8a8_hadamard(xa, sb, ws[0], swq, y, stream=stream)  # workspace allocated outside the capture
+
+    def ff():
+        for w in ws:
+            q.gemm_w8a8_hadamard(xa, sb, w, swq, y, stream=stream)
+    tf, _ = time_graph(ff, 5, stream)
+    tf /= copies
+    fbytes = N * K + 4 * N + 2 * M * K + 4 * M * N
     return {"us_per_call": t * 1e6, "GB_per_s": nbytes / t / 1e9, "weight_copies_rotated": int(copies),
-            "hadamard_quant_us_per_call": th / 50 * 1e6}
+            "hadamard_quant_us_per_call": th / 50 * 1e6,
+            "two_launch_path_us": (t + th / 50) * 1e6,
+            "fused": {"us_per_call": tf * 1e6, "GB_per_s": fbytes / tf / 1e9, "algorithmic_bytes": fbytes,
+                      "form": "gemm_w8a8_hadamard: one cooperative launch, x bf16 -> y fp32"}}
 
 
 # --------------------------------------------------------------------------- single cases (profiling)
@@ -476,7 +490,7 @@ def bench_w8a8(q, dev, stream, N, l2_bytes):
 CASES = ["gemv_lm_head", "gemv_down", "gemv_q", "skinny16_gate_up", "skinny16_down", "moe_T1", "moe_T16",
          "w8a16_lm_head",
          "w8a8_12288", "hadamard_16x4096", "gemv_group_4layers", "skinny16_group_4layers", "chain_4layers",
-         "chain_flat_4layers", "chain_trace"]
+         "chain_flat_4layers", "chain_trace", "w8a8_fused_12288", "w8a8_fused_4096"]
 
 
 def chain_trace_summary(q, dev):
@@ -592,6 +606,15 @@ def run_case(args):
         w = torch.randint(-127, 128, (N, K), dtype=torch.int8, device=dev)
         f = lambda: q.gemm_w8a8_i32(a, w)  # noqa: E731
         nbytes = N * K + 16 * K + 16 * N * 4
+    elif c.startswith("w8a8_fused_"):
+        N, K, M = int(c.split("_")[-1]), 4096, 16
+        wf = synth.normal_f32((N, K), 0.02, 4, 20, dev).to(torch.bfloat16)
+        sb = synth.sign_bits(K, 4, 5, dev)
+        wq, swq = q.hadamard32_quant_i8(wf, sb)
+        xa = synth.outlier_activations(M, K, 4, 0, dev)
+        y = torch.empty(M, N, device=dev)
+        f = lambda: q.gemm_w8a8_hadamard(xa, sb, wq, swq, y)  # noqa: E731
+        nbytes = N * K + 4 * N + 2 * M * K + 4 * M * N
     elif c == "hadamard_16x4096":
         x = synth.outlier_activations(16, 4096, 4, 0, dev)
         sb = synth.sign_bits(4096, 4, 5, dev)
@@ -798,6 +821,7 @@ def main():
         for N in (4096, 12288):
             r = bench_w8a8(q, dev, stream, N, l2)
             r["frac"] = r["GB_per_s"] / hbm_peak
+            r["fused"]["frac"] = r["fused"]["GB_per_s"] / hbm_peak
             extras[f"w8a8_{N}x4096"] = r
 
     cpu = cpu_baseline(args.cpu_seconds, mats, xs) if rank == 0 else None

@@ -491,6 +491,40 @@ QG_API qg_status gemm_w8a8_i32(const int8_t *a, const int8_t *w, int32_t *c,
                         int M, int N, int K, void *stream);
 
 /*
+ * gemm_w8a8_hadamard -- the whole int8 matrix path of the Uzu article ("How
+ * Uzu optimizes bytes and tokens per pass") in ONE launch: the activations'
+ * block-32 randomized Hadamard transform and per-row int8 quantization, the
+ * exact int8 product with the weights, and the dequantization,
+ *     y[m][n] = C[m][n] * s_a[m] * s_w[n] / 32,
+ * where (q_a, s_a) = hadamard32_quant_i8(x_bf16, sign_bits) bit for bit and
+ * C = q_a w^T exactly (int32). The weights must carry the same transform and
+ * quantizer per row (w = q_w, sw = s_w of hadamard32_quant_i8 on the weight
+ * rows with the same sign_bits), so that C s_a s_w / 32 approximates x . w.
+ *
+ *   x_bf16     bf16 [M][K], 1 <= M <= 16; finite values (a NaN or infinity
+ *              in a row makes that row's outputs meaningless).
+ *   sign_bits  uint32 [K/32] as in hadamard32_quant_i8.
+ *   w          int8 [N][K] (row-major), sw fp32 [N]; N >= 1.
+ *   y          fp32 [M][N] (output), computed in fp32 as
+ *              (float)C * s_a * (s_w * 0.03125).
+ *   K          a multiple of 1024 and at most 4096 (others:
+ *              QG_ERR_UNSUPPORTED; gemm_w8a8_i32 and hadamard32_quant_i8
+ *              serve them).
+ *   workspace / ws_bytes: at least qg_w8a8_hadamard_workspace_size(M, K)
+ *              bytes of device memory, 16-byte aligned, zero-filled before
+ *              its first use; every call leaves it zero-filled again, so one
+ *              workspace serves any sequence of calls ordered on one stream
+ *              (after a reported device timeout zero-fill it again).
+ * One cooperative launch (one CTA per SM, all resident at once: the CTAs
+ * share the transform and wait for each other twice); capturable in a CUDA
+ * graph.
+ */
+QG_API qg_status gemm_w8a8_hadamard(const uint16_t *x_bf16, const uint32_t *sign_bits, const int8_t *w,
+                                    const float *sw, float *y, int M, int N, int K, void *workspace,
+                                    size_t ws_bytes, void *stream);
+QG_API size_t qg_w8a8_hadamard_workspace_size(int M, int K);
+
+/*
  * qg_set_pdl -- process-wide launch mode. With enable != 0 every kernel is
  * launched with programmatic dependent launch, so its weight streaming may
  * start while the previous kernel on the stream is still draining. Activations

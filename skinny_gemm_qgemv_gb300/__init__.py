@@ -35,6 +35,7 @@ EXPORTS = [
     "qgemv_w4a16_chain_create", "qgemv_w4a16_chain_run", "qgemv_w4a16_chain_destroy", "qgemv_w4a16_chain_bytes",
     "qg_last_cuda_error", "qg_last_cuda_error_string", "qg_selftest_wait_timeout",
     "qgemv_w4a16_chain_trace_enable", "qgemv_w4a16_chain_trace_read", "qgemv_w4a16_chain_trace_shape",
+    "gemm_w8a8_hadamard", "qg_w8a8_hadamard_workspace_size",
 ]
 
 X_BF16, X_COPY, X_SWIGLU = 0, 1, 2
@@ -126,6 +127,10 @@ def lib() -> ctypes.CDLL:
         L.qgemv_w4a16_chain_run.argtypes = [P, P]
         L.qgemv_w4a16_chain_destroy.restype = None
         L.qgemv_w4a16_chain_destroy.argtypes = [P]
+        L.gemm_w8a8_hadamard.restype = I
+        L.gemm_w8a8_hadamard.argtypes = [P, P, P, P, P, I, I, I, P, Z, P]
+        L.qg_w8a8_hadamard_workspace_size.restype = Z
+        L.qg_w8a8_hadamard_workspace_size.argtypes = [I, I]
         L.qg_selftest_wait_timeout.restype = I
         L.qg_selftest_wait_timeout.argtypes = [I, ctypes.c_uint32, P]
         L.qg_last_cuda_error.restype = I
@@ -444,6 +449,37 @@ def hadamard32_quant_i8(x, sign_bits, q=None, scale=None, stream=None):
     _check(lib().hadamard32_quant_i8(_p(x), _p(sign_bits), _p(q), _p(scale), M, K, _stream(stream)),
            "hadamard32_quant_i8")
     return q, scale
+
+
+_W8WS = {}
+
+
+def gemm_w8a8_hadamard(x, sign_bits, w, sw, y=None, workspace=None, stream=None):
+    """y[m][n] = C[m][n] s_a[m] s_w[n] / 32 in one launch: x bf16 [M][K] is
+    transformed and quantized like hadamard32_quant_i8 (bit-exact), C = q_a w^T
+    exactly; w int8 [N][K] and sw fp32 [N] are the weights quantized the same
+    way. The zero-filled workspace is cached per (device, stream) (every call
+    leaves it zeroed)."""
+    M, K = x.shape
+    N = w.shape[0]
+    for t, b, n in ((x, 2, "x"), (sign_bits, 4, "sign_bits"), (w, 1, "w"), (sw, 4, "sw")):
+        _need(t, b, n)
+    if y is None:
+        y = torch.empty(M, N, device=x.device, dtype=torch.float32)
+    need = lib().qg_w8a8_hadamard_workspace_size(M, K)
+    if workspace is None:
+        st = stream if stream is not None else torch.cuda.current_stream(x.device)
+        key = (str(x.device), st.cuda_stream)
+        workspace = _W8WS.get(key)
+        if workspace is None or workspace.numel() < need:
+            if torch.cuda.is_current_stream_capturing():
+                workspace = torch.zeros(need, device=x.device, dtype=torch.uint8)
+            else:
+                workspace = torch.zeros(max(need, 1 << 16), device=x.device, dtype=torch.uint8)
+                _W8WS[key] = workspace
+    _check(lib().gemm_w8a8_hadamard(_p(x), _p(sign_bits), _p(w), _p(sw), _p(y), M, N, K, _p(workspace),
+                                    workspace.numel(), _stream(stream)), "gemm_w8a8_hadamard")
+    return y
 
 
 def gemm_w8a8_i32(a, w, c=None, stream=None):

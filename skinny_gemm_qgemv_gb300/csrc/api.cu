@@ -98,6 +98,26 @@ int qg_version(void) { return 100; }
 // stream. Activations and outputs are only touched after the dependency wait,
 // but WEIGHTS may be read early: enable only when no kernel immediately before
 // a call writes that call's weights. Off by default.
+size_t qg_w8a8_hadamard_workspace_size(int M, int K) {
+  if (M < 1 || M > 16 || K < 1) return 0;
+  return qg::w8a8_fused_workspace_size(M, K);
+}
+
+qg_status gemm_w8a8_hadamard(const uint16_t* x_bf16, const uint32_t* sign_bits, const int8_t* w, const float* sw,
+                             float* y, int M, int N, int K, void* workspace, size_t ws_bytes, void* stream) {
+  if (!x_bf16 || !sign_bits || !w || !sw || !y || !workspace) return QG_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 32 || K % 32 != 0) return QG_ERR_INVALID_ARG;
+  if (!aligned16(x_bf16) || !aligned16(sign_bits) || !aligned16(w) || !aligned16(sw) || !aligned16(y) ||
+      !aligned16(workspace))
+    return QG_ERR_MISALIGNED;
+  if (!qg::w8a8_fused_ok(M, N, K)) return QG_ERR_UNSUPPORTED;
+  if (ws_bytes < qg::w8a8_fused_workspace_size(M, K)) return QG_ERR_WORKSPACE;
+  uint32_t* err = err_word();
+  if (!err) return QG_ERR_CUDA;
+  return from_cuda(qg::launch_w8a8_fused(x_bf16, sign_bits, w, sw, y, M, N, K, workspace, err,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
 void qg_set_pdl(int enable) { g_pdl = enable != 0; }
 
 size_t qg_gemv_workspace_size(int N, int K, int group_size) {

@@ -29,6 +29,7 @@ enum DeviceError : uint32_t {
   kErrChainEmptyWait = 0x402,
   kErrChainDrain = 0x403,
   kErrChainLevelWait = 0x404,
+  kErrW8FusedBarrier = 0x405,
   kErrSelftestBarrier = 0x501,
   kErrSelftestFlag = 0x502,
 };
@@ -175,6 +176,19 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
 __device__ __forceinline__ uint16_t lds16(uint32_t addr) {
   uint16_t v;
   asm volatile("ld.shared.b16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+
+// Load of data another CTA of the same launch may have written: L2, not L1.
+__device__ __forceinline__ uint32_t ldcg32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.cg.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint4 ldcg128(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
   return v;
 }
 

@@ -112,6 +112,12 @@ cudaError_t launch_w8a8_i32(const int8_t* a, const int8_t* w, int32_t* c, int M,
 bool w8a8_mma_ok(int M, int N, int K);
 cudaError_t launch_w8a8_mma(const int8_t* a, const int8_t* w, int32_t* c, int M, int N, int K, uint32_t* err,
                             cudaStream_t stream, bool pdl);
+// Hadamard + int8 + W8A8 + dequant in one cooperative launch (w8a8_mma.cu):
+// M <= 16, K a multiple of 1024 and at most 4096
+bool w8a8_fused_ok(int M, int N, int K);
+size_t w8a8_fused_workspace_size(int M, int K);
+cudaError_t launch_w8a8_fused(const uint16_t* x, const uint32_t* sign_bits, const int8_t* w, const float* sw,
+                              float* y, int M, int N, int K, void* ws, uint32_t* err, cudaStream_t stream);
 
 // Grouped M = 1 W4A16 GEMV (w4a16_group.cu): one persistent launch over a list
 // of independent projections. The caller fills wq, scales, biases, x, y, N, K;

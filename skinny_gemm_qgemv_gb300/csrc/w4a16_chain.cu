@@ -101,12 +101,8 @@ __device__ __forceinline__ void f16x2_split(uint32_t v, float& lo, float& hi) {
   asm("{.reg .f16 l, h; mov.b32 {l, h}, %2; cvt.f32.f16 %0, l; cvt.f32.f16 %1, h;}" : "=f"(lo), "=f"(hi) : "r"(v));
 }
 
-// Loads of data other CTAs of the same launch may have written: L2, not L1.
-__device__ __forceinline__ uint32_t ldcg32(const void* p) {
-  uint32_t v;
-  asm volatile("ld.global.cg.b32 %0, [%1];" : "=r"(v) : "l"(p));
-  return v;
-}
+// Loads of data other CTAs of the same launch may have written: L2, not L1
+// (ldcg32 in the common header).
 __device__ __forceinline__ float2 ldcg_f2(const float* p) {
   float2 v;
   asm volatile("ld.global.cg.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));

@@ -89,6 +89,16 @@ __device__ __forceinline__ void a8_to_f16x2(uint32_t word, uint32_t& lo, uint32_
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(h), "r"(k1152));
 }
 
+// D += A B in int32: m16n8k32, s8 operands (row-major A, column-major B)
+__device__ __forceinline__ void mma16832_s8(int (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                            uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(kW8Threads, 1)
@@ -258,6 +268,273 @@ __global__ void __launch_bounds__(kW8Threads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Fused: Hadamard -> int8 -> W8A8 -> dequant in one launch (w8a8_fused_kernel)
+//
+// y[m][n] = C[m][n] s_a[m] s_w[n] / 32 with (q_a, s_a) the block-32 randomized
+// Hadamard + per-row int8 of x (bit-exact with hadamard32_quant_i8) and C =
+// q_a w^T exact -- the whole int8 path of the Uzu article's "How Uzu optimizes
+// bytes and tokens per pass", with no int8 round trip through a separate
+// quantizer launch and no cleared accumulator.
+//
+// One cooperative launch, one CTA per SM (8 consumer warps + 1 producer warp):
+//  1. transform: the M x K/32 blocks are split over the CTAs; a warp takes a
+//     block (one element per lane, the five butterflies as shuffles in the
+//     fixed order), the CTA's per-row maxima of |z| are taken in shared memory
+//     and then into the rows' maxima in the workspace (an integer max on the
+//     float bits: exact, any order). Grid barrier.
+//  2. quantize: every CTA reads the M row maxima, s = max / 127 and q =
+//     rint(z / s) (IEEE divisions), and writes its blocks' codes to the
+//     workspace already in the order the product reads them. Grid barrier.
+//  3. every CTA copies all of q_a (M <= 16 rows, 64 KB at K = 4096) into
+//     shared memory with one bulk copy.
+//  4. product: tiles of 16 weight rows x the whole K, one contiguous range of
+//     tiles per CTA; a tile is one ring stage, 16 bulk copies of one row each
+//     into rows padded to K + 64 bytes (every shared read conflict-free), and
+//     the producer warp streams tiles from the start of the launch, so the
+//     weight stream overlaps steps 1-3. Per 64-k group a warp runs four int8
+//     mma.sync.m16n8k32 (weights and codes as stored, int32 accumulation:
+//     exact, nothing to convert); at the end of a tile the 8 warps' int32
+//     partials are added through shared memory (two buffers, one barrier per
+//     tile) and each thread writes one y = float(C) s_a s_w / 32.
+// The last CTA to finish zeroes the row maxima and the barrier counters, so the
+// workspace stays ready for the next call.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kFzRows = 16;                             // weight rows per tile (= per stage)
+constexpr int kFzMaxK = 4096;
+constexpr uint32_t kFzQa = (kFzMaxK / 64) * 1024;       // q_a: [group][row g, g + 8][32 lanes][16 B]
+constexpr uint32_t kFzRed = 2 * kW8Warps * 32 * 8 * 4;  // int32 partial tiles of the 8 warps, two buffers
+constexpr unsigned long long kFzWaitNs = 1000000000ull;
+
+struct W8FusedArgs {
+  const uint16_t* x;
+  const uint32_t* sign_bits;
+  const int8_t* w;
+  const float* sw;
+  float* y;
+  uint32_t* amax;   // [16] row maxima (float bits), zero between calls
+  uint32_t* cnt;    // [4]: grid barriers 1 and 2, CTAs finished
+  int8_t* qa;       // codes in product order, [K / 64][2][32][16]
+  int M, N, K, ntiles, ST;
+  int zcap;         // transformed blocks a CTA keeps: ceil(M K / 32 / grid)
+  uint32_t pitch;   // shared row pitch of a tile: K + 64 bytes
+  uint32_t* err;
+};
+
+__device__ __forceinline__ uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// grid barrier over all CTAs (cooperative launch): the consumer warps of a CTA
+// have synchronized before thread 0 arrives; a bounded wait
+__device__ __forceinline__ bool fz_grid_barrier(uint32_t* cnt, uint32_t* err) {
+  __shared__ int ok_s;
+  if (threadIdx.x == 0) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(cnt) : "memory");
+    const uint64_t t0 = gtimer();
+    int ok = 1;
+    for (uint32_t i = 0;; ++i) {
+      unsigned v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+      if (v >= gridDim.x) break;
+      if ((i & 63) == 63 && gtimer() - t0 > kFzWaitNs) {
+        report_error(err, kErrW8FusedBarrier);
+        ok = 0;
+        break;
+      }
+      if (i > 256) __nanosleep(32);
+    }
+    ok_s = ok;
+  }
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+  return ok_s != 0;
+}
+
+// one 64-k group for one lane: rows g, g + 8 of the tile, x rows g, g + 8
+__device__ __forceinline__ void fz_group(int (&y0)[4], int (&y1)[4], uint32_t sb, uint32_t pitch, uint32_t qs,
+                                         int gi, int g, int c, int lane) {
+  const uint4 w0 = lds128(sb + g * pitch + gi * 64 + 16 * c);
+  const uint4 w1 = lds128(sb + (g + 8) * pitch + gi * 64 + 16 * c);
+  const uint4 q0 = lds128(qs + gi * 1024 + lane * 16);
+  const uint4 q1 = lds128(qs + gi * 1024 + 512 + lane * 16);
+  // two k = 32 steps: the lane's 16 bytes are (a0, a2) of step 0 and of step 1
+  // for its rows, and the same bytes of the x rows are (b0, b1)
+  mma16832_s8(y0, w0.x, w1.x, w0.y, w1.y, q0.x, q0.y);
+  mma16832_s8(y1, w0.x, w1.x, w0.y, w1.y, q1.x, q1.y);
+  mma16832_s8(y0, w0.z, w1.z, w0.w, w1.w, q0.z, q0.w);
+  mma16832_s8(y1, w0.z, w1.z, w0.w, w1.w, q1.z, q1.w);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kW8Threads, 1) w8a8_fused_kernel(const W8FusedArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ float s_row[16];
+  __shared__ unsigned cta_max[16];
+  __shared__ __align__(8) uint64_t qbar;
+  // shared layout: ring [ST][16 rows][K + 64] | q_a | red x 2 | barriers | z blocks
+  const uint32_t stage_bytes = kFzRows * a.pitch;
+  const uint32_t base = smem_u32(smem);
+  const uint32_t qs = base + a.ST * stage_bytes;
+  int32_t* red = reinterpret_cast<int32_t*>(smem + (size_t)a.ST * stage_bytes + kFzQa);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)a.ST * stage_bytes + kFzQa + kFzRed);
+  uint64_t* empty = full + a.ST;
+  float* zb = reinterpret_cast<float*>(smem + (size_t)a.ST * stage_bytes + kFzQa + kFzRed + 16 * a.ST);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int K = a.K, M = a.M, G = a.K / 64;
+  const int t0 = (int)((long long)a.ntiles * blockIdx.x / gridDim.x);
+  const int t1 = (int)((long long)a.ntiles * (blockIdx.x + 1) / gridDim.x);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < a.ST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kW8Warps);
+    }
+    mbar_init(&qbar, 1);
+    fence_mbar_init();
+  }
+  if (threadIdx.x < 16) cta_max[threadIdx.x] = 0u;
+  __syncthreads();
+
+  if (warp == kW8Warps) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int issued = 0;
+      bool ok = true;
+      for (int t = t0; t < t1 && ok; ++t, ++issued) {
+        const int st = issued % a.ST;
+        if (issued >= a.ST) ok = mbar_wait(&empty[st], ((issued / a.ST) & 1) ^ 1, a.err, kErrGemvEmptyWait);
+        if (!ok) break;
+        const int rows = min(kFzRows, a.N - t * kFzRows);
+        mbar_arrive_expect_tx(&full[st], (uint32_t)rows * K);
+        uint8_t* dst = smem + (size_t)st * stage_bytes;
+        for (int r = 0; r < rows; ++r)
+          bulk_g2s_evict_first(dst + r * a.pitch, a.w + (size_t)(t * kFzRows + r) * K, K, &full[st], pol);
+      }
+      for (int j = max(0, issued - a.ST); j < issued; ++j)
+        mbar_wait(&full[j % a.ST], (j / a.ST) & 1, a.err, kErrGemvDrain);
+    }
+  } else {
+    // ---------------------------------------------------------------- consumers
+    const int g = lane >> 2, c = lane & 3;
+    bool ok = true;
+    // 1. transform this CTA's blocks, row maxima
+    const int nblk = M * (K / 32);
+    const int b0 = (int)((long long)nblk * blockIdx.x / gridDim.x);
+    const int b1 = (int)((long long)nblk * (blockIdx.x + 1) / gridDim.x);
+    for (int j = b0 + warp, i = warp; j < b1; j += kW8Warps, i += kW8Warps) {
+      const int m = j / (K / 32), kb = j % (K / 32);
+      float v = bf16_bits_to_f32(a.x[(size_t)m * K + 32 * kb + lane]);
+      if ((a.sign_bits[kb] >> lane) & 1u) v = -v;
+#pragma unroll
+      for (int h = 1; h < 32; h <<= 1) {
+        const float p = __shfl_xor_sync(0xffffffffu, v, h);
+        v = (lane & h) ? __fsub_rn(p, v) : __fadd_rn(v, p);
+      }
+      zb[32 * i + lane] = v;
+      float mx = fabsf(v);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      if (lane == 0) atomicMax(&cta_max[m], __float_as_uint(mx));
+    }
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    if (threadIdx.x < M && cta_max[threadIdx.x] != 0u) atomicMax(&a.amax[threadIdx.x], cta_max[threadIdx.x]);
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    ok = fz_grid_barrier(&a.cnt[0], a.err);
+    // 2. scales and this CTA's codes, written in product order: code (m, k) at
+    //    group k / 64, half m / 8, lane 4 (m % 8) + (k % 64) / 16, byte k % 16
+    if (threadIdx.x < 16) {
+      unsigned bits;
+      asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(bits) : "l"(&a.amax[threadIdx.x]) : "memory");
+      s_row[threadIdx.x] = __fdiv_rn(__uint_as_float(bits), 127.0f);
+    }
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    if (ok) {
+      for (int j = b0 + warp, i = warp; j < b1; j += kW8Warps, i += kW8Warps) {
+        const int m = j / (K / 32), kb = j % (K / 32);
+        const float sc = s_row[m];
+        int8_t code = 0;
+        if (sc > 0.f) {
+          float r = rintf(__fdiv_rn(zb[32 * i + lane], sc));
+          r = fminf(fmaxf(r, -127.f), 127.f);
+          code = (int8_t)(int)r;
+        }
+        const int k = 32 * kb + lane;
+        a.qa[(size_t)(k >> 6) * 1024 + (m >> 3) * 512 + (((m & 7) << 2) + ((k >> 4) & 3)) * 16 + (k & 15)] = code;
+      }
+    }
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    if (ok) ok = fz_grid_barrier(&a.cnt[1], a.err);
+    // 3. all of q_a into shared memory: one bulk copy (the codes of the other
+    //    CTAs were published before the barrier; the copy reads them through
+    //    the async proxy)
+    if (threadIdx.x == 0 && ok) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      mbar_arrive_expect_tx(&qbar, (uint32_t)G * 1024);
+      bulk_g2s(smem + (size_t)a.ST * stage_bytes, a.qa, (uint32_t)G * 1024, &qbar);
+    }
+    if (ok) ok = mbar_wait(&qbar, 0, a.err, kErrGemvFullWait);
+    // 4. the product
+    int tile_i = 0;
+    for (int t = t0; t < t1; ++t, ++tile_i) {
+      const int st = tile_i % a.ST;
+      int y0[4] = {0, 0, 0, 0}, y1[4] = {0, 0, 0, 0};
+      if (ok) ok = mbar_wait(&full[st], (tile_i / a.ST) & 1, a.err, kErrGemvFullWait);
+      if (ok) {
+        const uint32_t sb = base + st * stage_bytes;
+        int gi = warp;
+        for (; gi + kW8Warps < G; gi += 2 * kW8Warps) {
+          fz_group(y0, y1, sb, a.pitch, qs, gi, g, c, lane);
+          fz_group(y0, y1, sb, a.pitch, qs, gi + kW8Warps, g, c, lane);
+        }
+        if (gi < G) fz_group(y0, y1, sb, a.pitch, qs, gi, g, c, lane);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+      // the 8 warps' partial tiles added in warp order, then y = C s_a s_w / 32;
+      // two buffers, so one barrier per tile orders both the writes before the
+      // reads and this tile's reads before the next-but-one tile's writes
+      int32_t* rt = red + (tile_i & 1) * (kW8Warps * 32 * 8);
+      {
+        int4* rv = reinterpret_cast<int4*>(rt);
+        rv[(warp * 32 + lane) * 2] = make_int4(y0[0], y0[1], y0[2], y0[3]);
+        rv[(warp * 32 + lane) * 2 + 1] = make_int4(y1[0], y1[1], y1[2], y1[3]);
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      {
+        // thread -> (row r of the tile, x row m): fragment lane and element
+        const int r = threadIdx.x >> 4, m = threadIdx.x & 15;
+        const int tt = m >> 3, col = m & 7;
+        const int L = ((r & 7) << 2) | (col >> 1);
+        const int e = ((r >> 3) << 1) | (col & 1);
+        int tot = 0;
+#pragma unroll
+        for (int w2 = 0; w2 < kW8Warps; ++w2) tot += rt[((w2 * 32 + L) * 2 + tt) * 4 + e];
+        const int n = t * kFzRows + r;
+        if (ok && m < M && n < a.N) a.y[(size_t)m * a.N + n] = (float)tot * s_row[m] * (a.sw[n] * 0.03125f);
+      }
+    }
+  }
+  __syncwarp();
+  __syncthreads();
+  // the last CTA to finish leaves the workspace zeroed for the next call
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned prev = atomicAdd(&a.cnt[2], 1u);
+    if (prev == gridDim.x - 1) {
+      for (int i = 0; i < 16; ++i) atomicExch(&a.amax[i], 0u);
+      atomicExch(&a.cnt[0], 0u);
+      atomicExch(&a.cnt[1], 0u);
+      __threadfence();
+      atomicExch(&a.cnt[2], 0u);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 bool w8a8_mma_ok(int M, int N, int K) {
@@ -296,6 +573,59 @@ cudaError_t launch_w8a8_mma(const int8_t* a8, const int8_t* w8, int32_t* c, int 
   if (e != cudaSuccess) return e;
   return launch_kernel(w8a8_mma_kernel, dim3(std::min(a.nunits, sms)), dim3(kW8Threads), smem, stream, pdl, tm_w,
                        tm_a, a);
+}
+
+bool w8a8_fused_ok(int M, int N, int K) {
+  return M >= 1 && M <= 16 && N >= 1 && K >= 1024 && K % 1024 == 0 && K <= kFzMaxK;
+}
+
+size_t w8a8_fused_workspace_size(int M, int K) {
+  (void)M;
+  return 128 + 16 * (size_t)K;  // row maxima [16], barrier counters [4], pad | codes [16][K]
+}
+
+cudaError_t launch_w8a8_fused(const uint16_t* x, const uint32_t* sign_bits, const int8_t* w, const float* sw,
+                              float* y, int M, int N, int K, void* ws, uint32_t* err, cudaStream_t stream) {
+  W8FusedArgs a{};
+  a.x = x;
+  a.sign_bits = sign_bits;
+  a.w = w;
+  a.sw = sw;
+  a.y = y;
+  a.amax = static_cast<uint32_t*>(ws);
+  a.cnt = a.amax + 16;
+  a.qa = reinterpret_cast<int8_t*>(static_cast<uint8_t*>(ws) + 128);
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.ntiles = (N + kFzRows - 1) / kFzRows;
+  a.pitch = (uint32_t)K + 64;
+  a.err = err;
+  // every SM takes a share of the transform, also when there are fewer tiles
+  const int grid = device_sm_count();
+  const int nblk = M * (K / 32);
+  a.zcap = (nblk + grid - 1) / grid;
+  const size_t fixed = kFzQa + kFzRed + 128 * (size_t)a.zcap;
+  const size_t stage = (size_t)kFzRows * a.pitch;
+  const size_t budget = (size_t)device_max_smem_optin() - 256;
+  if (budget < fixed + 2 * (stage + 16)) return cudaErrorInvalidValue;
+  a.ST = (int)std::min<size_t>(4, (budget - fixed) / (stage + 16));
+  const size_t smem = fixed + (size_t)a.ST * (stage + 16);
+  cudaError_t e = allow_max_smem(w8a8_fused_kernel);
+  if (e != cudaSuccess) return e;
+  // CTAs wait for each other at the two grid barriers: a cooperative launch,
+  // which the driver refuses rather than start partially
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kW8Threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, w8a8_fused_kernel, a);
 }
 
 }  // namespace qg
