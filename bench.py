@@ -412,6 +412,7 @@ def bench_dependent_stack(q, mats, dev, stream, hbm_peak, steps):
         assert q.device_error() == 0
         levels = items[-1]["level"] + 1
         out[key] = {"value": step_bytes / t / 1e9, "unit": "GB/s", "frac": step_bytes / t / 1e9 / hbm_peak,
+                    "traffic": kernel_traffic("w4a16_chain_m1", step_bytes),
                     "ms_per_step": t * 1e3, "tokens_per_s": 1.0 / t, "bytes_per_step": step_bytes,
                     "levels": levels, "launches_per_step": 1,
                     "min_ms_per_step": reps[0] * 1e3, "max_ms_per_step": reps[-1] * 1e3,
@@ -490,7 +491,8 @@ def bench_w8a8(q, dev, stream, N, l2_bytes):
 CASES = ["gemv_lm_head", "gemv_down", "gemv_q", "skinny16_gate_up", "skinny16_down", "moe_T1", "moe_T16",
          "w8a16_lm_head",
          "w8a8_12288", "hadamard_16x4096", "gemv_group_4layers", "skinny16_group_4layers", "chain_4layers",
-         "chain_flat_4layers", "chain_trace", "w8a8_fused_12288", "w8a8_fused_4096"]
+         "chain_flat_4layers", "chain_trace", "w8a8_fused_12288", "w8a8_fused_4096",
+         "skinny32_group_4layers"]
 
 
 def chain_trace_summary(q, dev):
@@ -564,13 +566,15 @@ def run_case(args):
         ch = q.GemvChain(items)
         f = ch.run
         nbytes = sum(w4_bytes(N, K) for (_, N, K, *_r) in mats)
-    elif c == "skinny16_group_4layers":
-        # the grouped skinny launch, M = 16 (warp-level MMA), over 4 decoder layers + the lm_head
-        mats = build_stack(q, dev, 16, layers=4)
-        xs, ys = stack_io(mats, dev, 16)
+    elif c in ("skinny16_group_4layers", "skinny32_group_4layers"):
+        # the grouped skinny launch over 4 decoder layers + the lm_head: M = 16
+        # (warp-level MMA kernel) or M = 32 (tcgen05 kernel)
+        Mr = 16 if c.startswith("skinny16") else 32
+        mats = build_stack(q, dev, Mr, layers=4)
+        xs, ys = stack_io(mats, dev, Mr)
         grp = q.SkinnyGroup([(wq, s, b, x, y) for (_, N, K, wq, s, b), x, y in zip(mats, xs, ys)])
         f = grp.run
-        nbytes = sum(w4_bytes(N, K, 16) for (_, N, K, *_r) in mats)
+        nbytes = sum(w4_bytes(N, K, Mr) for (_, N, K, *_r) in mats)
     elif c.startswith("gemv_") or c.startswith("skinny16_"):
         shape = {"lm_head": (151936, 4096), "down": (4096, 12288), "q": (4096, 4096),
                  "gate_up": (24576, 4096)}[c.split("_", 1)[1]]
