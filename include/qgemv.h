@@ -463,7 +463,9 @@ QG_API size_t qg_moe_noalloc_max_bytes(void);
  * per-row symmetric int8 quantization (Uzu article, "How Uzu optimizes bytes
  * and tokens per pass").
  *
- *   x_bf16     bf16 [M][K], K a multiple of 32, M >= 1.
+ *   x_bf16     bf16 [M][K], K a multiple of 32, M >= 1; finite values (a
+ *              NaN or an infinity in a row makes that row's codes and scale
+ *              meaningless; nothing else is affected).
  *   sign_bits  uint32 [K/32]: bit j of word b set = negate element 32b+j
  *              before the transform. Apply the same vector to the weights.
  *   q          int8 [M][K] (output); scale fp32 [M] (output).
