@@ -436,10 +436,45 @@ __global__ void __launch_bounds__(kMxThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// B of the down product, once: p h 2^-sigma_t of every pair in fp16
+// ---------------------------------------------------------------------------
+// sigma_t puts the largest p |h| of token t's pairs in [2^14, 2^15) (the same
+// exact power of two the down kernel undoes at the end). Every CTA of the down
+// kernel reads these rows instead of converting the fp32 h of each of its
+// stages itself. Row P is all zeros (the B column of a token not in a virtual
+// expert).
+__global__ void __launch_bounds__(256) moe_mx_hprep_kernel(const float* __restrict__ h,
+                                                           const uint32_t* __restrict__ hmax,
+                                                           const float* __restrict__ wts, uint16_t* __restrict__ hh,
+                                                           int T, int I, int top_k) {
+  pdl_wait();  // h and its maxima come from gate/up
+  pdl_launch_dependents();
+  const int P = T * top_k;
+  const long long n8 = (long long)(P + 1) * I / 8;
+  for (long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x; q < n8; q += (long long)gridDim.x * blockDim.x) {
+    const int p = (int)(q * 8 / I);
+    uint4 o = make_uint4(0u, 0u, 0u, 0u);
+    if (p < P) {
+      const int t0 = (p / top_k) * top_k;
+      float m = 0.f;
+      for (int j = 0; j < top_k; ++j) m = fmaxf(m, wts[t0 + j] * __uint_as_float(hmax[t0 + j]));
+      const float f = wts[p] * pow2f(-fp16_prescale_exp(m));
+      const float4 lo = __ldcg(reinterpret_cast<const float4*>(h + q * 8));
+      const float4 hi = __ldcg(reinterpret_cast<const float4*>(h + q * 8 + 4));
+      o.x = f16x2_rn(lo.x * f, lo.y * f);
+      o.y = f16x2_rn(lo.z * f, lo.w * f);
+      o.z = f16x2_rn(hi.x * f, hi.y * f);
+      o.w = f16x2_rn(hi.z * f, hi.w * f);
+    }
+    reinterpret_cast<uint4*>(hh)[q] = o;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // down + routing-weighted combine
 // ---------------------------------------------------------------------------
 struct MxDnArgs {
-  const float* h;         // [P][I] fp32
+  const uint16_t* hh;     // [P + 1][I] fp16 p h 2^-sigma_t of every pair (moe_mx_hprep_kernel), then a zero row
   const uint32_t* hmax;   // [P]
   const float* wts;       // [P] routing weights
   const int32_t* vexp;
@@ -450,26 +485,24 @@ struct MxDnArgs {
   uint32_t* err;
 };
 
-// a lane's tokens 8 nt + g in one virtual expert: the h row of the token's
-// pair and p * 2^-sigma_t (a token not in it: pair 0's row and factor 0, so its
-// column of B is 0); act: n tiles with at least one of their tokens in it
+// a lane's tokens 8 nt + g in one virtual expert: the fp16 B row of the
+// token's pair (a token not in it: the zero row, so its column of B is 0);
+// act: n tiles with at least one of their tokens in it
 template <int NT>
 struct DnLane {
-  const float* hp[NT];
-  float f[NT];
+  const uint16_t* hp[NT];
   uint32_t act;
 };
 
-// from the shared tables: pair of (virtual expert, token) or -1, and p * 2^-sigma_t per pair
+// from the shared table: pair of (virtual expert, token) or -1
 template <int NT>
-__device__ __forceinline__ void dn_lane(const MxDnArgs& a, int v, int g, const int16_t* tab, const float* fp,
-                                        DnLane<NT>& L) {
+__device__ __forceinline__ void dn_lane(const MxDnArgs& a, int v, int g, const int16_t* tab, DnLane<NT>& L) {
   L.act = 0u;
+  const int P = a.T * a.top_k;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int pair = tab[v * 8 * NT + 8 * nt + g];
-    L.hp[nt] = a.h + (size_t)max(pair, 0) * a.I;
-    L.f[nt] = pair >= 0 ? fp[pair] : 0.f;
+    L.hp[nt] = a.hh + (size_t)(pair >= 0 ? pair : P) * a.I;
     if (__any_sync(kFull, pair >= 0)) L.act |= 1u << nt;
   }
 }
@@ -495,8 +528,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(sig + 8 * NT);
   uint32_t* rel = reinterpret_cast<uint32_t*>(full + a.ST);
   int* vrow = reinterpret_cast<int*>(rel + a.ST);  // first weight row of each virtual expert's range
-  float* fp = reinterpret_cast<float*>(vrow + a.nvmax);                   // [P] p * 2^-sigma_t
-  int16_t* tab = reinterpret_cast<int16_t*>(fp + a.T * a.top_k);          // [nvmax][8 NT] pair or -1
+  int16_t* tab = reinterpret_cast<int16_t*>(vrow + a.nvmax);              // [nvmax][8 NT] pair or -1
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.ST; ++i) {
@@ -505,7 +537,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     }
     fence_mbar_init();
   }
-  pdl_wait();  // h and its maxima come from gate/up, the table from the route kernel
+  pdl_wait();  // the fp16 B rows come from the preparation kernel, h's maxima from gate/up, the table
+              // from the route kernel
   // sigma_t: max over the token's pairs of p |h| lands in [2^14, 2^15) after scaling
   if (threadIdx.x < 8 * NT) {
     const int t = threadIdx.x;
@@ -528,7 +561,6 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   const int nstages = nv * nks;
   const uint64_t pol = policy_evict_first();
   for (int v2 = threadIdx.x; v2 < nv; v2 += blockDim.x) vrow[v2] = __ldg(a.vexp + (size_t)v2 * kMxVexpInts) * H + n0;
-  for (int p = threadIdx.x; p < a.T * a.top_k; p += blockDim.x) fp[p] = a.wts[p] * pow2f(-sig[p / a.top_k]);
   for (int q = threadIdx.x; q < nv * 8 * NT; q += blockDim.x) tab[q] = -1;
   __syncthreads();
   for (int q = threadIdx.x; q < nv * kMxTC; q += blockDim.x) {
@@ -572,48 +604,43 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[mt][nt][i] = 0.f;
-  // fp32 h of the next stage, loaded one stage ahead (L2-resident): [nt][block][half]
-  uint4 hn[NT][BPW][2];
+  // the next stage's B (fp16 p h 2^-sigma_t, k = 8c .. 8c + 7 of each block),
+  // loaded one stage ahead (L2-resident): [nt][block]
+  uint4 hn[NT][BPW];
   auto load_h = [&](const DnLane<NT>& L, int ks) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
       if ((L.act >> nt) & 1u)
 #pragma unroll
-        for (int j = 0; j < BPW; ++j) {
-          const uint4* p = reinterpret_cast<const uint4*>(L.hp[nt] + ks * KS + 32 * (BPW * warp + j) + 8 * c);
-          hn[nt][j][0] = __ldcg(p);
-          hn[nt][j][1] = __ldcg(p + 1);
-        }
+        for (int j = 0; j < BPW; ++j)
+          hn[nt][j] = __ldcg(reinterpret_cast<const uint4*>(L.hp[nt] + ks * KS + 32 * (BPW * warp + j) + 8 * c));
   };
   DnLane<NT> cur, nxt;
   int st = 0, v = vstart, ks = 0, i = 0;
   uint32_t par = 0;
   bool ok = true;
   if (nv > 0) {
-    dn_lane<NT>(a, v, g, tab, fp, cur);
+    dn_lane<NT>(a, v, g, tab, cur);
     load_h(cur, 0);
   }
   for (int q = 0; q < nstages; ++q) {
-    // this stage's B: p h 2^-sigma_t in fp16
+    // this stage's B: p h 2^-sigma_t in fp16, as prepared
     uint32_t b[NT][BPW][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
-      if ((cur.act >> nt) & 1u)
 #pragma unroll
-        for (int j = 0; j < BPW; ++j) {
-          const float f = cur.f[nt];
-          const uint4 lo = hn[nt][j][0], hi = hn[nt][j][1];
-          b[nt][j][0] = f16x2_rn(__uint_as_float(lo.x) * f, __uint_as_float(lo.y) * f);
-          b[nt][j][1] = f16x2_rn(__uint_as_float(lo.z) * f, __uint_as_float(lo.w) * f);
-          b[nt][j][2] = f16x2_rn(__uint_as_float(hi.x) * f, __uint_as_float(hi.y) * f);
-          b[nt][j][3] = f16x2_rn(__uint_as_float(hi.z) * f, __uint_as_float(hi.w) * f);
-        }
+      for (int j = 0; j < BPW; ++j) {
+        b[nt][j][0] = hn[nt][j].x;
+        b[nt][j][1] = hn[nt][j].y;
+        b[nt][j][2] = hn[nt][j].z;
+        b[nt][j][3] = hn[nt][j].w;
+      }
     // the next stage's h
     bool newv = false;
     if (ks + 1 < nks) {
       load_h(cur, ks + 1);
     } else if (i + 1 < nv) {
-      dn_lane<NT>(a, v + 1 == nv ? 0 : v + 1, g, tab, fp, nxt);
+      dn_lane<NT>(a, v + 1 == nv ? 0 : v + 1, g, tab, nxt);
       load_h(nxt, 0);
       newv = true;
     }
@@ -706,8 +733,7 @@ MxDnPlan plan_down(int T, int H, int I, int top_k, int nvmax, int sms) {
   p.BPW = p.NT == 4 ? 1 : ((p.NT == 1 && I % 2048 == 0) ? 4 : (I % 1024 == 0 ? 2 : 1));
   p.o_s = 256u * p.R * p.BPW;  // codes: [2 BPW chunks][R rows][128 B], then scales [R][16 BPW]
   p.stage_bytes = (272u * p.R * p.BPW + 1023u) & ~1023u;
-  const size_t fixed = 1024 + 4 * 8 * p.NT + 4 * (size_t)nvmax + 4 * (size_t)T * top_k +
-                       2 * (size_t)nvmax * 8 * p.NT + 64;
+  const size_t fixed = 1024 + 4 * 8 * p.NT + 4 * (size_t)nvmax + 2 * (size_t)nvmax * 8 * p.NT + 64;
   p.ST = (int)std::min<size_t>(8, (kMxSmem - fixed) / (p.stage_bytes + 16));
   p.smem = fixed + (size_t)p.ST * (p.stage_bytes + 16);
   return p;
@@ -761,8 +787,8 @@ bool moe_mx_mma_ok(int T, int H, int I, int E, int top_k) {
 cudaError_t launch_moe_mx_mma(const uint16_t* x, const float* logits, const uint8_t* gq, const uint8_t* gs,
                               const uint8_t* uq, const uint8_t* us, const uint8_t* dq, const uint8_t* ds, int T,
                               int H, int I, int E, int top_k, float* y, int32_t* idx, float* wts, int32_t* xexp,
-                              uint16_t* xh, int32_t* vexp, int32_t* nvirt, uint32_t* hmax, float* h, uint32_t* err,
-                              cudaStream_t stream, bool pdl) {
+                              uint16_t* xh, int32_t* vexp, int32_t* nvirt, uint32_t* hmax, float* h, uint16_t* hh,
+                              uint32_t* err, cudaStream_t stream, bool pdl) {
   const int sms = device_sm_count();
   cudaError_t e;
   if (E <= 128)
@@ -798,7 +824,14 @@ cudaError_t launch_moe_mx_mma(const uint16_t* x, const float* logits, const uint
   e = gbpw == 2 ? launch_gateup<2>(gmaps, ga, gu_grid, gateup_smem(gst), stream, pdl)
                 : launch_gateup<1>(gmaps, ga, gu_grid, gateup_smem(gst), stream, pdl);
   if (e != cudaSuccess) return e;
-  const MxDnArgs da{h,     hmax,  wts,   vexp,   nvirt,    y, T, H, I, top_k, pd.R, pd.ST, pd.BPW,
+  {
+    const long long n8 = (long long)(T * top_k + 1) * I / 8;
+    const int grid = (int)std::min<long long>(4LL * sms, (n8 + 255) / 256);
+    e = launch_kernel(moe_mx_hprep_kernel, dim3(grid), dim3(256), 0, stream, pdl, (const float*)h,
+                      (const uint32_t*)hmax, (const float*)wts, hh, T, I, top_k);
+    if (e != cudaSuccess) return e;
+  }
+  const MxDnArgs da{hh,    hmax,  wts,   vexp,   nvirt,    y, T, H, I, top_k, pd.R, pd.ST, pd.BPW,
                     moe_nvirt_max(T, E, top_k), pd.stage_bytes, pd.o_s, err};
   if (pd.NT == 1)
     return pd.BPW == 4   ? launch_down_mt<1, 4>(tm_dq, tm_ds, da, pd, stream, pdl)

@@ -57,7 +57,7 @@ MoeLayout moe_layout(int T, int H, int I, int E, int top_k) {
   L.xh = take(sizeof(uint16_t) * (size_t)T * H);
   L.xexp = take(sizeof(int32_t) * T);
   L.h = take(sizeof(float) * P * I);
-  L.hh = take(sizeof(uint16_t) * P * I);
+  L.hh = take(sizeof(uint16_t) * (P + 1) * I);  // + a zero row (the MMA path's down B)
   L.hexp = take(sizeof(int32_t) * P);
   L.vexp = take(sizeof(int32_t) * (size_t)moe_nvirt_max(T, E, top_k) * kMxVexpInts);
   L.nvirt = take(sizeof(int32_t) * 4);
@@ -400,8 +400,8 @@ cudaError_t launch_moe_mxfp4(const uint16_t* x, const float* logits, const uint8
     // main path (T <= 32): routing + grouping in one CTA, then gate/up and down on warp-level MMA
     return launch_moe_mx_mma(x, logits, gq, gs, uq, us, dq, ds, T, H, I, E, top_k, y, idx, wts, I32(L.xexp),
                              reinterpret_cast<uint16_t*>(base + L.xh), I32(L.vexp), I32(L.nvirt),
-                             reinterpret_cast<uint32_t*>(base + L.hmax), reinterpret_cast<float*>(base + L.h), err,
-                             stream, pdl);
+                             reinterpret_cast<uint32_t*>(base + L.hmax), reinterpret_cast<float*>(base + L.h),
+                             reinterpret_cast<uint16_t*>(base + L.hh), err, stream, pdl);
   }
   if (aligned && aligned32 && L.has_tc) {
     // larger batches (33..64 tokens): block-scaled tcgen05 MMAs on the stored E2M1 codes and E8M0 scales

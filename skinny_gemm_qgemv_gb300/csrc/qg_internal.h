@@ -247,8 +247,8 @@ cudaError_t launch_moe_mx_tc(const uint16_t* x, const float* logits, const uint8
 cudaError_t launch_moe_mx_mma(const uint16_t* x, const float* logits, const uint8_t* gq, const uint8_t* gs,
                               const uint8_t* uq, const uint8_t* us, const uint8_t* dq, const uint8_t* ds, int T,
                               int H, int I, int E, int top_k, float* y, int32_t* idx, float* wts, int32_t* xexp,
-                              uint16_t* xh, int32_t* vexp, int32_t* nvirt, uint32_t* hmax, float* h, uint32_t* err,
-                              cudaStream_t stream, bool pdl);
+                              uint16_t* xh, int32_t* vexp, int32_t* nvirt, uint32_t* hmax, float* h, uint16_t* hh,
+                              uint32_t* err, cudaStream_t stream, bool pdl);
 cudaError_t launch_moe_mxfp4(const uint16_t* x, const float* logits, const uint8_t* gq, const uint8_t* gs,
                              const uint8_t* uq, const uint8_t* us, const uint8_t* dq, const uint8_t* ds, int T,
                              int H, int I, int E, int top_k, float* y, int32_t* idx, float* wts, void* ws,

@@ -481,16 +481,30 @@ __global__ void __launch_bounds__(kW8Threads, 1) w8a8_fused_kernel(const W8Fused
     int tile_i = 0;
     for (int t = t0; t < t1; ++t, ++tile_i) {
       const int st = tile_i % a.ST;
-      int y0[4] = {0, 0, 0, 0}, y1[4] = {0, 0, 0, 0};
+      // four independent accumulator pairs (groups gi, gi + 8, gi + 16, gi + 24
+      // of a round), so four MMA chains are in flight per warp
+      int ya[4][2][4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) ya[u][0][e] = ya[u][1][e] = 0;
       if (ok) ok = mbar_wait(&full[st], (tile_i / a.ST) & 1, a.err, kErrGemvFullWait);
       if (ok) {
         const uint32_t sb = base + st * stage_bytes;
         int gi = warp;
-        for (; gi + kW8Warps < G; gi += 2 * kW8Warps) {
-          fz_group(y0, y1, sb, a.pitch, qs, gi, g, c, lane);
-          fz_group(y0, y1, sb, a.pitch, qs, gi + kW8Warps, g, c, lane);
+        for (; gi + 3 * kW8Warps < G; gi += 4 * kW8Warps) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) fz_group(ya[u][0], ya[u][1], sb, a.pitch, qs, gi + u * kW8Warps, g, c, lane);
         }
-        if (gi < G) fz_group(y0, y1, sb, a.pitch, qs, gi, g, c, lane);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (gi + u * kW8Warps < G) fz_group(ya[u][0], ya[u][1], sb, a.pitch, qs, gi + u * kW8Warps, g, c, lane);
+      }
+      int y0[4], y1[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        y0[e] = (ya[0][0][e] + ya[1][0][e]) + (ya[2][0][e] + ya[3][0][e]);
+        y1[e] = (ya[0][1][e] + ya[1][1][e]) + (ya[2][1][e] + ya[3][1][e]);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);

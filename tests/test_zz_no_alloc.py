@@ -4,9 +4,10 @@ moe_mxfp4_expert_forward_noalloc serves callers that cannot allocate device
 memory when they run the layer (a plugin handed only its input and output
 buffers, a runtime with one pre-reserved pool, code recorded during CUDA graph
 capture): its scratch is a fixed-size array inside the library. The test runs
-it on three shapes -- the one-warp-per-row path, and the warp-level MMA path
-that serves the real expert shapes at 4 tokens and at its largest batch of 32
-(larger batches need more scratch than the array holds) -- twice in a row with
+it on four shapes -- the one-warp-per-row path at 4 and at 36 tokens, and the
+warp-level MMA path that serves the real expert shapes at 4 tokens and at its
+largest batch of 32 (larger batches of the real shapes need more scratch than
+the array holds) -- twice in a row with
 different inputs (so that anything a call read from the scratch without
 writing it first would show), and requires each result to be bit-identical to
 the workspace entry point's on the same inputs (the same kernels run on the
@@ -41,8 +42,10 @@ def _inputs(E, H, I, T, seed):
 
 
 # (E, H, I, T, top_k): one-warp-per-row path (I not a multiple of 512), warp-level
-# MMA path at 4 and at 32 tokens
-@pytest.mark.parametrize("E,H,I,T,k", [(16, 512, 256, 4, 4), (64, 512, 512, 4, 8), (32, 1024, 512, 32, 8)])
+# MMA path at 4 and at 32 tokens, and a batch above 32 tokens on the
+# one-warp-per-row path
+@pytest.mark.parametrize("E,H,I,T,k", [(16, 512, 256, 4, 4), (64, 512, 512, 4, 8), (32, 1024, 512, 32, 8),
+                                       (8, 256, 128, 36, 2)])
 def test_noalloc_matches_workspace_entry_point_twice(E, H, I, T, k):
     from skinny_gemm_qgemv_gb300 import build
     build.build()
