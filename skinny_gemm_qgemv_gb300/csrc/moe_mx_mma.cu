@@ -174,31 +174,57 @@ __global__ void __launch_bounds__(kRouteThreads) moe_mx_route_mma_kernel(
   for (int t = warp; t < T; t += 32)
     route_token<PER>(logits + (size_t)t * E, E, top_k, lane, sel_k[warp], sel_e[warp], idx + (size_t)t * top_k,
                 wts + (size_t)t * top_k, pe + t * top_k);
-  // max |x| per token; the 32 chunks of a warp belong to one token
+  // max |x| per token, then x * 2^-sigma in fp16 (exact scaling; sigma puts
+  // max |x| in [2^14, 2^15)). The 16-byte chunks of x are read in rounds of
+  // kXb per thread, every load of a round issued before any is used (one
+  // round trip per round instead of one per chunk); the 32 chunks of a warp
+  // belong to one token.
+  constexpr int kXb = 8;
   const uint4* x4 = reinterpret_cast<const uint4*>(x);
-  for (int q0 = warp * 32; q0 < T * cpt; q0 += kRouteThreads) {
-    const uint4 w = __ldg(x4 + q0 + lane);
-    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-    float m = 0.f;
+  const int nch = T * cpt;
+  for (int b0 = 0; b0 < nch; b0 += kXb * kRouteThreads) {
+    uint4 xv[kXb];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      m = fmaxf(m, fmaxf(fabsf(bf16_bits_to_f32(ww[j] & 0xFFFFu)), fabsf(bf16_bits_to_f32(ww[j] >> 16))));
-    const unsigned mb = __reduce_max_sync(kFull, __float_as_uint(m));  // non-negative: uint order
-    if (lane == 0) atomicMax(&amax[q0 / cpt], mb);
+    for (int i = 0; i < kXb; ++i) {
+      const int q = b0 + tid + i * kRouteThreads;
+      xv[i] = q < nch ? __ldg(x4 + q) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int i = 0; i < kXb; ++i) {
+      const int q0 = b0 + warp * 32 + i * kRouteThreads;  // the warp's first chunk of this load
+      if (q0 >= nch) break;                               // warp-uniform
+      const uint32_t ww[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+      float m = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        m = fmaxf(m, fmaxf(fabsf(bf16_bits_to_f32(ww[j] & 0xFFFFu)), fabsf(bf16_bits_to_f32(ww[j] >> 16))));
+      const unsigned mb = __reduce_max_sync(kFull, __float_as_uint(m));  // non-negative: uint order
+      if (lane == 0) atomicMax(&amax[q0 / cpt], mb);
+    }
   }
   __syncthreads();
   pdl_launch_dependents();
-  // x * 2^-sigma in fp16 (exact scaling; sigma puts max |x| in [2^14, 2^15))
   if (tid < T) xexp[tid] = fp16_prescale_exp(__uint_as_float(amax[tid]));
-  for (int q = tid; q < T * cpt; q += kRouteThreads) {
-    const float sc = pow2f(-fp16_prescale_exp(__uint_as_float(amax[q / cpt])));
-    const uint4 w = __ldg(x4 + q);
-    uint4 o;
-    o.x = f16x2_rn(bf16_bits_to_f32(w.x & 0xFFFFu) * sc, bf16_bits_to_f32(w.x >> 16) * sc);
-    o.y = f16x2_rn(bf16_bits_to_f32(w.y & 0xFFFFu) * sc, bf16_bits_to_f32(w.y >> 16) * sc);
-    o.z = f16x2_rn(bf16_bits_to_f32(w.z & 0xFFFFu) * sc, bf16_bits_to_f32(w.z >> 16) * sc);
-    o.w = f16x2_rn(bf16_bits_to_f32(w.w & 0xFFFFu) * sc, bf16_bits_to_f32(w.w >> 16) * sc);
-    reinterpret_cast<uint4*>(xh)[q] = o;
+  for (int b0 = 0; b0 < nch; b0 += kXb * kRouteThreads) {
+    uint4 xv[kXb];
+#pragma unroll
+    for (int i = 0; i < kXb; ++i) {
+      const int q = b0 + tid + i * kRouteThreads;
+      xv[i] = q < nch ? __ldg(x4 + q) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int i = 0; i < kXb; ++i) {
+      const int q = b0 + tid + i * kRouteThreads;
+      if (q >= nch) break;
+      const float sc = pow2f(-fp16_prescale_exp(__uint_as_float(amax[q / cpt])));
+      const uint4 w = xv[i];
+      uint4 o;
+      o.x = f16x2_rn(bf16_bits_to_f32(w.x & 0xFFFFu) * sc, bf16_bits_to_f32(w.x >> 16) * sc);
+      o.y = f16x2_rn(bf16_bits_to_f32(w.y & 0xFFFFu) * sc, bf16_bits_to_f32(w.y >> 16) * sc);
+      o.z = f16x2_rn(bf16_bits_to_f32(w.z & 0xFFFFu) * sc, bf16_bits_to_f32(w.z >> 16) * sc);
+      o.w = f16x2_rn(bf16_bits_to_f32(w.w & 0xFFFFu) * sc, bf16_bits_to_f32(w.w >> 16) * sc);
+      reinterpret_cast<uint4*>(xh)[q] = o;
+    }
   }
   // grouping: pairs per expert, stable order by expert, virtual experts of <= kMxTC pairs
   for (int p = tid; p < P; p += kRouteThreads) {
@@ -537,8 +563,12 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     }
     fence_mbar_init();
   }
-  pdl_wait();  // the fp16 B rows come from the preparation kernel, h's maxima from gate/up, the table
-              // from the route kernel
+  // With programmatic launch this kernel starts once every CTA of the
+  // preparation kernel has passed its own dependency wait, i.e. after gate/up
+  // (and before it the route kernel) completed: h's maxima, the routing
+  // weights and the virtual-expert table are final, so the prologue and the
+  // first weight copies run before this kernel's wait. Only the prepared B rows
+  // (read in the loop below) need it.
   // sigma_t: max over the token's pairs of p |h| lands in [2^14, 2^15) after scaling
   if (threadIdx.x < 8 * NT) {
     const int t = threadIdx.x;
@@ -585,6 +615,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   };
   if (threadIdx.x == 0)
     for (int q = 0; q < min(a.ST, nstages); ++q) issue(q);
+  pdl_wait();  // the prepared B rows come from the preparation kernel
 
   // lane (g, c): rows g, g + 8 of each 16-row block, tokens 8 nt + g, k = 8c .. 8c + 7
   // of blocks BPW w + j of every stage
