@@ -63,7 +63,6 @@ constexpr uint32_t kGuCodes = 4 * 32 * 128;
 constexpr uint32_t kGuScales = 32 * 32;
 constexpr uint32_t kGuStage = 2 * kGuCodes + 2 * kGuScales;
 constexpr uint32_t kGuRed = 2u * kMxWarps * 4 * 32 * 16;  // two buffers of the warps' partial tiles
-constexpr int kGuTileRows = 512;  // tiles of a CTA whose first weight row is kept in shared memory
 
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {
@@ -144,120 +143,203 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void* tm, i
 }  // namespace
 
 // ---------------------------------------------------------------------------
-// route: top-k, softmax weights, fp16 activations, grouping (one CTA, 1024 threads)
+// route: top-k and softmax weights of one token per CTA, its fp16 activations
 // ---------------------------------------------------------------------------
-constexpr int kRouteThreads = 1024;
+constexpr int kRouteThreads = 1024;  // one logit per thread (E <= 1024)
 
-namespace {
-
-}  // namespace
-
-template <int PER>
+// CTA t routes token t: thread e holds logit e; the top_k-th largest key is
+// found bit by bit from the top with block-wide counts (__syncthreads_count),
+// stopping as soon as the keys matching the prefix are exactly the ones still
+// needed; equal keys at the threshold are taken in expert order. The selected
+// experts are ranked (larger logit first, ties to the lower index) and written
+// with their softmax probabilities. In the same CTA: max |x| of the token and
+// x * 2^-sigma in fp16 (sigma an exact power of two that puts max |x| in
+// [2^14, 2^15)). The grouping into virtual experts is left to the kernels that
+// use it (each CTA builds it from idx), so no CTA waits for another.
 __global__ void __launch_bounds__(kRouteThreads) moe_mx_route_mma_kernel(
-    const float* __restrict__ logits, const uint16_t* __restrict__ x, int T, int H, int E, int top_k,
+    const float* __restrict__ logits, const uint16_t* __restrict__ x, int H, int E, int top_k,
     int32_t* __restrict__ idx, float* __restrict__ wts, int32_t* __restrict__ xexp, uint16_t* __restrict__ xh,
-    int32_t* __restrict__ vexp, int32_t* __restrict__ nvirt, uint32_t* __restrict__ hmax) {
-  __shared__ uint32_t sel_k[32][32];
-  __shared__ int sel_e[32][32];
-  __shared__ int pe[kRouteThreads];      // expert of pair p = t * top_k + slot
-  __shared__ int cnt[kRouteThreads];     // pairs per expert, then the experts' offsets
-  __shared__ int sorder[kRouteThreads];  // pairs sorted by expert (stable)
-  __shared__ uint32_t amax[kRouteThreads];
-  __shared__ int wsum[33];
+    uint32_t* __restrict__ hmax) {
+  __shared__ float s_mx[32], s_sum[32];
+  __shared__ uint32_t s_xm[32];
+  __shared__ int s_eq[32];
+  __shared__ uint32_t sel_k[32];
+  __shared__ int sel_e[32];
+  __shared__ int s_n;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int P = T * top_k;
-  const int cpt = H >> 3;  // 16-byte chunks of x per token (a multiple of 32)
-  amax[tid] = 0u;
-  cnt[tid] = 0;
-  __syncthreads();
+  const int t = blockIdx.x;
+  const int cpt = H >> 3;  // 16-byte chunks of x per token
+  const bool valid = tid < E;
+  if (tid == 0) s_n = 0;
   pdl_wait();  // the logits and x may come from the previous kernel
-  for (int t = warp; t < T; t += 32)
-    route_token<PER>(logits + (size_t)t * E, E, top_k, lane, sel_k[warp], sel_e[warp], idx + (size_t)t * top_k,
-                wts + (size_t)t * top_k, pe + t * top_k);
-  // max |x| per token, then x * 2^-sigma in fp16 (exact scaling; sigma puts
-  // max |x| in [2^14, 2^15)). The 16-byte chunks of x are read in rounds of
-  // kXb per thread, every load of a round issued before any is used (one
-  // round trip per round instead of one per chunk); the 32 chunks of a warp
-  // belong to one token.
-  constexpr int kXb = 8;
-  const uint4* x4 = reinterpret_cast<const uint4*>(x);
-  const int nch = T * cpt;
-  for (int b0 = 0; b0 < nch; b0 += kXb * kRouteThreads) {
-    uint4 xv[kXb];
+  // every load first: logit tid of the token and the thread's chunks of x
+  constexpr int kXr = 2;  // chunks a thread keeps in registers (H <= 16384); the rest is read twice
+  const uint4* x4 = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+  const float l = valid ? __ldg(logits + (size_t)t * E + tid) : 0.f;
+  uint4 xv[kXr];
 #pragma unroll
-    for (int i = 0; i < kXb; ++i) {
-      const int q = b0 + tid + i * kRouteThreads;
-      xv[i] = q < nch ? __ldg(x4 + q) : make_uint4(0u, 0u, 0u, 0u);
-    }
+  for (int i = 0; i < kXr; ++i) {
+    const int q = tid + i * kRouteThreads;
+    xv[i] = q < cpt ? __ldg(x4 + q) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  auto absmax8 = [](const uint4& w) {
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+    float m = 0.f;
 #pragma unroll
-    for (int i = 0; i < kXb; ++i) {
-      const int q0 = b0 + warp * 32 + i * kRouteThreads;  // the warp's first chunk of this load
-      if (q0 >= nch) break;                               // warp-uniform
-      const uint32_t ww[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
-      float m = 0.f;
+    for (int j = 0; j < 4; ++j)
+      m = fmaxf(m, fmaxf(fabsf(bf16_bits_to_f32(ww[j] & 0xFFFFu)), fabsf(bf16_bits_to_f32(ww[j] >> 16))));
+    return m;
+  };
+  float xm = 0.f;
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        m = fmaxf(m, fmaxf(fabsf(bf16_bits_to_f32(ww[j] & 0xFFFFu)), fabsf(bf16_bits_to_f32(ww[j] >> 16))));
-      const unsigned mb = __reduce_max_sync(kFull, __float_as_uint(m));  // non-negative: uint order
-      if (lane == 0) atomicMax(&amax[q0 / cpt], mb);
-    }
+  for (int i = 0; i < kXr; ++i) xm = fmaxf(xm, absmax8(xv[i]));
+  for (int q = tid + kXr * kRouteThreads; q < cpt; q += kRouteThreads) xm = fmaxf(xm, absmax8(__ldg(x4 + q)));
+  // block maxima of the logits and of |x|
+  float lm = valid ? l : -INFINITY;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lm = fmaxf(lm, __shfl_xor_sync(kFull, lm, o));
+    xm = fmaxf(xm, __shfl_xor_sync(kFull, xm, o));
+  }
+  if (lane == 0) {
+    s_mx[warp] = lm;
+    s_xm[warp] = __float_as_uint(xm);
   }
   __syncthreads();
-  pdl_launch_dependents();
-  if (tid < T) xexp[tid] = fp16_prescale_exp(__uint_as_float(amax[tid]));
-  for (int b0 = 0; b0 < nch; b0 += kXb * kRouteThreads) {
-    uint4 xv[kXb];
+  float mx = s_mx[lane];
+  uint32_t xmb = s_xm[lane];  // non-negative floats: integer order
 #pragma unroll
-    for (int i = 0; i < kXb; ++i) {
-      const int q = b0 + tid + i * kRouteThreads;
-      xv[i] = q < nch ? __ldg(x4 + q) : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int i = 0; i < kXb; ++i) {
-      const int q = b0 + tid + i * kRouteThreads;
-      if (q >= nch) break;
-      const float sc = pow2f(-fp16_prescale_exp(__uint_as_float(amax[q / cpt])));
-      const uint4 w = xv[i];
-      uint4 o;
-      o.x = f16x2_rn(bf16_bits_to_f32(w.x & 0xFFFFu) * sc, bf16_bits_to_f32(w.x >> 16) * sc);
-      o.y = f16x2_rn(bf16_bits_to_f32(w.y & 0xFFFFu) * sc, bf16_bits_to_f32(w.y >> 16) * sc);
-      o.z = f16x2_rn(bf16_bits_to_f32(w.z & 0xFFFFu) * sc, bf16_bits_to_f32(w.z >> 16) * sc);
-      o.w = f16x2_rn(bf16_bits_to_f32(w.w & 0xFFFFu) * sc, bf16_bits_to_f32(w.w >> 16) * sc);
-      reinterpret_cast<uint4*>(xh)[q] = o;
-    }
+  for (int o = 16; o > 0; o >>= 1) {
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+    xmb = max(xmb, __shfl_xor_sync(kFull, xmb, o));
   }
-  // grouping: pairs per expert, stable order by expert, virtual experts of <= kMxTC pairs
-  for (int p = tid; p < P; p += kRouteThreads) {
-    atomicAdd(&cnt[pe[p]], 1);
+  pdl_launch_dependents();
+  // x * 2^-sigma in fp16 (exact scaling)
+  const int sig = fp16_prescale_exp(__uint_as_float(xmb));
+  if (tid == 0) xexp[t] = sig;
+  const float sc = pow2f(-sig);
+  uint4* xo = reinterpret_cast<uint4*>(xh + (size_t)t * H);
+  auto scale8 = [sc](const uint4& w) {
+    uint4 o;
+    o.x = f16x2_rn(bf16_bits_to_f32(w.x & 0xFFFFu) * sc, bf16_bits_to_f32(w.x >> 16) * sc);
+    o.y = f16x2_rn(bf16_bits_to_f32(w.y & 0xFFFFu) * sc, bf16_bits_to_f32(w.y >> 16) * sc);
+    o.z = f16x2_rn(bf16_bits_to_f32(w.z & 0xFFFFu) * sc, bf16_bits_to_f32(w.z >> 16) * sc);
+    o.w = f16x2_rn(bf16_bits_to_f32(w.w & 0xFFFFu) * sc, bf16_bits_to_f32(w.w >> 16) * sc);
+    return o;
+  };
+#pragma unroll
+  for (int i = 0; i < kXr; ++i) {
+    const int q = tid + i * kRouteThreads;
+    if (q < cpt) xo[q] = scale8(xv[i]);
+  }
+  for (int q = tid + kXr * kRouteThreads; q < cpt; q += kRouteThreads) xo[q] = scale8(__ldg(x4 + q));
+  // softmax denominator: warp sums now, the block sum after the select's barriers
+  float ev = valid ? expf(l - mx) : 0.f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ev += __shfl_xor_sync(kFull, ev, o);
+  if (lane == 0) s_sum[warp] = ev;
+  // radix select of the top_k-th largest key
+  const uint32_t key = valid ? logit_key(l) : 0u;
+  uint32_t prefix = 0u, mask = 0u;
+  int need = top_k, match = E;  // keys still needed among those matching the prefix; how many match
+  for (int b = 31; b >= 0 && match != need; --b) {
+    const uint32_t bit = 1u << b, m2 = mask | bit, want = prefix | bit;
+    const int cnt = __syncthreads_count(valid && (key & m2) == want);
+    if (cnt >= need) {
+      prefix = want;
+      match = cnt;
+    } else {
+      need -= cnt;
+      match -= cnt;
+    }
+    mask = m2;
+  }
+  // every key above the prefix range, and `need` of the keys in it in expert order
+  const uint32_t km = key & mask;
+  const bool eq = valid && km == prefix;
+  bool take = valid && km > prefix;
+  if (match == need) {
+    take = take || eq;
+  } else {  // all bits fixed and more equal keys than needed: the lowest expert indices
+    const unsigned eqb = __ballot_sync(kFull, eq);
+    if (lane == 0) s_eq[warp] = __popc(eqb);
+    __syncthreads();
+    int before = __popc(eqb & ((1u << lane) - 1u));
+    for (int w = 0; w < warp; ++w) before += s_eq[w];
+    take = take || (eq && before < need);
+  }
+  if (take) {
+    const int pos = atomicAdd(&s_n, 1);
+    sel_k[pos] = key;
+    sel_e[pos] = tid;
+  }
+  __syncthreads();
+  float sm = s_sum[lane];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(kFull, sm, o);
+  if (tid < top_k) {
+    const uint32_t kj = sel_k[tid];
+    const int ej = sel_e[tid];
+    int rank = 0;
+    for (int j = 0; j < top_k; ++j) {
+      const uint32_t kl = sel_k[j];
+      rank += (kl > kj) || (kl == kj && sel_e[j] < ej);
+    }
+    const int p = t * top_k + rank;
+    idx[p] = ej;
+    wts[p] = expf(key_logit(kj) - mx) / sm;
     hmax[p] = 0u;
   }
-  __syncthreads();
-  const int n_e = tid < E ? cnt[tid] : 0;
-  int total_pairs, total_v;
-  const int off = cta_exclusive_scan(n_e, wsum, total_pairs);
-  const int nv_e = (n_e + kMxTC - 1) / kMxTC;
-  const int voff = cta_exclusive_scan(nv_e, wsum, total_v);
-  if (tid < E) cnt[tid] = off;
-  __syncthreads();
-  for (int p = tid; p < P; p += kRouteThreads) {
-    const int e = pe[p];
-    int r = 0;
-    for (int q = 0; q < p; ++q) r += pe[q] == e;
-    sorder[cnt[e] + r] = p;
+}
+
+// Virtual experts of the batch from the routing table idx [T][top_k]
+// (T <= 32): the pairs (token, slot) of every expert in token order, cut into
+// runs of at most kMxTC pairs (the N = 8 columns of one MMA), experts in index
+// order. Table entry v: {expert, pair count, kMxTC pairs (-1 padded)} as
+// int16. Every thread of the CTA calls it; returns the number of entries.
+// Scratch: 3 E words of shared memory.
+constexpr int kVt = 2 + kMxTC;  // int16 per table entry
+__device__ int mx_group(const int32_t* __restrict__ idx, int T, int E, int top_k, int* cnt, uint32_t* msk,
+                        int* voff, int16_t* vt) {
+  __shared__ int wsum[33];
+  const int P = T * top_k;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    cnt[e] = 0;
+    msk[e] = 0u;
   }
   __syncthreads();
-  if (tid < E) {
-    for (int c = 0; c < nv_e; ++c) {
-      int32_t* ent = vexp + (size_t)(voff + c) * kMxVexpInts;
-      const int n = min(kMxTC, n_e - c * kMxTC);
-      ent[0] = tid;
-      ent[1] = n;
-#pragma unroll
-      for (int j = 0; j < kMxTC; ++j) ent[2 + j] = j < n ? sorder[off + c * kMxTC + j] : -1;
+  for (int p = threadIdx.x; p < P; p += blockDim.x) {
+    const int e = __ldcg(idx + p);
+    atomicAdd(&cnt[e], 1);
+    atomicOr(&msk[e], 1u << (p / top_k));
+  }
+  __syncthreads();
+  // exclusive scan of the entries per expert; thread i owns experts [i EPT, (i + 1) EPT)
+  const int ept = (E + (int)blockDim.x - 1) / (int)blockDim.x;
+  const int e0 = threadIdx.x * ept;
+  int mine = 0;
+  for (int e = e0; e < min(E, e0 + ept); ++e) mine += (cnt[e] + kMxTC - 1) / kMxTC;
+  int nv;
+  int run = cta_exclusive_scan(mine, wsum, nv);
+  for (int e = e0; e < min(E, e0 + ept); ++e) {
+    voff[e] = run;
+    run += (cnt[e] + kMxTC - 1) / kMxTC;
+  }
+  for (int q = threadIdx.x; q < nv * kVt; q += blockDim.x) vt[q] = -1;
+  __syncthreads();
+  for (int p = threadIdx.x; p < P; p += blockDim.x) {
+    const int e = __ldcg(idx + p), t = p / top_k;
+    const int r = __popc(msk[e] & ((1u << t) - 1u));  // earlier tokens with this expert
+    int16_t* ent = vt + (voff[e] + r / kMxTC) * kVt;
+    const int j = r % kMxTC;
+    ent[2 + j] = (int16_t)p;
+    if (j == 0) {
+      ent[0] = (int16_t)e;
+      ent[1] = (int16_t)min(kMxTC, cnt[e] - r);
     }
   }
-  if (tid == 0) nvirt[0] = total_v;
-  (void)total_pairs;
+  __syncthreads();
+  return nv;
 }
 
 
@@ -267,20 +349,19 @@ __global__ void __launch_bounds__(kRouteThreads) moe_mx_route_mma_kernel(
 struct MxGuArgs {
   const uint16_t* xh;    // [T][H] fp16 x * 2^-sigma_t
   const int32_t* xexp;   // [T] sigma_t
-  const int32_t* vexp;   // [nv][kMxVexpInts]: expert, pair count, kMxTC pairs (-1 padded)
-  const int32_t* nvirt;
+  const int32_t* idx;    // [T][top_k] routed experts
   float* h;              // [P][I]
   uint32_t* hmax;        // [P] bits of max |h|
-  int H, I, top_k, ST, BPW;  // BPW: 32-k blocks per warp and stage (stage = 512 BPW k)
+  int H, I, T, E, top_k, ST, BPW;  // BPW: 32-k blocks per warp and stage (stage = 512 BPW k)
   uint32_t* err;
 };
 
-// x row of pair g of the tile's virtual expert; columns past the pair count
-// take pair 0's row (their MMA results are never read)
-__device__ __forceinline__ const uint16_t* gu_xrow(const MxGuArgs& a, int tile, int tpv, int g) {
-  const int32_t* ent = a.vexp + (size_t)(tile / tpv) * kMxVexpInts;
-  const int j = min(g, __ldg(ent + 1) - 1);
-  return a.xh + (size_t)(__ldg(ent + 2 + j) / a.top_k) * a.H;
+// x row of pair g of the tile's virtual expert (shared-memory table); columns
+// past the pair count take pair 0's row (their MMA results are never read)
+__device__ __forceinline__ const uint16_t* gu_xrow(const MxGuArgs& a, const int16_t* vt, int tile, int tpv, int g) {
+  const int16_t* ent = vt + (tile / tpv) * kVt;
+  const int j = min(g, ent[1] - 1);
+  return a.xh + (size_t)(ent[2 + j] / a.top_k) * a.H;
 }
 
 // BPW: 32-k blocks per warp and stage (a stage is 512 BPW k of the tile's rows)
@@ -293,12 +374,12 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const gbase = smem_raw + (base - raw);
-  // shared layout: stages | red (two buffers) | full barriers | release counters | first weight
-  //                row of each of this CTA's tiles
+  // shared layout: stages | red (two buffers; the grouping's scratch before the
+  //                first tile) | full barriers | release counters | virtual-expert table
   float4* red = reinterpret_cast<float4*>(gbase + (size_t)a.ST * kGuStage);
   uint64_t* full = reinterpret_cast<uint64_t*>(gbase + (size_t)a.ST * kGuStage + kGuRed);
   uint32_t* rel = reinterpret_cast<uint32_t*>(full + a.ST);
-  int* trow = reinterpret_cast<int*>(rel + a.ST);
+  int16_t* vt = reinterpret_cast<int16_t*>(rel + a.ST);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.ST; ++i) {
@@ -315,26 +396,19 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   constexpr uint32_t kSRow = 16u * BPW;    // scale bytes of one row in a stage
   const int nks = H / KS;                   // stages per tile
   const int tpv = I / 32;                   // tiles per virtual expert
-  const int total = *a.nvirt * tpv;
+  int* scratch = reinterpret_cast<int*>(red);  // free until the first tile ends
+  const int nv = mx_group(a.idx, a.T, a.E, a.top_k, scratch, reinterpret_cast<uint32_t*>(scratch + a.E),
+                          scratch + 2 * a.E, vt);
+  const int total = nv * tpv;
   const int per = (total + (int)gridDim.x - 1) / (int)gridDim.x;
   const int t0 = min(total, (int)blockIdx.x * per), t1 = min(total, t0 + per);
   const int nstages = (t1 - t0) * nks;
   const uint64_t pol = policy_evict_first();
-  for (int t = threadIdx.x; t < t1 - t0 && t < kGuTileRows; t += blockDim.x) {
-    const int v = (t0 + t) / tpv;
-    trow[t] = __ldg(a.vexp + (size_t)v * kMxVexpInts) * I + (t0 + t - v * tpv) * 32;
-  }
-  __syncthreads();
   // stage q of this CTA into its slot: codes and scales of 32 gate and 32 up rows, 512 BPW k
   auto issue = [&](int q) {
     const int tl = q / nks, ks = q - tl * nks;
-    int row;
-    if (tl < kGuTileRows) {
-      row = trow[tl];
-    } else {
-      const int v = (t0 + tl) / tpv;
-      row = __ldg(a.vexp + (size_t)v * kMxVexpInts) * I + (t0 + tl - v * tpv) * 32;
-    }
+    const int v = (t0 + tl) / tpv;
+    const int row = vt[v * kVt] * I + (t0 + tl - v * tpv) * 32;
     const int st = q % a.ST;
     const uint32_t sb = base + st * kGuStage;
     mbar_arrive_expect_tx(&full[st], (2 * 4096u + 512u) * 2u * BPW);
@@ -365,7 +439,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   bool ok = true;
   // x of the next stage, loaded one stage ahead (L2-resident)
   uint4 xn[BPW];
-  const uint16_t* xrow = t0 < t1 ? gu_xrow(a, t0, tpv, g) : a.xh;
+  const uint16_t* xrow = t0 < t1 ? gu_xrow(a, vt, t0, tpv, g) : a.xh;
   auto load_x = [&](const uint16_t* row, int ks) {
 #pragma unroll
     for (int j = 0; j < BPW; ++j)
@@ -374,12 +448,12 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   if (t0 < t1) load_x(xrow, 0);
   for (int tile = t0; tile < t1; ++tile) {
     const int v = tile / tpv, r0 = (tile - v * tpv) * 32;
-    const int32_t* ent = a.vexp + (size_t)v * kMxVexpInts;
-    const int np = __ldg(ent + 1);
-    const uint16_t* xnext = tile + 1 < t1 ? gu_xrow(a, tile + 1, tpv, g) : xrow;
+    const int16_t* ent = vt + v * kVt;
+    const int np = ent[1];
+    const uint16_t* xnext = tile + 1 < t1 ? gu_xrow(a, vt, tile + 1, tpv, g) : xrow;
     // this thread's epilogue column (pair) and its 2^sigma, fetched early
     const int ecol = 2 * (et & 3) + ((et >> 5) & 1);
-    const int epair = ecol < np ? __ldg(ent + 2 + ecol) : 0;
+    const int epair = ecol < np ? ent[2 + ecol] : 0;
     const float esc = pow2f(__ldg(a.xexp + epair / a.top_k));
     float acc[4][4];
 #pragma unroll
@@ -476,23 +550,46 @@ __global__ void __launch_bounds__(256) moe_mx_hprep_kernel(const float* __restri
   pdl_wait();  // h and its maxima come from gate/up
   pdl_launch_dependents();
   const int P = T * top_k;
+  const int lane = threadIdx.x & 31;
   const long long n8 = (long long)(P + 1) * I / 8;
-  for (long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x; q < n8; q += (long long)gridDim.x * blockDim.x) {
-    const int p = (int)(q * 8 / I);
-    uint4 o = make_uint4(0u, 0u, 0u, 0u);
-    if (p < P) {
-      const int t0 = (p / top_k) * top_k;
-      float m = 0.f;
-      for (int j = 0; j < top_k; ++j) m = fmaxf(m, wts[t0 + j] * __uint_as_float(hmax[t0 + j]));
-      const float f = wts[p] * pow2f(-fp16_prescale_exp(m));
-      const float4 lo = __ldcg(reinterpret_cast<const float4*>(h + q * 8));
-      const float4 hi = __ldcg(reinterpret_cast<const float4*>(h + q * 8 + 4));
-      o.x = f16x2_rn(lo.x * f, lo.y * f);
-      o.y = f16x2_rn(lo.z * f, lo.w * f);
-      o.z = f16x2_rn(hi.x * f, hi.y * f);
-      o.w = f16x2_rn(hi.z * f, hi.w * f);
+  // 2^-sigma_t of token tok (warp-uniform): its pairs' p |h| maxima, one load per lane
+  auto token_scale = [&](int tok) {
+    float m = 0.f;
+    for (int j = lane; j < top_k; j += 32)
+      m = fmaxf(m, __ldcg(wts + tok * top_k + j) * __uint_as_float(__ldcg(hmax + tok * top_k + j)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+    return pow2f(-fp16_prescale_exp(m));
+  };
+  // the loop is uniform over the block: every lane of a warp takes part in the shuffles
+  for (long long q0 = (long long)blockIdx.x * blockDim.x; q0 < n8; q0 += (long long)gridDim.x * blockDim.x) {
+    const long long q = q0 + threadIdx.x;
+    const int p = q < n8 ? (int)(q * 8 / I) : P;
+    const int tok = p < P ? p / top_k : -1;
+    float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
+    if (tok >= 0) {  // h first, so its latency overlaps the scale's loads
+      lo = __ldcg(reinterpret_cast<const float4*>(h + q * 8));
+      hi = __ldcg(reinterpret_cast<const float4*>(h + q * 8 + 4));
     }
-    reinterpret_cast<uint4*>(hh)[q] = o;
+    // a warp's items cover one or two tokens (at least 32 items per token);
+    // any other token falls back to its own loop
+    const int ta = __shfl_sync(kFull, tok, 0), tb = __shfl_sync(kFull, tok, 31);
+    const float fa = ta >= 0 ? token_scale(ta) : 0.f;
+    const float fb = (tb >= 0 && tb != ta) ? token_scale(tb) : fa;
+    float f = tok == ta ? fa : fb;
+    if (tok >= 0 && tok != ta && tok != tb) {
+      float m = 0.f;
+      for (int j = 0; j < top_k; ++j)
+        m = fmaxf(m, __ldcg(wts + tok * top_k + j) * __uint_as_float(__ldcg(hmax + tok * top_k + j)));
+      f = pow2f(-fp16_prescale_exp(m));
+    }
+    f *= tok >= 0 ? __ldcg(wts + p) : 0.f;
+    uint4 o;
+    o.x = f16x2_rn(lo.x * f, lo.y * f);
+    o.y = f16x2_rn(lo.z * f, lo.w * f);
+    o.z = f16x2_rn(hi.x * f, hi.y * f);
+    o.w = f16x2_rn(hi.z * f, hi.w * f);
+    if (q < n8) reinterpret_cast<uint4*>(hh)[q] = o;
   }
 }
 
@@ -503,10 +600,9 @@ struct MxDnArgs {
   const uint16_t* hh;     // [P + 1][I] fp16 p h 2^-sigma_t of every pair (moe_mx_hprep_kernel), then a zero row
   const uint32_t* hmax;   // [P]
   const float* wts;       // [P] routing weights
-  const int32_t* vexp;
-  const int32_t* nvirt;
+  const int32_t* idx;     // [T][top_k] routed experts
   float* y;               // [T][H]
-  int T, H, I, top_k, R, ST, BPW, nvmax;
+  int T, H, I, E, top_k, R, ST, BPW, nvmax;
   uint32_t stage_bytes, o_s;  // stage size; offset of the scales in a stage
   uint32_t* err;
 };
@@ -584,22 +680,28 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   pdl_launch_dependents();
   const int H = a.H, I = a.I;
   const int nks = I / KS;
-  const int nv = *a.nvirt;
   const int n0 = blockIdx.x * R;
+  // the virtual experts, built in the (still empty) stage ring: scratch, then the table
+  int* scratch = reinterpret_cast<int*>(gbase);
+  int16_t* vt = reinterpret_cast<int16_t*>(scratch + 3 * a.E);
+  const int nv = mx_group(a.idx, a.T, a.E, a.top_k, scratch, reinterpret_cast<uint32_t*>(scratch + a.E),
+                          scratch + 2 * a.E, vt);
   // CTAs walk the virtual experts from different starting points (no L2 hot spot on one h row)
   const int vstart = nv > 0 ? (int)(((long long)blockIdx.x * nv) / gridDim.x) : 0;
   const int nstages = nv * nks;
   const uint64_t pol = policy_evict_first();
-  for (int v2 = threadIdx.x; v2 < nv; v2 += blockDim.x) vrow[v2] = __ldg(a.vexp + (size_t)v2 * kMxVexpInts) * H + n0;
+  for (int v2 = threadIdx.x; v2 < nv; v2 += blockDim.x) vrow[v2] = vt[v2 * kVt] * H + n0;
   for (int q = threadIdx.x; q < nv * 8 * NT; q += blockDim.x) tab[q] = -1;
   __syncthreads();
   for (int q = threadIdx.x; q < nv * kMxTC; q += blockDim.x) {
     const int v2 = q / kMxTC, j = q - v2 * kMxTC;
-    if (j < __ldg(a.vexp + (size_t)v2 * kMxVexpInts + 1)) {
-      const int pair = __ldg(a.vexp + (size_t)v2 * kMxVexpInts + 2 + j);
+    if (j < vt[v2 * kVt + 1]) {
+      const int pair = vt[v2 * kVt + 2 + j];
       tab[v2 * 8 * NT + pair / a.top_k] = (int16_t)pair;
     }
   }
+  // the ring's generic writes (scratch, table) before the copies that refill it
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   __syncthreads();
   // stage q of this CTA into its slot: codes and scales of its R rows of one virtual expert, KS k
   auto issue = [&](int q) {
@@ -770,11 +872,13 @@ MxDnPlan plan_down(int T, int H, int I, int top_k, int nvmax, int sms) {
   return p;
 }
 
-int plan_gateup_stages() {
-  return (int)std::min<size_t>(8, (kMxSmem - 1024 - kGuRed - 4 * kGuTileRows - 64) / (kGuStage + 16));
+int plan_gateup_stages(int nvmax) {
+  return (int)std::min<size_t>(8, (kMxSmem - 1024 - kGuRed - 2 * kVt * (size_t)nvmax - 64) / (kGuStage + 16));
 }
 
-size_t gateup_smem(int ST) { return 1024 + (size_t)ST * (kGuStage + 16) + kGuRed + 4 * kGuTileRows + 64; }
+size_t gateup_smem(int ST, int nvmax) {
+  return 1024 + (size_t)ST * (kGuStage + 16) + kGuRed + 2 * kVt * (size_t)nvmax + 64;
+}
 
 template <int NT, int MT, int BPW>
 cudaError_t launch_down(const CUtensorMap& tm_dq, const CUtensorMap& tm_ds, const MxDnArgs& da, const MxDnPlan& pd,
@@ -810,31 +914,27 @@ cudaError_t launch_gateup(const CUtensorMap* tm, const MxGuArgs& ga, int grid, s
 bool moe_mx_mma_ok(int T, int H, int I, int E, int top_k) {
   if (T < 1 || T > 32 || E < 1 || E > 1024 || top_k < 1 || top_k > 32 || top_k > E) return false;
   if (H < 512 || I < 512 || H % 512 || I % 512) return false;
-  const MxDnPlan pd = plan_down(T, H, I, top_k, moe_nvirt_max(T, E, top_k), device_sm_count());
+  const int nvmax = moe_nvirt_max(T, E, top_k);
+  const MxDnPlan pd = plan_down(T, H, I, top_k, nvmax, device_sm_count());
   if (pd.ST < 2 || (size_t)kMxWarps * pd.MT * pd.NT * 512 > (size_t)pd.ST * pd.stage_bytes) return false;
-  return plan_gateup_stages() >= 2;
+  // the down kernel builds the virtual-expert table in its stage ring before the first copy
+  if ((size_t)12 * E + 2 * kVt * (size_t)nvmax > (size_t)pd.ST * pd.stage_bytes) return false;
+  return plan_gateup_stages(nvmax) >= 2;
 }
 
 cudaError_t launch_moe_mx_mma(const uint16_t* x, const float* logits, const uint8_t* gq, const uint8_t* gs,
                               const uint8_t* uq, const uint8_t* us, const uint8_t* dq, const uint8_t* ds, int T,
                               int H, int I, int E, int top_k, float* y, int32_t* idx, float* wts, int32_t* xexp,
-                              uint16_t* xh, int32_t* vexp, int32_t* nvirt, uint32_t* hmax, float* h, uint16_t* hh,
-                              uint32_t* err, cudaStream_t stream, bool pdl) {
+                              uint16_t* xh, uint32_t* hmax, float* h, uint16_t* hh, uint32_t* err,
+                              cudaStream_t stream, bool pdl) {
   const int sms = device_sm_count();
-  cudaError_t e;
-  if (E <= 128)
-    e = launch_kernel(moe_mx_route_mma_kernel<4>, dim3(1), dim3(kRouteThreads), 0, stream, pdl, logits, x, T, H, E,
-                      top_k, idx, wts, xexp, xh, vexp, nvirt, hmax);
-  else if (E <= 512)
-    e = launch_kernel(moe_mx_route_mma_kernel<16>, dim3(1), dim3(kRouteThreads), 0, stream, pdl, logits, x, T, H, E,
-                      top_k, idx, wts, xexp, xh, vexp, nvirt, hmax);
-  else
-    e = launch_kernel(moe_mx_route_mma_kernel<32>, dim3(1), dim3(kRouteThreads), 0, stream, pdl, logits, x, T, H, E,
-                      top_k, idx, wts, xexp, xh, vexp, nvirt, hmax);
+  const int nvmax = moe_nvirt_max(T, E, top_k);
+  cudaError_t e = launch_kernel(moe_mx_route_mma_kernel, dim3(T), dim3(kRouteThreads), 0, stream, pdl, logits, x, H,
+                                E, top_k, idx, wts, xexp, xh, hmax);
   if (e != cudaSuccess) return e;
   // E2M1 codes as [rows][128-byte chunks] with 128B swizzle; E8M0 scales as 16 BPW-byte boxes
   const int gbpw = H % 1024 == 0 ? 2 : 1;
-  const MxDnPlan pd = plan_down(T, H, I, top_k, moe_nvirt_max(T, E, top_k), sms);
+  const MxDnPlan pd = plan_down(T, H, I, top_k, nvmax, sms);
   CUtensorMap tm_gq, tm_uq, tm_gs, tm_us, tm_dq, tm_ds;
   const uint64_t rows_gu = (uint64_t)E * I, rows_d = (uint64_t)E * H;
   const uint32_t gb = 2 * gbpw, db = 2 * pd.BPW;
@@ -848,12 +948,12 @@ cudaError_t launch_moe_mx_mma(const uint16_t* x, const float* logits, const uint
       !tmap_2d(&tm_ds, CU_TENSOR_MAP_DATA_TYPE_UINT8, ds, I / 32, rows_d, I / 32, 8 * db, pd.R,
                scale_swizzle(8 * db)))
     return cudaErrorInvalidValue;
-  const int gst = plan_gateup_stages();
-  const MxGuArgs ga{xh, xexp, vexp, nvirt, h, hmax, H, I, top_k, gst, gbpw, err};
-  const int gu_grid = std::min(sms, moe_nvirt_max(T, E, top_k) * (I / 32));
+  const int gst = plan_gateup_stages(nvmax);
+  const MxGuArgs ga{xh, xexp, idx, h, hmax, H, I, T, E, top_k, gst, gbpw, err};
+  const int gu_grid = std::min(sms, nvmax * (I / 32));
   const CUtensorMap gmaps[4] = {tm_gq, tm_uq, tm_gs, tm_us};
-  e = gbpw == 2 ? launch_gateup<2>(gmaps, ga, gu_grid, gateup_smem(gst), stream, pdl)
-                : launch_gateup<1>(gmaps, ga, gu_grid, gateup_smem(gst), stream, pdl);
+  e = gbpw == 2 ? launch_gateup<2>(gmaps, ga, gu_grid, gateup_smem(gst, nvmax), stream, pdl)
+                : launch_gateup<1>(gmaps, ga, gu_grid, gateup_smem(gst, nvmax), stream, pdl);
   if (e != cudaSuccess) return e;
   {
     const long long n8 = (long long)(T * top_k + 1) * I / 8;
@@ -862,8 +962,7 @@ cudaError_t launch_moe_mx_mma(const uint16_t* x, const float* logits, const uint
                       (const uint32_t*)hmax, (const float*)wts, hh, T, I, top_k);
     if (e != cudaSuccess) return e;
   }
-  const MxDnArgs da{hh,    hmax,  wts,   vexp,   nvirt,    y, T, H, I, top_k, pd.R, pd.ST, pd.BPW,
-                    moe_nvirt_max(T, E, top_k), pd.stage_bytes, pd.o_s, err};
+  const MxDnArgs da{hh, hmax, wts, idx, y, T, H, I, E, top_k, pd.R, pd.ST, pd.BPW, nvmax, pd.stage_bytes, pd.o_s, err};
   if (pd.NT == 1)
     return pd.BPW == 4   ? launch_down_mt<1, 4>(tm_dq, tm_ds, da, pd, stream, pdl)
            : pd.BPW == 2 ? launch_down_mt<1, 2>(tm_dq, tm_ds, da, pd, stream, pdl)

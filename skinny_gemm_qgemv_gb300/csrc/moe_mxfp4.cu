@@ -59,8 +59,6 @@ MoeLayout moe_layout(int T, int H, int I, int E, int top_k) {
   L.h = take(sizeof(float) * P * I);
   L.hh = take(sizeof(uint16_t) * (P + 1) * I);  // + a zero row (the MMA path's down B)
   L.hexp = take(sizeof(int32_t) * P);
-  L.vexp = take(sizeof(int32_t) * (size_t)moe_nvirt_max(T, E, top_k) * kMxVexpInts);
-  L.nvirt = take(sizeof(int32_t) * 4);
   L.hmax = take(sizeof(uint32_t) * P);
   L.partial = take(0);
   L.has_tc = !moe_mx_mma_ok(T, H, I, E, top_k) && moe_mx_tc_ok(T, H, I, E, top_k);
@@ -397,9 +395,9 @@ cudaError_t launch_moe_mxfp4(const uint16_t* x, const float* logits, const uint8
   const bool aligned32 = ((reinterpret_cast<uintptr_t>(gq) | reinterpret_cast<uintptr_t>(uq) |
                            reinterpret_cast<uintptr_t>(dq)) & 31u) == 0;
   if (aligned && moe_mx_mma_ok(T, H, I, E, top_k)) {
-    // main path (T <= 32): routing + grouping in one CTA, then gate/up and down on warp-level MMA
+    // main path (T <= 32): routing (one CTA per token), then gate/up and down on warp-level MMA
     return launch_moe_mx_mma(x, logits, gq, gs, uq, us, dq, ds, T, H, I, E, top_k, y, idx, wts, I32(L.xexp),
-                             reinterpret_cast<uint16_t*>(base + L.xh), I32(L.vexp), I32(L.nvirt),
+                             reinterpret_cast<uint16_t*>(base + L.xh),
                              reinterpret_cast<uint32_t*>(base + L.hmax), reinterpret_cast<float*>(base + L.h),
                              reinterpret_cast<uint16_t*>(base + L.hh), err, stream, pdl);
   }

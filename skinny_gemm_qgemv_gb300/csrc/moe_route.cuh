@@ -22,7 +22,8 @@ __device__ __forceinline__ float key_logit(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// exclusive prefix sum of one value per thread of the CTA; every thread calls it
+// exclusive prefix sum of one value per thread of the CTA (blockDim a multiple
+// of 32); every thread calls it
 __device__ __forceinline__ int cta_exclusive_scan(int v, int* wsum, int& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int incl = v;
@@ -34,7 +35,7 @@ __device__ __forceinline__ int cta_exclusive_scan(int v, int* wsum, int& total) 
   if (lane == 31) wsum[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    const int w = wsum[lane];
+    const int w = lane < (int)(blockDim.x >> 5) ? wsum[lane] : 0;
     int wi = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {

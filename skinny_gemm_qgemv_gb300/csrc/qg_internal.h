@@ -218,7 +218,6 @@ cudaError_t launch_w8a16_gemv(const int8_t* wq, const float* scales, const uint1
 
 // MXFP4 MoE (moe_mxfp4.cu, moe_mx_mma.cu)
 constexpr int kMxTC = 8;                // pairs of one virtual expert: the N = 8 columns of one MMA
-constexpr int kMxVexpInts = 2 + kMxTC;  // virtual-expert table entry: expert, pair count, pairs
 // upper bound of the virtual experts of a batch: every active expert once, plus
 // one more for every further kMxTC pairs
 inline int moe_nvirt_max(int T, int E, int top_k) {
@@ -231,7 +230,7 @@ struct MoeTcLayout {
 };
 struct MoeLayout {
   size_t pair_expert, pair_weight, counts, offsets, active, order, nactive, xh, xexp, h, hh, hexp, partial;
-  size_t vexp, nvirt, hmax;
+  size_t hmax;
   bool has_tc;     // the tcgen05 path's scratch follows
   MoeTcLayout tc;
   size_t total;
@@ -247,8 +246,8 @@ cudaError_t launch_moe_mx_tc(const uint16_t* x, const float* logits, const uint8
 cudaError_t launch_moe_mx_mma(const uint16_t* x, const float* logits, const uint8_t* gq, const uint8_t* gs,
                               const uint8_t* uq, const uint8_t* us, const uint8_t* dq, const uint8_t* ds, int T,
                               int H, int I, int E, int top_k, float* y, int32_t* idx, float* wts, int32_t* xexp,
-                              uint16_t* xh, int32_t* vexp, int32_t* nvirt, uint32_t* hmax, float* h, uint16_t* hh,
-                              uint32_t* err, cudaStream_t stream, bool pdl);
+                              uint16_t* xh, uint32_t* hmax, float* h, uint16_t* hh, uint32_t* err,
+                              cudaStream_t stream, bool pdl);
 cudaError_t launch_moe_mxfp4(const uint16_t* x, const float* logits, const uint8_t* gq, const uint8_t* gs,
                              const uint8_t* uq, const uint8_t* us, const uint8_t* dq, const uint8_t* ds, int T,
                              int H, int I, int E, int top_k, float* y, int32_t* idx, float* wts, void* ws,
