@@ -607,31 +607,44 @@ struct MxDnArgs {
   uint32_t* err;
 };
 
-// a lane's tokens 8 nt + g in one virtual expert: the fp16 B row of the
-// token's pair (a token not in it: the zero row, so its column of B is 0);
-// act: n tiles with at least one of their tokens in it
+// A lane's B columns in one virtual expert. Token columns (PC false): the
+// columns are the batch's tokens 8 nt + g, B the fp16 row of the token's pair
+// in this virtual expert (a token not in it: the zero row, so its column of B
+// is 0); act: n tiles with at least one of their tokens in it. Pair columns
+// (PC true, one n tile): column j is pair j of the virtual expert (past its
+// pair count: the zero row); tk0, tk1: the tokens of the lane's accumulator
+// columns 2c, 2c + 1, or -1.
 template <int NT>
 struct DnLane {
   const uint16_t* hp[NT];
   uint32_t act;
+  int tk0, tk1;
 };
 
-// from the shared table: pair of (virtual expert, token) or -1
-template <int NT>
-__device__ __forceinline__ void dn_lane(const MxDnArgs& a, int v, int g, const int16_t* tab, DnLane<NT>& L) {
+// from the shared table: token columns, [nvmax][8 NT] pair of (virtual
+// expert, token) or -1; pair columns, [nvmax][8] pairs of the virtual expert
+// or -1
+template <int NT, bool PC>
+__device__ __forceinline__ void dn_lane(const MxDnArgs& a, int v, int g, int c, const int16_t* tab, DnLane<NT>& L) {
   L.act = 0u;
   const int P = a.T * a.top_k;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int pair = tab[v * 8 * NT + 8 * nt + g];
     L.hp[nt] = a.hh + (size_t)(pair >= 0 ? pair : P) * a.I;
-    if (__any_sync(kFull, pair >= 0)) L.act |= 1u << nt;
+    if (PC || __any_sync(kFull, pair >= 0)) L.act |= 1u << nt;
+  }
+  if (PC) {
+    const int p0 = tab[v * 8 + 2 * c], p1 = tab[v * 8 + 2 * c + 1];
+    L.tk0 = p0 >= 0 ? p0 / a.top_k : -1;
+    L.tk1 = p1 >= 0 ? p1 / a.top_k : -1;
   }
 }
 
 // NT: n tiles of 8 tokens (T <= 8 NT); MT: 16-row blocks per CTA (R = 16 MT);
-// BPW: 32-k blocks per warp and stage (a stage is 512 BPW k)
-template <int NT, int MT, int BPW>
+// BPW: 32-k blocks per warp and stage (a stage is 512 BPW k); PC: pair
+// columns (NT = 1) with per-warp token sums in shared memory, for T > 8
+template <int NT, int MT, int BPW, bool PC>
 __global__ void __launch_bounds__(kMxThreads, 1)
     moe_mx_dn_mma_kernel(const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_ds,
                          const MxDnArgs a) {
@@ -645,12 +658,15 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   constexpr uint32_t kStage = (272u * R * BPW + 1023u) & ~1023u;
   constexpr uint32_t kSRow = 16u * BPW;
   // shared layout: stages (the cross-warp sums reuse them at the end) | sigma per token |
-  //                full barriers | release counters
+  //                full barriers | release counters | first weight rows | pair table |
+  //                (pair columns) per-warp token sums [warp][R][T]
   int* sig = reinterpret_cast<int*>(gbase + (size_t)a.ST * kStage);
-  uint64_t* full = reinterpret_cast<uint64_t*>(sig + 8 * NT);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sig + 32);
   uint32_t* rel = reinterpret_cast<uint32_t*>(full + a.ST);
   int* vrow = reinterpret_cast<int*>(rel + a.ST);  // first weight row of each virtual expert's range
   int16_t* tab = reinterpret_cast<int16_t*>(vrow + a.nvmax);              // [nvmax][8 NT] pair or -1
+  float* ys = reinterpret_cast<float*>(
+      (reinterpret_cast<uintptr_t>(tab + (size_t)a.nvmax * 8 * NT) + 15) & ~(uintptr_t)15);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.ST; ++i) {
@@ -666,7 +682,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   // first weight copies run before this kernel's wait. Only the prepared B rows
   // (read in the loop below) need it.
   // sigma_t: max over the token's pairs of p |h| lands in [2^14, 2^15) after scaling
-  if (threadIdx.x < 8 * NT) {
+  if (threadIdx.x < 32) {
     const int t = threadIdx.x;
     float m = 0.f;
     if (t < a.T)
@@ -697,9 +713,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     const int v2 = q / kMxTC, j = q - v2 * kMxTC;
     if (j < vt[v2 * kVt + 1]) {
       const int pair = vt[v2 * kVt + 2 + j];
-      tab[v2 * 8 * NT + pair / a.top_k] = (int16_t)pair;
+      tab[v2 * 8 * NT + (PC ? j : pair / a.top_k)] = (int16_t)pair;
     }
   }
+  if (PC)
+    for (int q = threadIdx.x; q < kMxWarps * R * a.T; q += blockDim.x) ys[q] = 0.f;
   // the ring's generic writes (scratch, table) before the copies that refill it
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   __syncthreads();
@@ -753,7 +771,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   uint32_t par = 0;
   bool ok = true;
   if (nv > 0) {
-    dn_lane<NT>(a, v, g, tab, cur);
+    dn_lane<NT, PC>(a, v, g, c, tab, cur);
     load_h(cur, 0);
   }
   for (int q = 0; q < nstages; ++q) {
@@ -773,10 +791,15 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     if (ks + 1 < nks) {
       load_h(cur, ks + 1);
     } else if (i + 1 < nv) {
-      dn_lane<NT>(a, v + 1 == nv ? 0 : v + 1, g, tab, nxt);
+      dn_lane<NT, PC>(a, v + 1 == nv ? 0 : v + 1, g, c, tab, nxt);
       load_h(nxt, 0);
       newv = true;
     }
+    if (PC && ks == 0)  // pair columns: the accumulators hold one virtual expert at a time
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int i2 = 0; i2 < 4; ++i2) acc[mt][0][i2] = 0.f;
     if (ok) ok = mbar_wait(&full[st], par, a.err, kErrMoeWait);
     if (ok) {
       const uint8_t* sp = gbase + (size_t)st * kStage;
@@ -807,6 +830,17 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         }
       }
     }
+    if (PC && ks == nks - 1) {
+      // the virtual expert is complete: add its columns to their tokens' sums
+      // (this warp's own region; the lanes' (row, token) cells are distinct)
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int i2 = 0; i2 < 4; ++i2) {
+          const int tok = (i2 & 1) ? cur.tk1 : cur.tk0;
+          if (tok >= 0) ys[(warp * R + 16 * mt + g + 8 * (i2 >> 1)) * a.T + tok] += acc[mt][0][i2];
+        }
+    }
     __syncwarp();
     if (lane == 0 && release_is_last(&rel[st], kMxWarps) && q + a.ST < nstages) issue(q + a.ST);
     if (++st == a.ST) {
@@ -822,6 +856,17 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   }
   // every stage is consumed (and every copy landed): the ring holds the warps' partial tiles
   bar_consumers();
+  if (PC) {
+    for (int q = et; q < R * a.T; q += 32 * kMxWarps) {
+      const int row = q / a.T, t = q - row * a.T;
+      if (n0 + row >= H) continue;
+      float sum = 0.f;
+#pragma unroll 4
+      for (int w2 = 0; w2 < kMxWarps; ++w2) sum += ys[(w2 * R + row) * a.T + t];
+      a.y[(size_t)t * H + n0 + row] = sum * pow2f(sig[t]);
+    }
+    return;
+  }
   float4* red = reinterpret_cast<float4*>(gbase);
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt)
@@ -850,6 +895,7 @@ namespace {
 
 struct MxDnPlan {
   int R, MT, NT, ST, BPW, grid;
+  bool PC;  // pair columns
   uint32_t stage_bytes, o_s;
   size_t smem;
 };
@@ -860,14 +906,22 @@ MxDnPlan plan_down(int T, int H, int I, int top_k, int nvmax, int sms) {
   p.MT = std::min(4, std::max(1, (H + 16 * sms - 1) / (16 * sms)));
   p.R = 16 * p.MT;
   p.grid = (H + p.R - 1) / p.R;
-  p.NT = T <= 8 ? 1 : (T <= 16 ? 2 : 4);
-  // more token columns, fewer blocks per warp (registers): 2048 k stages at
-  // NT = 1, 1024 at NT = 2, 512 at NT = 4 (as far as I allows)
-  p.BPW = p.NT == 4 ? 1 : ((p.NT == 1 && I % 2048 == 0) ? 4 : (I % 1024 == 0 ? 2 : 1));
-  p.o_s = 256u * p.R * p.BPW;  // codes: [2 BPW chunks][R rows][128 B], then scales [R][16 BPW]
-  p.stage_bytes = (272u * p.R * p.BPW + 1023u) & ~1023u;
-  const size_t fixed = 1024 + 4 * 8 * p.NT + 4 * (size_t)nvmax + 2 * (size_t)nvmax * 8 * p.NT + 64;
-  p.ST = (int)std::min<size_t>(8, (kMxSmem - fixed) / (p.stage_bytes + 16));
+  // up to 8 tokens: the MMA columns are the tokens; more: the columns are the
+  // pairs of one virtual expert, with per-warp token sums in shared memory
+  p.PC = T > 8;
+  p.NT = 1;
+  const size_t fixed = 1024 + 4 * 32 + 4 * (size_t)nvmax + 2 * (size_t)nvmax * 8 * p.NT + 64 +
+                       (p.PC ? 16 + 4 * (size_t)kMxWarps * p.R * T : 0);
+  // 2048 k stages as far as I allows (the per-stage work of a warp -- the next
+  // B rows, the wait, the release -- is spread over more blocks; measured on
+  // T = 16 and 32: 2048 k with 3 or 2 stages in flight beats 1024 k with 6 or
+  // 4), shorter ones only while fewer than 2 fit
+  for (p.BPW = I % 2048 == 0 ? 4 : (I % 1024 == 0 ? 2 : 1);; p.BPW /= 2) {
+    p.o_s = 256u * p.R * p.BPW;  // codes: [2 BPW chunks][R rows][128 B], then scales [R][16 BPW]
+    p.stage_bytes = (272u * p.R * p.BPW + 1023u) & ~1023u;
+    p.ST = fixed >= kMxSmem ? 0 : (int)std::min<size_t>(8, (kMxSmem - fixed) / (p.stage_bytes + 16));
+    if (p.ST >= 2 || p.BPW == 1) break;
+  }
   p.smem = fixed + (size_t)p.ST * (p.stage_bytes + 16);
   return p;
 }
@@ -880,24 +934,32 @@ size_t gateup_smem(int ST, int nvmax) {
   return 1024 + (size_t)ST * (kGuStage + 16) + kGuRed + 2 * kVt * (size_t)nvmax + 64;
 }
 
-template <int NT, int MT, int BPW>
+template <int MT, int BPW, bool PC>
 cudaError_t launch_down(const CUtensorMap& tm_dq, const CUtensorMap& tm_ds, const MxDnArgs& da, const MxDnPlan& pd,
                         cudaStream_t stream, bool pdl) {
-  cudaError_t e = allow_max_smem(moe_mx_dn_mma_kernel<NT, MT, BPW>);
+  cudaError_t e = allow_max_smem(moe_mx_dn_mma_kernel<1, MT, BPW, PC>);
   if (e != cudaSuccess) return e;
-  return launch_kernel(moe_mx_dn_mma_kernel<NT, MT, BPW>, dim3(pd.grid), dim3(kMxThreads), pd.smem, stream, pdl,
+  return launch_kernel(moe_mx_dn_mma_kernel<1, MT, BPW, PC>, dim3(pd.grid), dim3(kMxThreads), pd.smem, stream, pdl,
                        tm_dq, tm_ds, da);
 }
 
-template <int NT, int BPW>
+template <int BPW, bool PC>
 cudaError_t launch_down_mt(const CUtensorMap& tm_dq, const CUtensorMap& tm_ds, const MxDnArgs& da,
                            const MxDnPlan& pd, cudaStream_t stream, bool pdl) {
   switch (pd.MT) {
-    case 1: return launch_down<NT, 1, BPW>(tm_dq, tm_ds, da, pd, stream, pdl);
-    case 2: return launch_down<NT, 2, BPW>(tm_dq, tm_ds, da, pd, stream, pdl);
-    case 3: return launch_down<NT, 3, BPW>(tm_dq, tm_ds, da, pd, stream, pdl);
-    default: return launch_down<NT, 4, BPW>(tm_dq, tm_ds, da, pd, stream, pdl);
+    case 1: return launch_down<1, BPW, PC>(tm_dq, tm_ds, da, pd, stream, pdl);
+    case 2: return launch_down<2, BPW, PC>(tm_dq, tm_ds, da, pd, stream, pdl);
+    case 3: return launch_down<3, BPW, PC>(tm_dq, tm_ds, da, pd, stream, pdl);
+    default: return launch_down<4, BPW, PC>(tm_dq, tm_ds, da, pd, stream, pdl);
   }
+}
+
+template <bool PC>
+cudaError_t launch_down_bpw(const CUtensorMap& tm_dq, const CUtensorMap& tm_ds, const MxDnArgs& da,
+                            const MxDnPlan& pd, cudaStream_t stream, bool pdl) {
+  return pd.BPW == 4   ? launch_down_mt<4, PC>(tm_dq, tm_ds, da, pd, stream, pdl)
+         : pd.BPW == 2 ? launch_down_mt<2, PC>(tm_dq, tm_ds, da, pd, stream, pdl)
+                       : launch_down_mt<1, PC>(tm_dq, tm_ds, da, pd, stream, pdl);
 }
 
 template <int BPW>
@@ -963,14 +1025,8 @@ cudaError_t launch_moe_mx_mma(const uint16_t* x, const float* logits, const uint
     if (e != cudaSuccess) return e;
   }
   const MxDnArgs da{hh, hmax, wts, idx, y, T, H, I, E, top_k, pd.R, pd.ST, pd.BPW, nvmax, pd.stage_bytes, pd.o_s, err};
-  if (pd.NT == 1)
-    return pd.BPW == 4   ? launch_down_mt<1, 4>(tm_dq, tm_ds, da, pd, stream, pdl)
-           : pd.BPW == 2 ? launch_down_mt<1, 2>(tm_dq, tm_ds, da, pd, stream, pdl)
-                         : launch_down_mt<1, 1>(tm_dq, tm_ds, da, pd, stream, pdl);
-  if (pd.NT == 2)
-    return pd.BPW == 2 ? launch_down_mt<2, 2>(tm_dq, tm_ds, da, pd, stream, pdl)
-                       : launch_down_mt<2, 1>(tm_dq, tm_ds, da, pd, stream, pdl);
-  return launch_down_mt<4, 1>(tm_dq, tm_ds, da, pd, stream, pdl);
+  return pd.PC ? launch_down_bpw<true>(tm_dq, tm_ds, da, pd, stream, pdl)
+               : launch_down_bpw<false>(tm_dq, tm_ds, da, pd, stream, pdl);
 }
 
 }  // namespace qg
