@@ -87,7 +87,7 @@ struct TcGroupPlan {
   void* d_gemvs;    // device descriptors (tensor maps + shapes)
   int* d_cta;       // [grid + 1] first unit of each CTA, then [grid] its projection
   void* d_scratch;  // M <= 16: every projection's B fragments and group table
-  int ngemv, grid, NT, ST, mma, max_groups;
+  int ngemv, grid, NT, ST, mma, mma_nt, max_groups;
   uint32_t stage_bytes;
   size_t smem;
 };

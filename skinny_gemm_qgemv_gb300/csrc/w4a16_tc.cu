@@ -766,6 +766,8 @@ __global__ void __launch_bounds__(256) w4a16_mma_prep_kernel(const MmaPrepArgs a
   pdl_launch_dependents();
 }
 
+// MNT: n tiles of 8 activation rows that carry rows (1: M <= 8, 2: M <= 16)
+template <int MNT>
 __global__ void __launch_bounds__(kMmaThreads, 1)
     w4a16_mma_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scales,
                      const __grid_constant__ CUtensorMap tm_biases, const TcArgs a) {
@@ -903,7 +905,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
               const uint32_t* qb = (s4 >> 1) ? q11 : q10;
               const int p = 2 * (s4 & 1);
 #pragma unroll
-              for (int t = 0; t < 2; ++t)
+              for (int t = 0; t < MNT; ++t)
                 mma_16816(acc[t], qa[p], qb[p], qa[p + 1], qb[p + 1], b[(s4 * 2 + t) * 2], b[(s4 * 2 + t) * 2 + 1]);
             }
             const float s0 = f16_bits_to_f32(lds16(sb + s_off + r0 * 16 + 2 * warp));
@@ -916,7 +918,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             const uint64_t d0 = pair2(__float_as_uint(bb0), __float_as_uint(bb0));
             const uint64_t d1 = pair2(__float_as_uint(bb1), __float_as_uint(bb1));
 #pragma unroll
-            for (int t = 0; t < 2; ++t) {
+            for (int t = 0; t < MNT; ++t) {  // an n tile without rows stays zero
               y2[rb][t][0] = ffma2(c0, pair2(__float_as_uint(acc[t][0]), __float_as_uint(acc[t][1])),
                                    ffma2(d0, sxp[t], y2[rb][t][0]));
               y2[rb][t][1] = ffma2(c1, pair2(__float_as_uint(acc[t][2]), __float_as_uint(acc[t][3])),
@@ -1053,6 +1055,15 @@ int mma_stages() {
   return ST;
 }
 
+template <int MNT>
+cudaError_t launch_mma(dim3 grid, size_t smem, cudaStream_t stream, bool pdl, const CUtensorMap* maps,
+                       const TcArgs& a) {
+  cudaError_t e = allow_max_smem(w4a16_mma_kernel<MNT>);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(w4a16_mma_kernel<MNT>, grid, dim3(kMmaThreads), smem, stream, pdl, maps[0], maps[1], maps[2],
+                       a);
+}
+
 TcPlan tc_plan(int M, int N, int K, int sms) {
   TcPlan p;
   p.NT = M <= 16 ? 16 : 32;
@@ -1145,10 +1156,8 @@ cudaError_t launch_w4a16_tc(const uint32_t* wq, const uint16_t* sc, const uint16
     pa.K = K;
     cudaError_t e = launch_kernel(w4a16_mma_prep_kernel, dim3((K / 64 + 7) / 8), dim3(256), 0, stream, pdl, pa);
     if (e != cudaSuccess) return e;
-    e = allow_max_smem(w4a16_mma_kernel);
-    if (e != cudaSuccess) return e;
-    return launch_kernel(w4a16_mma_kernel, dim3(grid), dim3(kMmaThreads), p.smem, stream, pdl, maps[0], maps[1],
-                         maps[2], a);
+    return M <= 8 ? launch_mma<1>(dim3(grid), p.smem, stream, pdl, maps, a)
+                  : launch_mma<2>(dim3(grid), p.smem, stream, pdl, maps, a);
   }
   if (p.NT == 16) return launch_tc_nt<16>(maps, a, p, grid, stream, pdl);
   return launch_tc_nt<32>(maps, a, p, grid, stream, pdl);
@@ -1174,6 +1183,9 @@ cudaError_t tc_group_plan_build(const TcGroupItem* list, int n, int sms, TcGroup
   TcGroupPlan p{};
   p.NT = list[0].M <= 16 ? 16 : 32;
   p.mma = list[0].M <= 16 ? 1 : 0;
+  p.mma_nt = 1;  // n tiles of 8 rows the MMA kernel computes: the group's largest M
+  for (int i = 0; i < n; ++i)
+    if (list[i].M > 8) p.mma_nt = 2;
   std::vector<TcGemv> g(n);
   long long units = 0;
   size_t scratch = 0;  // mma path: every projection's B fragments and group table
@@ -1290,10 +1302,8 @@ cudaError_t tc_group_launch(const TcGroupPlan& p, uint32_t* err, cudaStream_t st
     cudaError_t e = launch_kernel(w4a16_mma_prep_kernel, dim3((p.max_groups + 7) / 8, p.ngemv), dim3(256), 0,
                                   stream, pdl, pa);
     if (e != cudaSuccess) return e;
-    e = allow_max_smem(w4a16_mma_kernel);
-    if (e != cudaSuccess) return e;
-    return launch_kernel(w4a16_mma_kernel, dim3(p.grid), dim3(kMmaThreads), p.smem, stream, pdl, unused[0],
-                         unused[1], unused[2], a);
+    return p.mma_nt == 1 ? launch_mma<1>(dim3(p.grid), p.smem, stream, pdl, unused, a)
+                         : launch_mma<2>(dim3(p.grid), p.smem, stream, pdl, unused, a);
   }
   if (p.NT == 16) return launch_tc_nt<16>(unused, a, tp, p.grid, stream, pdl);
   return launch_tc_nt<32>(unused, a, tp, p.grid, stream, pdl);
