@@ -492,7 +492,7 @@ CASES = ["gemv_lm_head", "gemv_down", "gemv_q", "skinny16_gate_up", "skinny16_do
          "w8a16_lm_head",
          "w8a8_12288", "hadamard_16x4096", "gemv_group_4layers", "skinny16_group_4layers", "chain_4layers",
          "chain_flat_4layers", "chain_trace", "w8a8_fused_12288", "w8a8_fused_4096",
-         "skinny32_group_4layers"]
+         "skinny32_group_4layers", "skinny8_group_4layers"]
 
 
 def chain_trace_summary(q, dev):
@@ -566,10 +566,10 @@ def run_case(args):
         ch = q.GemvChain(items)
         f = ch.run
         nbytes = sum(w4_bytes(N, K) for (_, N, K, *_r) in mats)
-    elif c in ("skinny16_group_4layers", "skinny32_group_4layers"):
-        # the grouped skinny launch over 4 decoder layers + the lm_head: M = 16
-        # (warp-level MMA kernel) or M = 32 (tcgen05 kernel)
-        Mr = 16 if c.startswith("skinny16") else 32
+    elif c in ("skinny8_group_4layers", "skinny16_group_4layers", "skinny32_group_4layers"):
+        # the grouped skinny launch over 4 decoder layers + the lm_head: M = 8
+        # or 16 (warp-level MMA kernel, one or two n tiles) or M = 32 (tcgen05 kernel)
+        Mr = int(c[6:8].rstrip("_"))
         mats = build_stack(q, dev, Mr, layers=4)
         xs, ys = stack_io(mats, dev, Mr)
         grp = q.SkinnyGroup([(wq, s, b, x, y) for (_, N, K, wq, s, b), x, y in zip(mats, xs, ys)])
@@ -816,7 +816,7 @@ def main():
             dq, ds = synth.mxfp4_weights(E * H, I, 3, 4, dev)
         moe_w = [t.reshape(E, r, -1) for t, r in ((gq, I), (gs, I), (uq, I), (us, I), (dq, H), (ds, H))]
         torch.cuda.synchronize()
-        for T in (1, 16):
+        for T in (1, 16, 32):  # the two configured batches, then 32 (the largest of the same kernels)
             r = bench_moe(q, dev, stream, T, moe_w)
             r["frac"] = r["GB_per_s"] / hbm_peak
             extras[f"moe_mxfp4_T{T}"] = r
