@@ -659,7 +659,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   constexpr uint32_t kSRow = 16u * BPW;
   // shared layout: stages (the cross-warp sums reuse them at the end) | sigma per token |
   //                full barriers | release counters | first weight rows | pair table |
-  //                (pair columns) per-warp token sums [warp][R][T]
+  //                (pair columns) per-warp token sums [warp][T][R + 8]
   int* sig = reinterpret_cast<int*>(gbase + (size_t)a.ST * kStage);
   uint64_t* full = reinterpret_cast<uint64_t*>(sig + 32);
   uint32_t* rel = reinterpret_cast<uint32_t*>(full + a.ST);
@@ -717,7 +717,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     }
   }
   if (PC)
-    for (int q = threadIdx.x; q < kMxWarps * R * a.T; q += blockDim.x) ys[q] = 0.f;
+    for (int q = threadIdx.x; q < kMxWarps * (R + 8) * a.T; q += blockDim.x) ys[q] = 0.f;
   // the ring's generic writes (scratch, table) before the copies that refill it
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   __syncthreads();
@@ -832,13 +832,15 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     }
     if (PC && ks == nks - 1) {
       // the virtual expert is complete: add its columns to their tokens' sums
-      // (this warp's own region; the lanes' (row, token) cells are distinct)
+      // (this warp's own region; the lanes' (row, token) cells are distinct;
+      // a token's rows are contiguous and tokens R + 8 words apart, so the 8
+      // rows of one column fall in 8 consecutive banks)
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
         for (int i2 = 0; i2 < 4; ++i2) {
           const int tok = (i2 & 1) ? cur.tk1 : cur.tk0;
-          if (tok >= 0) ys[(warp * R + 16 * mt + g + 8 * (i2 >> 1)) * a.T + tok] += acc[mt][0][i2];
+          if (tok >= 0) ys[(warp * a.T + tok) * (R + 8) + 16 * mt + g + 8 * (i2 >> 1)] += acc[mt][0][i2];
         }
     }
     __syncwarp();
@@ -858,11 +860,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   bar_consumers();
   if (PC) {
     for (int q = et; q < R * a.T; q += 32 * kMxWarps) {
-      const int row = q / a.T, t = q - row * a.T;
+      const int t = q / R, row = q - t * R;
       if (n0 + row >= H) continue;
       float sum = 0.f;
 #pragma unroll 4
-      for (int w2 = 0; w2 < kMxWarps; ++w2) sum += ys[(w2 * R + row) * a.T + t];
+      for (int w2 = 0; w2 < kMxWarps; ++w2) sum += ys[(w2 * a.T + t) * (R + 8) + row];
       a.y[(size_t)t * H + n0 + row] = sum * pow2f(sig[t]);
     }
     return;
@@ -911,7 +913,7 @@ MxDnPlan plan_down(int T, int H, int I, int top_k, int nvmax, int sms) {
   p.PC = T > 8;
   p.NT = 1;
   const size_t fixed = 1024 + 4 * 32 + 4 * (size_t)nvmax + 2 * (size_t)nvmax * 8 * p.NT + 64 +
-                       (p.PC ? 16 + 4 * (size_t)kMxWarps * p.R * T : 0);
+                       (p.PC ? 16 + 4 * (size_t)kMxWarps * (p.R + 8) * T : 0);
   // 2048 k stages as far as I allows (the per-stage work of a warp -- the next
   // B rows, the wait, the release -- is spread over more blocks; measured on
   // T = 16 and 32: 2048 k with 3 or 2 stages in flight beats 1024 k with 6 or
