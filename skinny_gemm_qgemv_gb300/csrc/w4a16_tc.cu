@@ -656,6 +656,15 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// d = A B + c, with the accumulator input in registers of its own
+__device__ __forceinline__ void mma_16816_c(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                            uint32_t b0, uint32_t b1, const float (&c)[4]) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%10, %11, %12, %13};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
+}
+
 __device__ __forceinline__ uint32_t f16x2_of(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -875,6 +884,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           }
           const uint64_t sxp[2] = {pair2(__float_as_uint(x0.x), __float_as_uint(x0.y)),
                                    pair2(__float_as_uint(x1.x), __float_as_uint(x1.y))};
+          // every row block's accumulators start at minus the group's offsets
+          const float negc[2][4] = {{-o0.x, -o0.y, -o0.x, -o0.y}, {-o1.x, -o1.y, -o1.x, -o1.y}};
           // codes of group `warp`: chunk warp / 4, 32-byte segment warp % 4 of each 128-byte row;
           // words 2c, 2c + 1 are 8 bytes of 16-byte unit 2 (warp % 4) + c / 2
           const uint32_t cu = 2u * (uint32_t)(warp & 3) + ((uint32_t)c >> 1);
@@ -892,21 +903,17 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             nib8_to_f16x2_offset(w1.y, q11);
             float acc[2][4];
 #pragma unroll
-            for (int t = 0; t < 2; ++t) {
-              const float2 o = t == 0 ? o0 : o1;
-              acc[t][0] = -o.x;
-              acc[t][1] = -o.y;
-              acc[t][2] = -o.x;
-              acc[t][3] = -o.y;
-            }
-#pragma unroll
             for (int s4 = 0; s4 < 4; ++s4) {
               const uint32_t* qa = (s4 >> 1) ? q01 : q00;
               const uint32_t* qb = (s4 >> 1) ? q11 : q10;
               const int p = 2 * (s4 & 1);
 #pragma unroll
-              for (int t = 0; t < MNT; ++t)
-                mma_16816(acc[t], qa[p], qb[p], qa[p + 1], qb[p + 1], b[(s4 * 2 + t) * 2], b[(s4 * 2 + t) * 2 + 1]);
+              for (int t = 0; t < MNT; ++t) {
+                if (s4 == 0)
+                  mma_16816_c(acc[t], qa[p], qb[p], qa[p + 1], qb[p + 1], b[t * 2], b[t * 2 + 1], negc[t]);
+                else
+                  mma_16816(acc[t], qa[p], qb[p], qa[p + 1], qb[p + 1], b[(s4 * 2 + t) * 2], b[(s4 * 2 + t) * 2 + 1]);
+              }
             }
             const float s0 = f16_bits_to_f32(lds16(sb + s_off + r0 * 16 + 2 * warp));
             const float s1 = f16_bits_to_f32(lds16(sb + s_off + (r0 + 8) * 16 + 2 * warp));
