@@ -892,12 +892,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           const uint32_t cbase = sb + c_off + (uint32_t)(warp >> 2) * 16384 + 8u * (uint32_t)(c & 1);
 #pragma unroll
           for (int rb = 0; rb < 8; ++rb) {
-            // MMA row g is weight row pg = 2 (g % 4) + g / 4 of each half of the
-            // block: the 16 lanes of one shared-load phase (g = 0..3 or 4..7)
-            // then read rows whose swizzled 32-byte segments fall in different
-            // banks (with row g they pair up, rows g and g ^ 1 on the same two
-            // 16-byte units). Rows r0 and r0 + 8 share the swizzle (r & 7 = pg).
-            const int pg = 2 * (g & 3) + (g >> 2);
+            // One n tile: MMA row g is weight row pg = 2 (g % 4) + g / 4 of each
+            // half of the block, so the 16 lanes of one shared-load phase
+            // (g = 0..3 or 4..7) read rows whose swizzled 32-byte segments fall
+            // in different banks (with row g, rows g and g ^ 1 share two 16-byte
+            // units); measured slower with two n tiles, which keep row g. Rows
+            // r0 and r0 + 8 share the swizzle (r & 7 = pg).
+            const int pg = MNT == 1 ? 2 * (g & 3) + (g >> 2) : g;
             const int r0 = 16 * rb + pg;
             const uint32_t sw = (cu ^ (uint32_t)pg) << 4;
             const uint2 w0 = lds64(cbase + r0 * 128 + sw);
@@ -984,7 +985,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           const int uu = u0 + h, rb = uu >> 1, t = uu & 1;
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int row = 16 * rb + 2 * (gg & 3) + (gg >> 2) + 8 * (e >> 1);
+            const int row = 16 * rb + (MNT == 1 ? 2 * (gg & 3) + (gg >> 2) : gg) + 8 * (e >> 1);
             const int m = 8 * t + 2 * cc + (e & 1);
             if (whole) {
               if (m < w.M && w.n0 + row < w.N) w.y[(size_t)m * w.N + w.n0 + row] = tot[h][e];
