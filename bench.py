@@ -342,6 +342,25 @@ def bench_w8a16(q, dev, stream, hbm_peak):
             "algorithmic_bytes": nbytes}
 
 
+def bench_affine(q, dev, stream, hbm_peak):
+    """qgemm_affine at M = 1 on the lm_head shape (151936 x 4096, > L2 at every
+    width): codes at 2, 3, 4, 5, 6 and 8 bits with groups of 64, and 4 bits with
+    groups of 32 and 128 (the chunked kernel; the 4-bit g64 case has the W4A16
+    fast path)."""
+    N, K = 151936, 4096
+    x = synth.bf16_normal((K,), 3, 2, dev)
+    y = torch.empty(N, device=dev)
+    out = {}
+    for bits, group in ((2, 64), (3, 64), (4, 64), (5, 64), (6, 64), (8, 64), (4, 32), (4, 128)):
+        wq, s, b = synth.affine_weights(N, K, bits, 5, bits, device=dev, group=group)
+        t, _ = time_graph(lambda: q.qgemm_affine(wq, bits, s, b, x, y=y, stream=stream), 10, stream)
+        nbytes = N * K * bits // 8 + 4 * N * (K // group) + 2 * K + 4 * N
+        out[f"b{bits}_g{group}"] = {"us_per_call": t * 1e6, "GB_per_s": nbytes / t / 1e9,
+                                   "frac": nbytes / t / 1e9 / hbm_peak, "algorithmic_bytes": nbytes}
+        del wq, s, b
+    return out
+
+
 def bench_skinny_stacks(q, mats, dev, stream, hbm_peak):
     """The layer stack at M in {2, 4, 8, 16, 32} activation rows (continuous-batch
     rows or speculative-tree tokens): one grouped skinny launch per step
@@ -808,6 +827,7 @@ def main():
         extras["m1_stack_tokens_per_s"] = 1.0 / t_step
         extras["single_gemv_1024"] = bench_single_gemv(q, dev, stream, l2)
         extras["w8a16_lm_head_151936x4096"] = bench_w8a16(q, dev, stream, hbm_peak)
+        extras["affine_m1_151936x4096"] = bench_affine(q, dev, stream, hbm_peak)
         torch.cuda.empty_cache()
         E, H, I = 384, 7168, 2048
         with torch.cuda.stream(stream):

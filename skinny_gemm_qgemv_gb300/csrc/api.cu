@@ -148,8 +148,10 @@ static qg_status run_w4(const uint32_t* wq, const uint16_t* s, const uint16_t* b
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (group != 64) {
-    // groups of 32 or 128: the generic kernel (the fast paths fold per 64-code group)
-    e = qg::launch_w4a16_generic(wq, s, b, x, y, M, N, K, group, st, g_pdl);
+    // groups of 32 or 128 (the W4A16 fast paths fold per 64-code group): the
+    // chunked affine kernel up to 4 rows, else the generic kernel
+    e = qg::affine_fast_ok(4, M, K, group) ? qg::launch_affine_fast(wq, 4, s, b, x, y, M, N, K, group, st, g_pdl)
+                                           : qg::launch_w4a16_generic(wq, s, b, x, y, M, N, K, group, st, g_pdl);
   } else if (qg::gemv_fast_path_ok(M, N, K)) {
     uint32_t* err = err_word();
     if (!err) return QG_ERR_CUDA;
@@ -158,6 +160,8 @@ static qg_status run_w4(const uint32_t* wq, const uint16_t* s, const uint16_t* b
     uint32_t* err = err_word();
     if (!err) return QG_ERR_CUDA;
     e = qg::launch_w4a16_tc(wq, s, b, x, y, M, N, K, ws, ws_bytes, err, st, g_pdl);
+  } else if (qg::affine_fast_ok(4, M, K, 64)) {
+    e = qg::launch_affine_fast(wq, 4, s, b, x, y, M, N, K, 64, st, g_pdl);
   } else {
     e = qg::launch_w4a16_generic(wq, s, b, x, y, M, N, K, 64, st, g_pdl);
   }
@@ -183,8 +187,12 @@ qg_status qgemm_affine(const uint32_t* wq, int bits, const uint16_t* scales_f16,
   if ((long long)N * (K / 32) * bits >= (1LL << 40)) return QG_ERR_INVALID_ARG;
   if (!aligned16(wq) || !aligned16(scales_f16) || !aligned16(biases_f16) || !aligned16(x_bf16) || !aligned16(y))
     return QG_ERR_MISALIGNED;
-  return from_cuda(qg::launch_affine_generic(wq, bits, scales_f16, biases_f16, x_bf16, y, M, N, K, group_size,
-                                             static_cast<cudaStream_t>(stream), g_pdl));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (qg::affine_fast_ok(bits, M, K, group_size))
+    return from_cuda(qg::launch_affine_fast(wq, bits, scales_f16, biases_f16, x_bf16, y, M, N, K, group_size, st,
+                                            g_pdl));
+  return from_cuda(qg::launch_affine_generic(wq, bits, scales_f16, biases_f16, x_bf16, y, M, N, K, group_size, st,
+                                             g_pdl));
 }
 
 qg_status qgemv_w8a16(const int8_t* wq, const float* scales, const uint16_t* x_bf16, float* y, int N, int K,

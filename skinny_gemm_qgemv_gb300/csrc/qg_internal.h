@@ -207,7 +207,13 @@ bool tmap_3d(CUtensorMap* tm, CUtensorMapDataType dt, const void* ptr, uint64_t 
              uint64_t chunks, uint64_t row_bytes, uint64_t chunk_bytes, uint32_t box_inner, uint32_t box_rows,
              uint32_t box_chunks);
 
-// affine codes at 2, 3, 4, 5, 6 or 8 bits, groups 32/64/128, M <= 32 (affine_gemv.cu)
+// affine codes at 2, 3, 4, 5, 6 or 8 bits, groups 32/64/128 (affine_gemv.cu):
+// 1 <= M <= 4 on 32-code chunks (affine_fast_ok says which shapes), and the
+// one-code-per-lane kernel for any M <= 32
+bool affine_fast_ok(int bits, int M, int K, int group);
+cudaError_t launch_affine_fast(const uint32_t* wq, int bits, const uint16_t* sc, const uint16_t* bi,
+                               const uint16_t* x, float* y, int M, int N, int K, int group, cudaStream_t stream,
+                               bool pdl);
 cudaError_t launch_affine_generic(const uint32_t* wq, int bits, const uint16_t* sc, const uint16_t* bi,
                                   const uint16_t* x, float* y, int M, int N, int K, int group, cudaStream_t stream,
                                   bool pdl);

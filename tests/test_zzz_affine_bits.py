@@ -27,7 +27,10 @@ def q():
 
 
 @pytest.mark.parametrize("bits", [2, 3, 4, 5, 6, 8])
-@pytest.mark.parametrize("M,N,K,group", [(1, 300, 1024, 64), (4, 77, 2048, 128), (7, 50, 512, 32)])
+# M <= 4: the chunked kernel (M = 2 and 3 below its 4-row instance; K = 96: fewer
+# chunks than lanes); M = 7: the one-code-per-lane kernel
+@pytest.mark.parametrize("M,N,K,group", [(1, 300, 1024, 64), (4, 77, 2048, 128), (7, 50, 512, 32),
+                                         (2, 130, 96, 32), (3, 33, 4096, 64)])
 def test_affine_bits_vs_oracle(q, bits, M, N, K, group):
     wq, s, b = synth.affine_weights(N, K, bits, seed=700 + M, slot=bits, group=group)
     x = synth.bf16_normal((M, K), seed=700 + M, slot=1)
