@@ -14,12 +14,15 @@
 // dequantizes in fp32 and accumulates for every activation row. The 4-bit g64
 // case has its own fast kernels (qgemv_w4a16, qgemm_w4a16_skinny).
 //
-// Up to 4 activation rows take affine_fast_kernel instead: lane l of a warp
+// Up to 4 activation rows take the chunked kernels instead: lane l of a warp
 // takes whole 32-code chunks (BITS consecutive words: exactly 32 codes, so a
 // chunk never shares a word with the next one, and a warp reads 32 BITS words
-// contiguously), extracts the codes with constant shifts (a funnel shift where
-// a code spans two words), and folds the affine group per chunk as
-// s * sum(q x) + b * sum(x), the chunk sums of x computed once per CTA.
+// contiguously), four at a time with their loads issued first, and folds the
+// affine group per chunk as s * sum(q x) + b * sum(x). At 2, 4 and 8 bits
+// (affine_f16_kernel) codes become fp16 1024 + q 2^(j BITS) two at a time and
+// meet fp16 activations prepared once per CTA; at 3, 5 and 6 bits
+// (affine_fast_kernel) each code is extracted with constant shifts (a funnel
+// shift where it spans two words) and converted to fp32.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
