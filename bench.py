@@ -511,7 +511,7 @@ CASES = ["gemv_lm_head", "gemv_down", "gemv_q", "skinny16_gate_up", "skinny16_do
          "w8a16_lm_head",
          "w8a8_12288", "hadamard_16x4096", "gemv_group_4layers", "skinny16_group_4layers", "chain_4layers",
          "chain_flat_4layers", "chain_trace", "w8a8_fused_12288", "w8a8_fused_4096",
-         "skinny32_group_4layers", "skinny8_group_4layers"]
+         "skinny32_group_4layers", "skinny8_group_4layers", "affine_b4_lm_head", "affine_b6_lm_head"]
 
 
 def chain_trace_summary(q, dev):
@@ -616,6 +616,15 @@ def run_case(args):
         lg = synth.router_logits(T, E, 3, 1, dev)
         f = lambda: q.moe_mxfp4_expert_forward(x, lg, *w, top_k=k)  # noqa: E731
         nbytes = None
+    elif c.startswith("affine_b"):
+        # qgemm_affine at M = 1 on the lm_head shape, 4 or 6-bit codes, groups of 64
+        bits = int(c[8])
+        N, K = 151936, 4096
+        wq, s, b = synth.affine_weights(N, K, bits, 5, bits, device=dev, group=64)
+        x = synth.bf16_normal((K,), 3, 2, dev)
+        y = torch.empty(N, device=dev)
+        f = lambda: q.qgemm_affine(wq, bits, s, b, x, y=y)  # noqa: E731
+        nbytes = N * K * bits // 8 + 4 * N * (K // 64) + 2 * K + 4 * N
     elif c == "w8a16_lm_head":
         N, K = 151936, 4096
         wq, s = synth.w8_row_weights(N, K, 3, 1, dev)

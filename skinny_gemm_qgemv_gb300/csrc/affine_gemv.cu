@@ -128,7 +128,8 @@ struct ChunkDot<BITS, MM, 32> {
 
 }  // namespace
 
-// One warp per output row, 8 rows per CTA; MM >= M activation rows.
+// One warp per output row at a time, 8 rows per CTA and pass; MM >= M
+// activation rows.
 template <int BITS, int MM>
 __global__ void __launch_bounds__(256) affine_fast_kernel(const uint32_t* __restrict__ wq,
                                                           const uint16_t* __restrict__ scales,
@@ -153,56 +154,56 @@ __global__ void __launch_bounds__(256) affine_fast_kernel(const uint32_t* __rest
   }
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n = blockIdx.x * 8 + warp;
-  if (n >= N) return;
-  const uint32_t* row = wq + (size_t)n * nch * BITS;
   const int groups = K >> lg_group, gpc = lg_group - 5;  // chunks per group: 2^gpc
-  float acc[MM];
+  for (int n = blockIdx.x * 8 + warp; n < N; n += gridDim.x * 8) {
+    const uint32_t* row = wq + (size_t)n * nch * BITS;
+    float acc[MM];
 #pragma unroll
-  for (int m = 0; m < MM; ++m) acc[m] = 0.f;
-  // kU chunks a lane at a time, their weight words and factors loaded first
-  constexpr int kU = 4;
-  for (int c0 = lane; c0 < nch; c0 += 32 * kU) {
-    uint32_t wv[kU][BITS + 1];
-    uint16_t sv[kU], bv[kU];
+    for (int m = 0; m < MM; ++m) acc[m] = 0.f;
+    // kU chunks a lane at a time, their weight words and factors loaded first
+    constexpr int kU = 4;
+    for (int c0 = lane; c0 < nch; c0 += 32 * kU) {
+      uint32_t wv[kU][BITS + 1];
+      uint16_t sv[kU], bv[kU];
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int c = c0 + 32 * u;
-      if (c < nch) {
-        load_chunk<BITS>(row + (size_t)BITS * c, wv[u]);
-        sv[u] = __ldg(scales + (size_t)n * groups + (c >> gpc));
-        bv[u] = __ldg(biases + (size_t)n * groups + (c >> gpc));
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int c = c0 + 32 * u;
-      if (c >= nch) break;
-      uint32_t xv[MM][16];
-#pragma unroll
-      for (int m = 0; m < MM; ++m) {
-        const uint4* xp = reinterpret_cast<const uint4*>(x + (size_t)(m < M ? m : 0) * K + 32 * c);
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const uint4 q4 = __ldg(xp + v);
-          xv[m][4 * v] = q4.x, xv[m][4 * v + 1] = q4.y, xv[m][4 * v + 2] = q4.z, xv[m][4 * v + 3] = q4.w;
+      for (int u = 0; u < kU; ++u) {
+        const int c = c0 + 32 * u;
+        if (c < nch) {
+          load_chunk<BITS>(row + (size_t)BITS * c, wv[u]);
+          sv[u] = __ldg(scales + (size_t)n * groups + (c >> gpc));
+          bv[u] = __ldg(biases + (size_t)n * groups + (c >> gpc));
         }
       }
-      float dot[MM];
 #pragma unroll
-      for (int m = 0; m < MM; ++m) dot[m] = 0.f;
-      ChunkDot<BITS, MM, 0>::run(wv[u], xv, dot);
-      const float sc = f16_bits_to_f32(sv[u]), bi = f16_bits_to_f32(bv[u]);
+      for (int u = 0; u < kU; ++u) {
+        const int c = c0 + 32 * u;
+        if (c >= nch) break;
+        uint32_t xv[MM][16];
 #pragma unroll
-      for (int m = 0; m < MM; ++m)
-        if (m < M) acc[m] = fmaf(sc, dot[m], fmaf(bi, sxs[m * nch + c], acc[m]));
+        for (int m = 0; m < MM; ++m) {
+          const uint4* xp = reinterpret_cast<const uint4*>(x + (size_t)(m < M ? m : 0) * K + 32 * c);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const uint4 q4 = __ldg(xp + v);
+            xv[m][4 * v] = q4.x, xv[m][4 * v + 1] = q4.y, xv[m][4 * v + 2] = q4.z, xv[m][4 * v + 3] = q4.w;
+          }
+        }
+        float dot[MM];
+#pragma unroll
+        for (int m = 0; m < MM; ++m) dot[m] = 0.f;
+        ChunkDot<BITS, MM, 0>::run(wv[u], xv, dot);
+        const float sc = f16_bits_to_f32(sv[u]), bi = f16_bits_to_f32(bv[u]);
+#pragma unroll
+        for (int m = 0; m < MM; ++m)
+          if (m < M) acc[m] = fmaf(sc, dot[m], fmaf(bi, sxs[m * nch + c], acc[m]));
+      }
     }
-  }
 #pragma unroll
-  for (int m = 0; m < MM; ++m) {
-    if (m < M) {
-      const float t = warp_sum(acc[m]);
-      if (lane == 0) y[(size_t)m * N + n] = t;
+    for (int m = 0; m < MM; ++m) {
+      if (m < M) {
+        const float t = warp_sum(acc[m]);
+        if (lane == 0) y[(size_t)m * N + n] = t;
+      }
     }
   }
 }
@@ -366,16 +367,17 @@ size_t affine_fast_smem(int bits, int M, int K) {
 template <int BITS>
 cudaError_t launch_affine_fast_bits(const uint32_t* wq, const uint16_t* sc, const uint16_t* bi, const uint16_t* x,
                                     float* y, int M, int N, int K, int lg, cudaStream_t stream, bool pdl) {
+  // persistent rows (at most 8 CTAs per SM): the activations are prepared
+  // once per CTA
   const dim3 block(256);
   const size_t smem = affine_fast_smem(BITS, M, K);
   if constexpr (BITS == 2 || BITS == 4 || BITS == 8) {
-    // persistent rows: the activations are prepared once per CTA
     const dim3 grid((unsigned)std::min<long long>((N + 7) / 8, 8LL * device_sm_count()));
     if (M <= 1)
       return launch_kernel(affine_f16_kernel<BITS, 1>, grid, block, smem, stream, pdl, wq, sc, bi, x, y, M, N, K, lg);
     return launch_kernel(affine_f16_kernel<BITS, 4>, grid, block, smem, stream, pdl, wq, sc, bi, x, y, M, N, K, lg);
   } else {
-    const dim3 grid((N + 7) / 8);
+    const dim3 grid((unsigned)std::min<long long>((N + 7) / 8, 8LL * device_sm_count()));
     if (M <= 1)
       return launch_kernel(affine_fast_kernel<BITS, 1>, grid, block, smem, stream, pdl, wq, sc, bi, x, y, M, N, K,
                            lg);
