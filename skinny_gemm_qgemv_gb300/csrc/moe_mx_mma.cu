@@ -7,14 +7,15 @@
 // the multiply. The layer is g = Wg[e] x, u = Wu[e] x, h = silu(g) u,
 // y = sum_j p_j (Wd[e_j] h_j).
 //
-// Three launches:
-//  * route (one CTA): per token one warp finds the exact top-k by a radix
-//    select on order-preserving 32-bit keys of the logits (ties to the lower
-//    expert index) while the other warps take the activations' max |x|; then
-//    x * 2^-sigma in fp16 (sigma per token, an exact power of two that puts
-//    max |x| in [2^14, 2^15)), the per-expert grouping and the "virtual
-//    experts": runs of at most kMxTC = 8 pairs (token, slot) of one expert,
-//    the N = 8 columns of one MMA.
+// Four launches:
+//  * route (one CTA of 1024 threads per token): the exact top-k by a radix
+//    select on order-preserving 32-bit keys of the logits with block-wide
+//    counts (ties to the lower expert index), softmax weights, and the token's
+//    x * 2^-sigma in fp16 (sigma an exact power of two that puts max |x| in
+//    [2^14, 2^15)). The per-expert grouping into "virtual experts" (runs of at
+//    most kMxTC = 8 pairs (token, slot) of one expert, the N = 8 columns of one
+//    MMA) is built from the routing table by every CTA of the next kernels
+//    (mx_group), so no CTA waits for another.
 //  * gate/up: persistent, 16 warps; a tile is (virtual expert, 32 rows of I)
 //    with both matrices, CTAs take contiguous tile ranges. A stage is 1024 k
 //    (512 if H is not a multiple of 1024) of the tile's 32 gate and 32 up rows:
@@ -29,14 +30,15 @@
 //    of a tile the warps' partial sums are added in warp order through shared
 //    memory by one half of the warps (alternating per tile) and h = silu(g) u
 //    is written in fp32 with the pair's max |h|.
+//  * B rows of the down product (moe_mx_hprep_kernel): p h 2^-sigma_t in fp16
+//    once per pair (sigma_t per token from max_j p_j max|h_j|), and a zero row.
 //  * down: one CTA of 16 warps per range of R = 16 * MT rows of H, over every
-//    virtual expert, stages of 2048 k (T <= 8) or 1024 k of its R rows; the MMA
-//    columns are the batch's tokens, so one accumulator per (row, token)
-//    collects all of a token's experts. B is p * h * 2^-sigma_t in fp16
-//    (sigma_t per token from max_j p_j max|h_j|), converted from fp32 h (loaded
-//    from L2 one stage ahead) by the warp that owns the block; n tiles with none
-//    of their tokens in a virtual expert are skipped. One cross-warp sum at the
-//    end, then y = acc * 2^sigma_t.
+//    virtual expert, 2048-k stages of its R rows as far as I allows. Up to 8
+//    tokens the MMA columns are the batch's tokens, so one accumulator per
+//    (row, token) collects all of a token's experts and one cross-warp sum
+//    ends the kernel; with more tokens the columns are the pairs of the
+//    current virtual expert (one n tile) and each virtual expert's columns are
+//    added into per-warp token sums in shared memory. y = sum * 2^sigma_t.
 // E2M1 codes go through the hardware cvt.rn.f16x2.e2m1x2 (exact); products are
 // f16 x f16 with fp32 accumulation. Lane (g, c) of an MMA takes the 4 code
 // bytes 4c..4c+3 of a block (codes 8c..8c+7): bytes 0, 1 are the k slots
