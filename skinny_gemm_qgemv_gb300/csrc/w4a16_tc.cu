@@ -640,6 +640,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 //  * Per group: y += s * 2^sigma * acc + b * sum x, in paired fp32 FMAs; at the
 //    end of a 128-row tile the eight warps' partial sums are added in warp
 //    order through shared memory (deterministic).
+//  * Up to 8 activation rows the kernel computes one 8-column n tile (MNT = 1:
+//    half the MMAs and folds of MNT = 2), and MMA row g reads weight row
+//    2 (g % 4) + g / 4 of each 8-row half, which spreads the 16 lanes of one
+//    shared-load phase over distinct banks.
 // ---------------------------------------------------------------------------
 constexpr int kMmaWarps = 8;                           // consumer warps = 64-k groups per stage
 constexpr int kMmaThreads = 32 * (kMmaWarps + 1);      // + 1 producer warp
