@@ -96,8 +96,8 @@ QG_API int qg_version(void);
  *   y          fp32 [N] (output): y[n] = sum_k (s * q[n][k] + b) * x[k].
  *   group_size 32, 64 or 128 (other values: QG_ERR_INVALID_ARG). 64 runs on the
  *              fast kernels; 32 and 128 (the other group sizes of the affine
- *              format, "MLX Runner ...") run on a generic one-warp-per-row
- *              kernel: correct, not tuned.
+ *              format, "MLX Runner ...") run on the chunked kernel of
+ *              qgemm_affine (one warp per row, 32-code chunks per lane).
  *   K          multiple of group_size; N >= 1.
  *   workspace  may be NULL when ws_bytes == 0; qg_gemv_workspace_size()
  *              gives the size needed (currently 0 for every shape).
@@ -525,6 +525,26 @@ QG_API qg_status gemm_w8a8_hadamard(const uint16_t *x_bf16, const uint32_t *sign
                                     const float *sw, float *y, int M, int N, int K, void *workspace,
                                     size_t ws_bytes, void *stream);
 QG_API size_t qg_w8a8_hadamard_workspace_size(int M, int K);
+
+/*
+ * qg_workspace_size -- the single workspace query of the boundary: device
+ * bytes the operation `op` needs for the given shape, group size 64 where
+ * the operation has one (M, N, K for the W4A16 and W8A8 products; T, E,
+ * top_k with N = H and K = I for the MoE; M, K for the fused Hadamard W8A8
+ * product). Arguments an operation does not use are ignored. 0 for an
+ * operation that needs no workspace, an unknown op or a shape the operation
+ * refuses. The per-operation queries above give the same values.
+ */
+typedef enum {
+  QG_OP_GEMV_W4A16 = 0,     /* qgemv_w4a16 */
+  QG_OP_SKINNY_W4A16 = 1,   /* qgemm_w4a16_skinny */
+  QG_OP_MOE_MXFP4 = 2,      /* moe_mxfp4_expert_forward */
+  QG_OP_HADAMARD_I8 = 3,    /* hadamard32_quant_i8 (none) */
+  QG_OP_W8A8_I32 = 4,       /* gemm_w8a8_i32 (none) */
+  QG_OP_W8A8_HADAMARD = 5   /* gemm_w8a8_hadamard */
+} qg_op;
+
+QG_API size_t qg_workspace_size(int op, int M, int N, int K, int T, int E, int top_k);
 
 /*
  * qg_set_pdl -- process-wide launch mode. With enable != 0 every kernel is

@@ -35,8 +35,10 @@ EXPORTS = [
     "qgemv_w4a16_chain_create", "qgemv_w4a16_chain_run", "qgemv_w4a16_chain_destroy", "qgemv_w4a16_chain_bytes",
     "qg_last_cuda_error", "qg_last_cuda_error_string", "qg_selftest_wait_timeout",
     "qgemv_w4a16_chain_trace_enable", "qgemv_w4a16_chain_trace_read", "qgemv_w4a16_chain_trace_shape",
-    "gemm_w8a8_hadamard", "qg_w8a8_hadamard_workspace_size",
+    "gemm_w8a8_hadamard", "qg_w8a8_hadamard_workspace_size", "qg_workspace_size",
 ]
+
+OP_GEMV_W4A16, OP_SKINNY_W4A16, OP_MOE_MXFP4, OP_HADAMARD_I8, OP_W8A8_I32, OP_W8A8_HADAMARD = range(6)
 
 X_BF16, X_COPY, X_SWIGLU = 0, 1, 2
 
@@ -97,6 +99,8 @@ def lib() -> ctypes.CDLL:
         L.qg_moe_workspace_size.argtypes = [I, I, I, I, I]
         L.qg_moe_workspace_h_offset.restype = Z
         L.qg_moe_workspace_h_offset.argtypes = [I, I, I, I, I]
+        L.qg_workspace_size.restype = Z
+        L.qg_workspace_size.argtypes = [I, I, I, I, I, I, I]
         L.hadamard32_quant_i8.restype = I
         L.hadamard32_quant_i8.argtypes = [P, P, P, P, I, I, P]
         L.gemm_w8a8_i32.restype = I
@@ -405,6 +409,12 @@ class SkinnyGroup:
 
 def moe_workspace_size(T, H, I, E, top_k):
     return lib().qg_moe_workspace_size(T, H, I, E, top_k)
+
+
+def workspace_size(op, M=0, N=0, K=0, T=0, E=0, top_k=0):
+    """Device bytes operation `op` (one of the OP_* constants) needs; the
+    single query of the boundary (group size 64 where it applies)."""
+    return lib().qg_workspace_size(op, M, N, K, T, E, top_k)
 
 
 def moe_workspace_h_offset(T, H, I, E, top_k):

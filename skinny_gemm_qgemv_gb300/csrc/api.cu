@@ -375,6 +375,16 @@ size_t qg_moe_workspace_size(int T, int H, int I, int E, int top_k) {
   return qg::moe_layout(T, H, I, E, top_k).total;
 }
 
+size_t qg_workspace_size(int op, int M, int N, int K, int T, int E, int top_k) {
+  switch (op) {
+    case QG_OP_GEMV_W4A16: return qg_gemv_workspace_size(N, K, 64);
+    case QG_OP_SKINNY_W4A16: return qg_skinny_workspace_size(M, N, K, 64);
+    case QG_OP_MOE_MXFP4: return qg_moe_workspace_size(T, N, K, E, top_k);
+    case QG_OP_W8A8_HADAMARD: return qg_w8a8_hadamard_workspace_size(M, K);
+    default: return 0;  // the Hadamard quantizer and the int32 W8A8 product need none
+  }
+}
+
 size_t qg_moe_workspace_h_offset(int T, int H, int I, int E, int top_k) {
   if (T < 1 || H < 1 || I < 1 || E < 1 || top_k < 1) return 0;
   return qg::moe_layout(T, H, I, E, top_k).h;

@@ -50,6 +50,20 @@ B = 0x20010   # because every call below fails validation first
 P = ctypes.c_void_p
 
 
+def test_single_workspace_query(L):
+    # the one query of the boundary gives what the per-operation queries give
+    assert L.qg_workspace_size(q.OP_GEMV_W4A16, 1, 4096, 4096, 0, 0, 0) == L.qg_gemv_workspace_size(4096, 4096, 64)
+    for M, N, K in ((16, 129, 12288), (32, 4096, 4096), (3, 64, 512)):
+        assert L.qg_workspace_size(q.OP_SKINNY_W4A16, M, N, K, 0, 0, 0) == L.qg_skinny_workspace_size(M, N, K, 64)
+    for T, H, I, E, k in ((1, 7168, 2048, 384, 16), (16, 512, 256, 8, 2)):
+        assert L.qg_workspace_size(q.OP_MOE_MXFP4, 0, H, I, T, E, k) == L.qg_moe_workspace_size(T, H, I, E, k) > 0
+    assert L.qg_workspace_size(q.OP_W8A8_HADAMARD, 16, 0, 4096, 0, 0, 0) == \
+        L.qg_w8a8_hadamard_workspace_size(16, 4096) > 0
+    assert L.qg_workspace_size(q.OP_HADAMARD_I8, 16, 0, 4096, 0, 0, 0) == 0
+    assert L.qg_workspace_size(q.OP_W8A8_I32, 16, 4096, 4096, 0, 0, 0) == 0
+    assert L.qg_workspace_size(99, 16, 4096, 4096, 1, 8, 2) == 0
+
+
 def test_w4a16_validation(L):
     f = L.qgemv_w4a16
     assert f(None, P(A), P(A), P(A), P(A), 16, 128, 64, None, 0, None) == 1
