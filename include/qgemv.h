@@ -97,7 +97,8 @@ QG_API int qg_version(void);
  *   group_size 32, 64 or 128 (other values: QG_ERR_INVALID_ARG). 64 runs on the
  *              fast kernels; 32 and 128 (the other group sizes of the affine
  *              format, "MLX Runner ...") run on the chunked kernel of
- *              qgemm_affine (one warp per row, 32-code chunks per lane).
+ *              qgemm_affine (one warp per row, 32-code chunks per lane; with
+ *              more than 4 rows on qgemm_w4a16_skinny, one code per lane).
  *   K          multiple of group_size; N >= 1.
  *   workspace  may be NULL when ws_bytes == 0; qg_gemv_workspace_size()
  *              gives the size needed (currently 0 for every shape).
@@ -343,8 +344,10 @@ QG_API void qgemm_w4a16_skinny_group_destroy(qg_w4_skinny_group *group);
  *              y[m][n] = sum_k (s * q[n][k] + b) * x[m][k].
  *   M 1..32; N >= 1; K a multiple of 32 and of group_size, at most 2^20;
  *   group_size 32, 64 or 128. Every pointer 16-byte aligned.
- * A generic kernel (one warp per output row, correct, not tuned); 4-bit g64
- * projections have the fast entry points above.
+ * One warp per output row. Up to 4 rows: 32-code chunks per lane (at 2, 4 and
+ * 8 bits codes turned into fp16 two at a time; the chunk sums of x once per
+ * CTA); more rows: one code per lane (correct, not tuned). 4-bit g64
+ * projections have the fast entry points above. Results are deterministic.
  * Errors: QG_ERR_INVALID_ARG, QG_ERR_MISALIGNED.
  */
 QG_API qg_status qgemm_affine(const uint32_t *wq, int bits, const uint16_t *scales_f16,
