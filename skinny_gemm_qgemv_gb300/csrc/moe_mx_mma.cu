@@ -625,21 +625,21 @@ struct DnLane {
 
 // from the shared table: token columns, [nvmax][8 NT] pair of (virtual
 // expert, token) or -1; pair columns, [nvmax][8] pairs of the virtual expert
-// or -1
+// with their tokens, token << 10 | pair (T, top_k <= 32), or -1
 template <int NT, bool PC>
 __device__ __forceinline__ void dn_lane(const MxDnArgs& a, int v, int g, int c, const int16_t* tab, DnLane<NT>& L) {
   L.act = 0u;
   const int P = a.T * a.top_k;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const int pair = tab[v * 8 * NT + 8 * nt + g];
-    L.hp[nt] = a.hh + (size_t)(pair >= 0 ? pair : P) * a.I;
-    if (PC || __any_sync(kFull, pair >= 0)) L.act |= 1u << nt;
+    const int e = tab[v * 8 * NT + 8 * nt + g];
+    const int pair = PC ? e & 1023 : e;
+    L.hp[nt] = a.hh + (size_t)(e >= 0 ? pair : P) * a.I;
+    if (PC || __any_sync(kFull, e >= 0)) L.act |= 1u << nt;
   }
-  if (PC) {
-    const int p0 = tab[v * 8 + 2 * c], p1 = tab[v * 8 + 2 * c + 1];
-    L.tk0 = p0 >= 0 ? p0 / a.top_k : -1;
-    L.tk1 = p1 >= 0 ? p1 / a.top_k : -1;
+  if (PC) {  // -1 >> 10 is -1: no token
+    L.tk0 = tab[v * 8 + 2 * c] >> 10;
+    L.tk1 = tab[v * 8 + 2 * c + 1] >> 10;
   }
 }
 
@@ -715,7 +715,10 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     const int v2 = q / kMxTC, j = q - v2 * kMxTC;
     if (j < vt[v2 * kVt + 1]) {
       const int pair = vt[v2 * kVt + 2 + j];
-      tab[v2 * 8 * NT + (PC ? j : pair / a.top_k)] = (int16_t)pair;
+      if (PC)
+        tab[v2 * 8 + j] = (int16_t)((pair / a.top_k) << 10 | pair);
+      else
+        tab[v2 * 8 * NT + pair / a.top_k] = (int16_t)pair;
     }
   }
   if (PC)
