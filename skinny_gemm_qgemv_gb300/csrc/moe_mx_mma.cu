@@ -298,7 +298,9 @@ __global__ void __launch_bounds__(kRouteThreads) moe_mx_route_mma_kernel(
 // (T <= 32): the pairs (token, slot) of every expert in token order, cut into
 // runs of at most kMxTC pairs (the N = 8 columns of one MMA), experts in index
 // order. Table entry v: {expert, pair count, kMxTC pairs (-1 padded)} as
-// int16. Every thread of the CTA calls it; returns the number of entries.
+// int16, a pair p of token t stored as t << 10 | p (T, top_k <= 32, so p <
+// 1024 and t < 32). Every thread of the CTA calls it; returns the number of
+// entries.
 // Scratch: 3 E words of shared memory.
 constexpr int kVt = 2 + kMxTC;  // int16 per table entry
 __device__ int mx_group(const int32_t* __restrict__ idx, int T, int E, int top_k, int* cnt, uint32_t* msk,
@@ -334,7 +336,7 @@ __device__ int mx_group(const int32_t* __restrict__ idx, int T, int E, int top_k
     const int r = __popc(msk[e] & ((1u << t) - 1u));  // earlier tokens with this expert
     int16_t* ent = vt + (voff[e] + r / kMxTC) * kVt;
     const int j = r % kMxTC;
-    ent[2 + j] = (int16_t)p;
+    ent[2 + j] = (int16_t)(t << 10 | p);
     if (j == 0) {
       ent[0] = (int16_t)e;
       ent[1] = (int16_t)min(kMxTC, cnt[e] - r);
@@ -363,7 +365,7 @@ struct MxGuArgs {
 __device__ __forceinline__ const uint16_t* gu_xrow(const MxGuArgs& a, const int16_t* vt, int tile, int tpv, int g) {
   const int16_t* ent = vt + (tile / tpv) * kVt;
   const int j = min(g, ent[1] - 1);
-  return a.xh + (size_t)(ent[2 + j] / a.top_k) * a.H;
+  return a.xh + (size_t)(ent[2 + j] >> 10) * a.H;
 }
 
 // BPW: 32-k blocks per warp and stage (a stage is 512 BPW k of the tile's rows)
@@ -455,8 +457,9 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     const uint16_t* xnext = tile + 1 < t1 ? gu_xrow(a, vt, tile + 1, tpv, g) : xrow;
     // this thread's epilogue column (pair) and its 2^sigma, fetched early
     const int ecol = 2 * (et & 3) + ((et >> 5) & 1);
-    const int epair = ecol < np ? ent[2 + ecol] : 0;
-    const float esc = pow2f(__ldg(a.xexp + epair / a.top_k));
+    const int eent = ecol < np ? ent[2 + ecol] : 0;
+    const int epair = eent & 1023;
+    const float esc = pow2f(__ldg(a.xexp + (eent >> 10)));
     float acc[4][4];
 #pragma unroll
     for (int mt = 0; mt < 4; ++mt)
@@ -714,11 +717,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   for (int q = threadIdx.x; q < nv * kMxTC; q += blockDim.x) {
     const int v2 = q / kMxTC, j = q - v2 * kMxTC;
     if (j < vt[v2 * kVt + 1]) {
-      const int pair = vt[v2 * kVt + 2 + j];
+      const int16_t ent = vt[v2 * kVt + 2 + j];  // token << 10 | pair
       if (PC)
-        tab[v2 * 8 + j] = (int16_t)((pair / a.top_k) << 10 | pair);
+        tab[v2 * 8 + j] = ent;
       else
-        tab[v2 * 8 * NT + pair / a.top_k] = (int16_t)pair;
+        tab[v2 * 8 * NT + (ent >> 10)] = (int16_t)(ent & 1023);
     }
   }
   if (PC)
